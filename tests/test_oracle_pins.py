@@ -1,0 +1,384 @@
+"""Pins for the CPU oracle: each test ties it to something other than itself.
+
+Sources of truth used here:
+  * a hand-worked example (tests/golden/tree_example.json) derived from the
+    tree-causal mask of the JETFLOW summary (§2 "Arquitectura Central");
+  * library routines: networkx ancestry, torch scaled_dot_product_attention
+    (fp64, CPU), scipy logsumexp, numpy argmax;
+  * closed forms and special cases (zero query, chain tree = causal
+    attention, single node = decode attention, star tree);
+  * invariances the mask semantics imply (sibling relabelling, physical page
+    placement) and brute-force path enumeration on every small tree.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "tree_example.json")
+
+
+def _bits(mask_row):
+    return {w * 32 + b for w, word in enumerate(mask_row) for b in range(32) if (int(word) >> b) & 1}
+
+
+def _random_trees(rng, B, n):
+    out = []
+    for k in range(n):
+        if k % 3 == 0:
+            out.append(wl.tree_window(rng, B, window=int(rng.integers(1, 6))))
+        elif k % 3 == 1:
+            out.append(wl.tree_best_first(rng, B, child_cap=int(rng.integers(1, 5)), max_depth=B))
+        else:
+            p = np.array([-1] + [int(rng.integers(0, i)) for i in range(1, B)], dtype=np.int32)
+            out.append(p)
+    return out
+
+
+def _small_workload(seed, nb, B, Hq, Hkv, D, prefix, shuffle=True, trees=None):
+    rng = np.random.default_rng(seed)
+    if trees is None:
+        trees = _random_trees(rng, B, nb)
+    return wl.make_workload("pin", nb, B, Hq, Hkv, D, 64, prefix, trees, seed,
+                            shuffle_pages=shuffle, extra_pages=3, with_logits=False)
+
+
+def _f64(u16):
+    return wl.bf16_to_f32(u16).astype(np.float64)
+
+
+# ------------------------------------------------------------------------ mask
+
+def test_mask_golden_example():
+    fx = json.load(open(GOLDEN))["tree"]
+    mask, depth = oracle.build_mask(np.array([fx["parent"]], dtype=np.int32))
+    assert mask[0, :, 0].tolist() == fx["mask_words"]
+    assert depth[0].tolist() == fx["depth"]
+
+
+@pytest.mark.parametrize("B", [1, 2, 31, 32, 33, 64, 100, 255, 256])
+def test_mask_matches_networkx_ancestry(B):
+    nx = pytest.importorskip("networkx")
+    rng = np.random.default_rng(B)
+    trees = _random_trees(rng, B, 3)
+    mask, depth = oracle.build_mask(np.stack(trees))
+    for t, p in enumerate(trees):
+        g = nx.DiGraph()
+        g.add_nodes_from(range(B))
+        g.add_edges_from((int(p[i]), i) for i in range(1, B))
+        lengths = nx.single_source_shortest_path_length(g, 0)
+        for i in range(B):
+            assert _bits(mask[t, i]) == nx.ancestors(g, i) | {i}
+            assert depth[t, i] == lengths[i]
+
+
+def test_mask_invariants():
+    rng = np.random.default_rng(7)
+    trees = _random_trees(rng, 200, 6)
+    mask, depth = oracle.build_mask(np.stack(trees))
+    for t in range(len(trees)):
+        sets = [_bits(mask[t, i]) for i in range(200)]
+        for i, s in enumerate(sets):
+            assert len(s) == depth[t, i] + 1
+            assert 0 in s and i in s and max(s) == i
+            for j in s:
+                assert sets[j] <= s
+        # unused high bits of the last word stay clear
+        assert all(max(_bits(mask[t, i])) < 200 for i in range(200))
+
+
+@pytest.mark.parametrize("bad", [[0, 0, 1], [-1, 1, 0], [-1, 0, -1], [-1, 0, 5], [-1, 0, 2]])
+def test_mask_rejects_non_topological(bad):
+    with pytest.raises(oracle.OracleError):
+        oracle.build_mask(np.array([bad], dtype=np.int32))
+
+
+# ------------------------------------------------------------------- attention
+
+def test_attention_golden_example():
+    fx = json.load(open(GOLDEN))["attention"]
+    q = wl.f32_to_bf16(np.array(fx["q"], dtype=np.float32)).reshape(3, 1, 2)
+    kc = np.zeros((1, 1, 16, 2), dtype=np.uint16)
+    vc = np.zeros((1, 1, 16, 2), dtype=np.uint16)
+    kc[0, 0, :4] = wl.f32_to_bf16(np.array(fx["k_logical"], dtype=np.float32))
+    vc[0, 0, :4] = wl.f32_to_bf16(np.array(fx["v_logical"], dtype=np.float32))
+    O, L = oracle.attn(q, kc, vc, np.array([[0]], np.int32), np.array([fx["prefix_len"]], np.int32),
+                       np.array([fx["parent"]], np.int32), 1, 1, scale=fx["scale"])
+    np.testing.assert_allclose(O[:, 0, :], np.array(fx["O"]), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(L[:, 0], np.array(fx["LSE"]), rtol=0, atol=1e-12)
+
+
+def _sdpa_last_row(qv, K, Vv, scale):
+    """Library pin: torch SDPA (fp64, CPU), one query attending to all given keys."""
+    qt = torch.from_numpy(qv)[None, None, None, :]
+    kt = torch.from_numpy(K)[None, None]
+    vt = torch.from_numpy(Vv)[None, None]
+    return torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=scale)[0, 0, 0].numpy()
+
+
+@pytest.mark.parametrize("G,D,P", [(1, 8, 0), (2, 16, 17), (4, 16, 40), (4, 8, 33)])
+def test_attention_each_node_equals_attention_over_its_root_path(G, D, P):
+    """Per-branch factorisation: row i = last row of causal attention over prefix ++ path(i)."""
+    nx = pytest.importorskip("networkx")
+    from scipy.special import logsumexp
+    Hkv = 2
+    Hq = Hkv * G
+    w = _small_workload(100 + G + D + P, nb=2, B=8, Hq=Hq, Hkv=Hkv, D=D, prefix=[P, P + 5])
+    O, L = oracle.attn_workload(w)
+    scale = 1.0 / math.sqrt(D)
+    for b in range(w.nb):
+        Kl = _f64(wl.logical_kv(w, b, "k"))
+        Vl = _f64(wl.logical_kv(w, b, "v"))
+        Pb = int(w.prefix_lens[b])
+        g = nx.DiGraph()
+        g.add_edges_from((int(w.parent[b, i]), i) for i in range(1, w.B))
+        g.add_node(0)
+        for i in range(w.B):
+            path = nx.shortest_path(g, 0, i)
+            keys = list(range(Pb)) + [Pb + t for t in path]
+            for h in range(Hq):
+                kvh = h // G
+                qv = _f64(w.q[b * w.B + i, h])
+                ref = _sdpa_last_row(qv, Kl[keys, kvh], Vl[keys, kvh], scale)
+                np.testing.assert_allclose(O[b * w.B + i, h], ref, rtol=0, atol=1e-12)
+                lse = logsumexp(scale * (Kl[keys, kvh] @ qv))
+                assert abs(L[b * w.B + i, h] - lse) < 1e-12
+
+
+def test_attention_chain_tree_equals_causal_attention():
+    """A chain-shaped tree is ordinary causal attention over prefix ++ chain."""
+    B, P, Hq, Hkv, D = 12, 37, 4, 2, 16
+    chain = np.arange(-1, B - 1, dtype=np.int32)
+    w = _small_workload(5, nb=1, B=B, Hq=Hq, Hkv=Hkv, D=D, prefix=[P], trees=[chain])
+    O, _ = oracle.attn_workload(w)
+    K = torch.from_numpy(_f64(wl.logical_kv(w, 0, "k"))).permute(1, 0, 2)   # [Hkv][P+B][D]
+    Vv = torch.from_numpy(_f64(wl.logical_kv(w, 0, "v"))).permute(1, 0, 2)
+    K = K.repeat_interleave(Hq // Hkv, dim=0)
+    Vv = Vv.repeat_interleave(Hq // Hkv, dim=0)
+    q = torch.from_numpy(_f64(w.q)).permute(1, 0, 2)                      # [Hq][B][D]
+    allowed = torch.ones(B, P + B, dtype=torch.bool).tril(diagonal=P)     # row i sees keys <= P+i
+    ref = torch.nn.functional.scaled_dot_product_attention(q, K, Vv, attn_mask=allowed)
+    np.testing.assert_allclose(O, ref.permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
+
+
+def test_attention_single_node_is_decode_attention():
+    w = _small_workload(9, nb=3, B=1, Hq=8, Hkv=2, D=16, prefix=[0, 5, 48])
+    O, _ = oracle.attn_workload(w)
+    for b in range(3):
+        K = _f64(wl.logical_kv(w, b, "k"))
+        Vv = _f64(wl.logical_kv(w, b, "v"))
+        for h in range(8):
+            ref = _sdpa_last_row(_f64(w.q[b, h]), K[:, h // 4], Vv[:, h // 4], 0.25)
+            np.testing.assert_allclose(O[b, h], ref, rtol=0, atol=1e-12)
+
+
+def test_attention_zero_query_closed_form():
+    """q = 0 makes every visible score 0: O = mean of the visible V rows, LSE = ln(#visible)."""
+    rng = np.random.default_rng(3)
+    B, P = 9, 21
+    trees = _random_trees(rng, B, 2)
+    w = _small_workload(11, nb=2, B=B, Hq=2, Hkv=1, D=8, prefix=[P, 0], trees=trees)
+    w.q[:] = 0
+    O, L = oracle.attn_workload(w)
+    for b in range(2):
+        Pb = int(w.prefix_lens[b])
+        Vl = _f64(wl.logical_kv(w, b, "v"))
+        for i in range(B):
+            path = [i]
+            while path[-1] != 0:
+                path.append(int(w.parent[b, path[-1]]))
+            rows = list(range(Pb)) + [Pb + t for t in path]
+            np.testing.assert_allclose(O[b * B + i, :, :], np.broadcast_to(Vl[rows, 0].mean(0), (2, 8)),
+                                       rtol=0, atol=1e-12)
+            np.testing.assert_allclose(L[b * B + i], math.log(len(rows)), rtol=0, atol=1e-12)
+
+
+def test_attention_star_tree_sees_prefix_root_and_self():
+    B, P = 6, 19
+    star = np.array([-1] + [0] * (B - 1), dtype=np.int32)
+    w = _small_workload(12, nb=1, B=B, Hq=2, Hkv=2, D=8, prefix=[P], trees=[star])
+    O, _ = oracle.attn_workload(w)
+    K = _f64(wl.logical_kv(w, 0, "k"))
+    Vv = _f64(wl.logical_kv(w, 0, "v"))
+    for i in range(B):
+        rows = list(range(P + 1)) + ([P + i] if i else [])
+        for h in range(2):
+            ref = _sdpa_last_row(_f64(w.q[i, h]), K[rows, h], Vv[rows, h], 1 / math.sqrt(8))
+            np.testing.assert_allclose(O[i, h], ref, rtol=0, atol=1e-12)
+
+
+def _random_topological_relabel(rng, parent):
+    """A node relabelling that keeps every parent before its children (random sibling order)."""
+    B = len(parent)
+    children = [[] for _ in range(B)]
+    for i in range(1, B):
+        children[parent[i]].append(i)
+    order, frontier = [], [0]
+    while frontier:
+        k = int(rng.integers(0, len(frontier)))
+        n = frontier.pop(k)
+        order.append(n)
+        frontier.extend(children[n])
+    new_of_old = np.empty(B, dtype=np.int64)
+    new_of_old[np.array(order)] = np.arange(B)
+    new_parent = np.full(B, -1, dtype=np.int32)
+    for old in range(1, B):
+        new_parent[new_of_old[old]] = new_of_old[parent[old]]
+    return new_of_old, new_parent
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_attention_invariant_under_sibling_relabelling(seed):
+    rng = np.random.default_rng(seed)
+    B, P, Hq, Hkv, D = 10, 23, 4, 2, 8
+    w = _small_workload(20 + seed, nb=1, B=B, Hq=Hq, Hkv=Hkv, D=D, prefix=[P])
+    O, L = oracle.attn_workload(w)
+    nmap, npar = _random_topological_relabel(rng, w.parent[0])
+    assert (npar[1:] < np.arange(1, B)).all()
+    w2 = _small_workload(20 + seed, nb=1, B=B, Hq=Hq, Hkv=Hkv, D=D, prefix=[P], trees=[npar])
+    # same data, relabelled: q rows and the tree slots of the cache move with the nodes
+    w2.q[nmap] = w.q
+    w2.k_cache[:] = w.k_cache
+    w2.v_cache[:] = w.v_cache
+    w2.block_table[:] = w.block_table
+    for old in range(B):
+        for cache, cache2 in ((w.k_cache, w2.k_cache), (w.v_cache, w2.v_cache)):
+            po, pn = P + old, P + int(nmap[old])
+            cache2[w.block_table[0, pn // 16], :, pn % 16] = cache[w.block_table[0, po // 16], :, po % 16]
+    O2, L2 = oracle.attn_workload(w2)
+    np.testing.assert_allclose(O2[nmap], O, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(L2[nmap], L, rtol=0, atol=1e-12)
+
+
+def test_attention_independent_of_physical_page_placement():
+    w1 = _small_workload(31, nb=3, B=7, Hq=4, Hkv=2, D=8, prefix=[40, 3, 70], shuffle=False)
+    w2 = _small_workload(31, nb=3, B=7, Hq=4, Hkv=2, D=8, prefix=[40, 3, 70], shuffle=True)
+    # place w1's logical rows into w2's (shuffled) pages
+    for b in range(3):
+        for which in ("k", "v"):
+            src = wl.logical_kv(w1, b, which)
+            cache = w2.k_cache if which == "k" else w2.v_cache
+            pos = np.arange(src.shape[0])
+            cache[w2.block_table[b, pos // 16], :, pos % 16, :] = src
+    w2.q[:] = w1.q
+    w2.parent[:] = w1.parent
+    O1, L1 = oracle.attn_workload(w1)
+    O2, L2 = oracle.attn_workload(w2)
+    assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
+
+
+def test_attention_key_ranges_merge_to_the_whole():
+    w = _small_workload(41, nb=2, B=9, Hq=4, Hkv=2, D=16, prefix=[50, 130])
+    O, L = oracle.attn_workload(w)
+    for cuts in ([0, 16, -1], [0, 7, 64, 128, -1], [0, 55, 56, 131, 135, -1]):
+        parts = []
+        for lo, hi in zip(cuts[:-1], cuts[1:]):
+            parts.append(oracle.attn_workload(w, key_range=(lo, hi)))
+        Om, Lm = oracle.lse_merge(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+        np.testing.assert_allclose(Om, O, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(Lm, L, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------- argmax
+
+def test_argmax_matches_numpy_first_occurrence():
+    rng = np.random.default_rng(5)
+    for V in (1, 2, 7, 1000, 4099):
+        vals = rng.integers(-3, 4, size=(20, V)).astype(np.float32) * np.float32(0.5)  # many ties
+        u = wl.f32_to_bf16(vals)
+        assert np.array_equal(oracle.argmax(u), np.argmax(wl.bf16_to_f32(u), axis=1))
+        x = wl.f32_to_bf16(rng.standard_normal((5, V), dtype=np.float32))
+        assert np.array_equal(oracle.argmax(x), np.argmax(wl.bf16_to_f32(x), axis=1))
+
+
+def test_argmax_signed_zero_and_nan():
+    rows = np.array([[0x8000, 0x0000, 0xBF80],        # -0, +0, -1  -> first zero (index 0)
+                     [0x3F80, 0x7FC0, 0x7F80],        # 1, NaN, +inf -> NaN counts as the max
+                     [0xFF80, 0xFF80, 0xFF80],        # all -inf -> 0
+                     [0x3F80, 0x7F80, 0xFFC1]],       # 1, +inf, -NaN -> the NaN
+                    dtype=np.uint16)
+    ref = torch.argmax(torch.from_numpy(wl.bf16_to_f32(rows)), dim=1).numpy()
+    assert oracle.argmax(rows).tolist() == ref.tolist() == [0, 1, 0, 2]
+
+
+# ------------------------------------------------------------------ acceptance
+
+def test_accept_golden_example():
+    fx = json.load(open(GOLDEN))
+    parent = np.array([fx["tree"]["parent"]], dtype=np.int32)
+    a = fx["accept"]
+    logits = wl.f32_to_bf16(np.array(a["logits"], dtype=np.float32))
+    for case in a["cases"]:
+        am, n_acc, path, bonus = oracle.accept(logits, np.array([case["draft"]], np.int32), parent)
+        assert am.tolist() == a["argmax"]
+        assert n_acc[0] == case["n_acc"] and bonus[0] == case["bonus"]
+        assert path[0].tolist() == case["path"]
+
+
+def _brute_accept(parent, draft, am):
+    """Enumerate every root-to-node path by DFS over child lists; keep the deepest fully matching one."""
+    B = len(parent)
+    children = [[] for _ in range(B)]
+    for i in range(1, B):
+        children[parent[i]].append(i)
+    best = (0, 0, [0])                       # (length, -index, path)
+    stack = [[0]]
+    while stack:
+        path = stack.pop()
+        v = path[-1]
+        key = (len(path) - 1, -v)
+        if key > best[:2]:
+            best = (len(path) - 1, -v, path)
+        for c in children[v]:
+            if draft[c] == am[v]:
+                stack.append(path + [c])
+    return best[0], best[2]
+
+
+def _all_trees(B):
+    return itertools.product(*[range(i) for i in range(1, B)])
+
+
+@pytest.mark.parametrize("B", [1, 2, 3, 4, 5, 6, 7])
+def test_accept_matches_exhaustive_path_enumeration(B):
+    rng = np.random.default_rng(B)
+    V = 3
+    trees = [np.array((-1,) + t, dtype=np.int32) for t in _all_trees(B)]
+    for parent in trees:
+        for _ in range(2):
+            logits = wl.f32_to_bf16(rng.integers(0, 3, size=(B, V)).astype(np.float32))
+            draft = rng.integers(0, V, size=B).astype(np.int32)
+            am, n_acc, path, bonus = oracle.accept(logits, draft, parent)
+            am_ref = np.argmax(wl.bf16_to_f32(logits), axis=1)
+            assert np.array_equal(am, am_ref)
+            depth, p = _brute_accept(parent, draft, am_ref)
+            assert n_acc[0] == depth
+            assert path[0, :depth + 1].tolist() == p and (path[0, depth + 1:] == -1).all()
+            assert bonus[0] == am_ref[p[-1]]
+
+
+def test_accept_closed_forms():
+    B, V = 9, 11
+    chain = np.arange(-1, B - 1, dtype=np.int32)
+    rng = np.random.default_rng(0)
+    logits = wl.f32_to_bf16(rng.standard_normal((B, V), dtype=np.float32))
+    am = np.argmax(wl.bf16_to_f32(logits), axis=1)
+    draft = np.zeros(B, np.int32)
+    draft[1:] = am[:-1]                                  # every draft matches: all accepted
+    _, n_acc, path, bonus = oracle.accept(logits, draft, chain)
+    assert n_acc[0] == B - 1 and path[0].tolist() == list(range(B)) and bonus[0] == am[-1]
+    draft[1:] = (am[:-1] + 1) % V                        # nothing matches: root only
+    _, n_acc, path, bonus = oracle.accept(logits, draft, chain)
+    assert n_acc[0] == 0 and path[0].tolist() == [0] + [-1] * (B - 1) and bonus[0] == am[0]
+
+
+def test_accept_rejects_non_topological():
+    with pytest.raises(oracle.OracleError):
+        oracle.accept(np.zeros((3, 4), np.uint16), np.zeros(3, np.int32), np.array([-1, 2, 0], np.int32))
