@@ -1,0 +1,167 @@
+/*
+ * libtreeverify — the verify step of tree speculative decoding on one GB300
+ * (sm_103a): ancestor masks, tree-causal paged attention, vocab argmax and
+ * greedy tree acceptance.
+ *
+ * Sources (page title, section):
+ *   [JF-2]  JETFLOW technical summary, §2 "Arquitectura Central": tree-causal
+ *           attention mask — a draft-tree node attends to the input prefix and
+ *           to its ancestors in the tree, never to descendants or to unrelated
+ *           sibling branches (per-branch factorisation
+ *           q(pi(v)|x) = prod_{u in pi(v)} q(y_u | x, h, pi_<u)).
+ *   [JF-3]  JETFLOW summary, §3 "Contribuciones Clave" item 3: verification
+ *           runs as paged FlashAttention with the tree mask staged in.
+ *   [TfM-P] DFlash-TfM summary, "Declaración del Problema" item 3: standard
+ *           tree verification = one target pass with ancestor-restricted
+ *           masking.
+ *   [TfM-3] DFlash-TfM summary, §3 "Solución": the tree is topologically
+ *           ordered (parents before children).
+ *   [JF-4]  JETFLOW summary, §3 item 2 and §4: accepted tokens (tau) and
+ *           longer accepted prefixes; the pages give no acceptance rule, so
+ *           the greedy rule below is this library's reading.
+ *
+ * Conventions for every entry point
+ *   - All pointers with a _d meaning are DEVICE pointers on the current
+ *     device; the caller allocates and owns every buffer.  The library
+ *     allocates no device memory, keeps no pointer after a call returns and
+ *     holds no state (it encodes TMA descriptors on every call).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call only enqueues work on `stream` and returns; results
+ *     are ready when the stream reaches that point.
+ *   - Host-detectable problems (null pointers, sizes, alignment, unsupported
+ *     shapes, workspace too small) are returned synchronously as a tv_status
+ *     and nothing is enqueued.  Data-dependent problems found on the device
+ *     (bad parent array, prefix too long for the block table, block id out of
+ *     range, an internal wait that ran out) are written to *dev_status_d (a
+ *     device int32 the caller zeroes beforehand; the first error code wins)
+ *     and the affected outputs are unspecified.  Kernels never trap.
+ *   - bf16 tensors are passed as raw 16-bit patterns.
+ *   - Shape limits: 1 <= B <= 256, head dim D = 128, page size 16,
+ *     Hq/Hkv = G in {1,2,4,8,16}.  Anything else returns
+ *     TV_ERR_UNSUPPORTED_SHAPE; there is no fallback path.
+ */
+#ifndef TREEVERIFY_H
+#define TREEVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TV_API __attribute__((visibility("default")))
+#else
+#define TV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum tv_status {
+    TV_OK = 0,
+    TV_ERR_INVALID_ARG = 1,       /* null pointer, bad size, misalignment, bad block id / prefix */
+    TV_ERR_NOT_TOPOLOGICAL = 2,   /* parent[0] != -1 or parent[i] not in [0, i) */
+    TV_ERR_UNSUPPORTED_SHAPE = 3, /* outside the supported shape set above */
+    TV_ERR_CUDA = 4,              /* a CUDA runtime/driver call failed */
+    TV_ERR_TIMEOUT = 5,           /* a bounded device-side wait ran out (device status only) */
+    TV_ERR_UNIMPLEMENTED = 6
+} tv_status;
+
+/* Human-readable name of a status code (static storage). */
+TV_API const char *tv_status_str(int32_t status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+TV_API int32_t tv_version(void);
+
+/*
+ * a1 — ancestor masks  [JF-2], [TfM-P], [TfM-3]
+ *
+ *   mask[b][i][w] bit j (j = 32*w + bit, LSB first) is 1 iff node j is node i
+ *   or one of its ancestors:  anc[0] = {0},  anc[i] = anc[parent[i]] U {i}.
+ *   depth[b][i] = number of edges from the root to node i.
+ *
+ *   parent_d  int32 [nb][B]    parent[b][0] = -1, 0 <= parent[b][i] < i
+ *   mask_d    uint32 [nb][B][W], W = ceil(B/32)   (out; bits >= B are 0)
+ *   depth_d   int32 [nb][B]    (out, may be NULL)
+ *   dev_status_d  int32 device word (may be NULL); TV_ERR_NOT_TOPOLOGICAL is
+ *                 written there when a parent array is invalid
+ * Returns TV_OK, TV_ERR_INVALID_ARG (null mask/parent, nb < 0),
+ * TV_ERR_UNSUPPORTED_SHAPE (B outside [1,256]) or TV_ERR_CUDA.
+ */
+TV_API int32_t tv_build_mask(const int32_t *parent_d, int32_t B, int32_t nb, uint32_t *mask_d,
+                      int32_t *depth_d, int32_t *dev_status_d, void *stream);
+
+/*
+ * a2 + a3 — tree-causal paged attention with split-KV merge
+ * [JF-2], [JF-3], [TfM-P]
+ *
+ * For every sequence b, node i, query head h (kv head g = h / G):
+ *   keys  j in [0, P_b)  U  { P_b + t : t in anc[i] }
+ *   s_j   = scale * <q[b,i,h], K[b,g,j]>
+ *   O     = sum_j softmax(s)_j V[b,g,j]       (bf16 out, fp32 accumulation)
+ *   LSE   = ln sum_j exp(s_j)                  (fp32 out)
+ * Logical position p of sequence b lives in physical page
+ * block_table[b][p / 16], slot p % 16.  The caller has already written the
+ * tree nodes' K/V at positions [P_b, P_b + B) (node t at P_b + t) and applied
+ * RoPE (position P_b + depth[i] is the natural choice; tv_build_mask returns
+ * depth).  Cache slots past P_b + B inside the last page must hold finite
+ * values (zero-initialised caches satisfy this): they are multiplied by zero
+ * probabilities.
+ */
+typedef struct tv_attn_args {
+    const void *q_d;             /* bf16 [nb*B][Hq][D], 16-byte aligned */
+    const void *k_cache_d;       /* bf16 [num_blocks][Hkv][page_size][D], 16-byte aligned */
+    const void *v_cache_d;       /* same layout as k_cache_d */
+    const int32_t *block_table_d;/* int32 [nb][max_pages]; must cover P_b + B positions */
+    const int32_t *prefix_lens_d;/* int32 [nb], P_b >= 0 (committed prefix, tree excluded) */
+    const uint32_t *mask_d;      /* uint32 [nb][B][ceil(B/32)] from tv_build_mask */
+    void *o_d;                   /* bf16 [nb*B][Hq][D] (out), 16-byte aligned */
+    float *lse_d;                /* fp32 [nb*B][Hq] (out), natural log */
+    int32_t *dev_status_d;       /* device status word, may be NULL */
+    int32_t nb, B, Hq, Hkv, D, page_size, num_blocks, max_pages;
+    float scale;                 /* <= 0 selects 1/sqrt(D) */
+    int32_t num_ctas;            /* 0 = one CTA per SM; otherwise the CTA count to use */
+} tv_attn_args;
+
+/* Bytes of device workspace tv_attn needs for these arguments (depends on
+ * num_ctas and the device's SM count; 0 never happens).  Returns 0 when the
+ * arguments are invalid. */
+TV_API size_t tv_attn_workspace_size(const tv_attn_args *args);
+
+/* Enqueue the attention.  workspace_d: device buffer of at least
+ * tv_attn_workspace_size(args) bytes, 256-byte aligned, contents ignored on
+ * entry (it carries split-KV partial results between the two kernels of one
+ * call, so concurrent calls need separate workspaces).
+ * Returns TV_OK, TV_ERR_INVALID_ARG, TV_ERR_UNSUPPORTED_SHAPE or TV_ERR_CUDA.
+ * nb == 0 is a no-op. */
+TV_API int32_t tv_attn(const tv_attn_args *args, void *workspace_d, size_t workspace_bytes, void *stream);
+
+/*
+ * a4 + a5 — vocab argmax and greedy acceptance  [JF-4] (rule: this library's reading)
+ *
+ *   argmax[b*B+i] = first index of the maximum of logits[b*B+i][0..V)
+ *                   (values compared as numbers, -0 == +0; a NaN counts as the maximum)
+ *   ok[i]  = draft_tokens[b][i] == argmax[b*B + parent[b][i]]      (i >= 1)
+ *   acc[i] = ok[j] for every j in anc[i] \ {0}                        (node 0 always accepted)
+ *   v*     = the accepted node of greatest depth, smallest index on ties
+ *   n_acc[b]   = depth[v*]  (accepted draft tokens, root excluded)
+ *   path[b][k] = k-th node on the root-to-v* path (path[b][0] = 0), -1 after n_acc
+ *   bonus[b]   = argmax[b*B + v*]  (the target's next token after the accepted path)
+ *
+ *   logits_d       bf16 [nb*B][V], 2-byte aligned (any V >= 1)
+ *   draft_tokens_d int32 [nb][B]  (entry 0 of each sequence is ignored)
+ *   parent_d       int32 [nb][B]  (the array given to tv_build_mask)
+ *   mask_d         uint32 [nb][B][ceil(B/32)] from tv_build_mask for the same parent
+ *   argmax_d       int32 [nb*B] (out), n_acc_d int32 [nb], path_d int32 [nb][B],
+ *   bonus_d        int32 [nb] (out)
+ * Returns TV_OK, TV_ERR_INVALID_ARG, TV_ERR_UNSUPPORTED_SHAPE or TV_ERR_CUDA.
+ */
+TV_API int32_t tv_accept(const uint16_t *logits_d, int32_t V, const int32_t *draft_tokens_d,
+                  const int32_t *parent_d, const uint32_t *mask_d, int32_t B, int32_t nb,
+                  int32_t *argmax_d, int32_t *n_acc_d, int32_t *path_d, int32_t *bonus_d,
+                  int32_t *dev_status_d, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TREEVERIFY_H */

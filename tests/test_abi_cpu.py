@@ -1,0 +1,111 @@
+"""The C ABI without a GPU: the library loads, exports every declared entry
+point, and rejects bad arguments on the host before touching a device."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import tree_speculative_decoding_tv_gb300 as tv
+from tree_speculative_decoding_tv_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "treeverify.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from tree_speculative_decoding_tv_gb300 import build
+    build.build()
+    return tv.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"TV_API\s+[\w\s\*]*?\b(tv_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    assert declared_symbols() == sorted(binding.EXPORTED)
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_symbols():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    names = [tv.status_str(i) for i in range(7)]
+    assert names == ["TV_OK", "TV_ERR_INVALID_ARG", "TV_ERR_NOT_TOPOLOGICAL", "TV_ERR_UNSUPPORTED_SHAPE",
+                     "TV_ERR_CUDA", "TV_ERR_TIMEOUT", "TV_ERR_UNIMPLEMENTED"]
+    assert tv.status_str(99) == "TV_ERR_UNKNOWN"
+    assert L.tv_version() == 100
+
+
+FAKE = 0x10000  # an aligned non-null address that is never dereferenced: every case below fails validation first
+
+
+def test_build_mask_argument_checks(L):
+    P = C.c_void_p
+    assert L.tv_build_mask(P(FAKE), 16, 0, P(FAKE), None, None, None) == 0        # nb = 0: nothing to do
+    assert L.tv_build_mask(P(FAKE), 0, 1, P(FAKE), None, None, None) == 3         # B = 0
+    assert L.tv_build_mask(P(FAKE), 257, 1, P(FAKE), None, None, None) == 3       # B > 256
+    assert L.tv_build_mask(None, 16, 1, P(FAKE), None, None, None) == 1           # null parent
+    assert L.tv_build_mask(P(FAKE), 16, 1, None, None, None, None) == 1           # null mask
+    assert L.tv_build_mask(P(FAKE + 2), 16, 1, P(FAKE), None, None, None) == 1    # misaligned parent
+    assert L.tv_build_mask(P(FAKE), 16, -1, P(FAKE), None, None, None) == 1       # nb < 0
+
+
+def _args(**kw):
+    a = dict(q_d=FAKE, k_cache_d=FAKE, v_cache_d=FAKE, block_table_d=FAKE, prefix_lens_d=FAKE, mask_d=FAKE,
+             o_d=FAKE, lse_d=FAKE, dev_status_d=None, nb=1, B=16, Hq=32, Hkv=8, D=128, page_size=16,
+             num_blocks=40, max_pages=40, scale=0.0, num_ctas=0)
+    a.update(kw)
+    return binding.AttnArgs(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=64), 3), (dict(page_size=32), 3), (dict(B=0), 3), (dict(B=257), 3),
+    (dict(Hq=24, Hkv=8), 3),                      # G = 3 unsupported
+    (dict(Hq=30, Hkv=8), 1),                      # Hq not a multiple of Hkv
+    (dict(Hq=64, Hkv=2), 3),                      # G = 32 unsupported
+    (dict(q_d=None), 1), (dict(lse_d=None), 1), (dict(mask_d=None), 1),
+    (dict(q_d=FAKE + 8), 1),                      # q not 16-byte aligned
+    (dict(o_d=FAKE + 4), 1),
+    (dict(num_blocks=0), 1), (dict(nb=-1), 1), (dict(num_ctas=-2), 1),
+    (dict(max_pages=1 << 27), 3),
+])
+def test_attn_argument_checks(L, kw, code):
+    a = _args(**kw)
+    assert L.tv_attn(C.byref(a), C.c_void_p(FAKE), 1 << 30, None) == code
+    assert L.tv_attn_workspace_size(C.byref(a)) == 0
+
+
+def test_attn_null_args(L):
+    assert L.tv_attn(None, None, 0, None) == 1
+    assert L.tv_attn_workspace_size(None) == 0
+
+
+def test_accept_argument_checks(L):
+    P = C.c_void_p
+    ok = [P(FAKE)] * 4
+    base = dict(logits=P(FAKE), V=100, draft=P(FAKE), parent=P(FAKE), mask=P(FAKE), B=16, nb=1)
+
+    def call(**kw):
+        d = dict(base)
+        d.update(kw)
+        return L.tv_accept(d["logits"], d["V"], d["draft"], d["parent"], d["mask"], d["B"], d["nb"], *ok, None, None)
+
+    assert call(nb=0) == 0
+    assert call(V=0) == 1
+    assert call(B=0) == 3 and call(B=300) == 3
+    assert call(logits=None) == 1 and call(mask=None) == 1
+    assert call(logits=P(FAKE + 1)) == 1
+    assert call(draft=P(FAKE + 2)) == 1
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        binding.lib()

@@ -1,0 +1,156 @@
+"""Thin ctypes binding over libtreeverify's C ABI (include/treeverify.h).
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+Tensors are torch CUDA tensors (device memory and streams come from torch);
+the functions keep the C names: build_mask, attn, accept.  There is no CPU
+path: if the library is missing, loading fails with an error.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtreeverify.so")
+
+TV_OK = 0
+TV_ERR_INVALID_ARG = 1
+TV_ERR_NOT_TOPOLOGICAL = 2
+TV_ERR_UNSUPPORTED_SHAPE = 3
+TV_ERR_CUDA = 4
+TV_ERR_TIMEOUT = 5
+TV_ERR_UNIMPLEMENTED = 6
+
+EXPORTED = ("tv_status_str", "tv_version", "tv_build_mask", "tv_attn_workspace_size", "tv_attn", "tv_accept")
+
+
+class TVError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {status_str(code)} ({code})")
+
+
+class AttnArgs(C.Structure):
+    """Mirror of tv_attn_args."""
+    _fields_ = [
+        ("q_d", C.c_void_p), ("k_cache_d", C.c_void_p), ("v_cache_d", C.c_void_p),
+        ("block_table_d", C.c_void_p), ("prefix_lens_d", C.c_void_p), ("mask_d", C.c_void_p),
+        ("o_d", C.c_void_p), ("lse_d", C.c_void_p), ("dev_status_d", C.c_void_p),
+        ("nb", C.c_int32), ("B", C.c_int32), ("Hq", C.c_int32), ("Hkv", C.c_int32), ("D", C.c_int32),
+        ("page_size", C.c_int32), ("num_blocks", C.c_int32), ("max_pages", C.c_int32),
+        ("scale", C.c_float), ("num_ctas", C.c_int32),
+    ]
+
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """Load libtreeverify.so (built by build.build()); raises if it is absent."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libtreeverify.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+        L = C.CDLL(LIB_PATH)
+        P, I = C.c_void_p, C.c_int32
+        L.tv_status_str.argtypes = [I]
+        L.tv_status_str.restype = C.c_char_p
+        L.tv_version.argtypes = []
+        L.tv_version.restype = I
+        L.tv_build_mask.argtypes = [P, I, I, P, P, P, P]
+        L.tv_build_mask.restype = I
+        L.tv_attn_workspace_size.argtypes = [C.POINTER(AttnArgs)]
+        L.tv_attn_workspace_size.restype = C.c_size_t
+        L.tv_attn.argtypes = [C.POINTER(AttnArgs), P, C.c_size_t, P]
+        L.tv_attn.restype = I
+        L.tv_accept.argtypes = [P, I, P, P, P, I, I, P, P, P, P, P, P]
+        L.tv_accept.restype = I
+        _lib = L
+    return _lib
+
+
+def status_str(code: int) -> str:
+    return lib().tv_status_str(int(code)).decode()
+
+
+def _p(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream)
+
+
+def _check(rc: int, what: str):
+    if rc != TV_OK:
+        raise TVError(rc, what)
+
+
+def build_mask(parent: torch.Tensor, status: torch.Tensor | None = None, mask: torch.Tensor | None = None,
+               depth: torch.Tensor | None = None, stream=None):
+    """tv_build_mask: parent int32 [nb][B] (cuda) -> (mask uint32-as-int32 [nb][B][W], depth int32 [nb][B])."""
+    nb, B = parent.shape
+    W = (B + 31) // 32
+    if mask is None:
+        mask = torch.empty((nb, B, W), dtype=torch.int32, device=parent.device)
+    if depth is None:
+        depth = torch.empty((nb, B), dtype=torch.int32, device=parent.device)
+    rc = lib().tv_build_mask(_p(parent), B, nb, _p(mask), _p(depth), _p(status), _stream(stream))
+    _check(rc, "tv_build_mask")
+    return mask, depth
+
+
+def attn_args(q, k_cache, v_cache, block_table, prefix_lens, mask, o, lse, status=None, scale: float = 0.0,
+              num_ctas: int = 0) -> AttnArgs:
+    nbB, Hq, D = q.shape
+    num_blocks, Hkv, page, _ = k_cache.shape
+    nb = prefix_lens.shape[0]
+    B = nbB // nb if nb else 0
+    return AttnArgs(q_d=q.data_ptr(), k_cache_d=k_cache.data_ptr(), v_cache_d=v_cache.data_ptr(),
+                    block_table_d=block_table.data_ptr(), prefix_lens_d=prefix_lens.data_ptr(),
+                    mask_d=mask.data_ptr(), o_d=o.data_ptr(), lse_d=lse.data_ptr(),
+                    dev_status_d=(status.data_ptr() if status is not None else None),
+                    nb=nb, B=B, Hq=Hq, Hkv=Hkv, D=D, page_size=page, num_blocks=num_blocks,
+                    max_pages=block_table.shape[1], scale=float(scale), num_ctas=int(num_ctas))
+
+
+def attn_workspace_size(args: AttnArgs) -> int:
+    return int(lib().tv_attn_workspace_size(C.byref(args)))
+
+
+def attn(q, k_cache, v_cache, block_table, prefix_lens, mask, status=None, scale: float = 0.0, num_ctas: int = 0,
+         o=None, lse=None, workspace=None, stream=None):
+    """tv_attn: returns (O bf16 [nb*B][Hq][D], LSE fp32 [nb*B][Hq])."""
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    a = attn_args(q, k_cache, v_cache, block_table, prefix_lens, mask, o, lse, status, scale, num_ctas)
+    need = attn_workspace_size(a)
+    if need == 0:  # invalid arguments: let the library say which
+        _check(lib().tv_attn(C.byref(a), None, 0, _stream(stream)), "tv_attn")
+        return o, lse
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    rc = lib().tv_attn(C.byref(a), _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "tv_attn")
+    return o, lse
+
+
+def accept(logits, draft, parent, mask, status=None, out=None, stream=None):
+    """tv_accept: returns (argmax [nb*B], n_acc [nb], path [nb][B], bonus [nb]) int32 tensors."""
+    nb, B = parent.shape
+    V = logits.shape[-1]
+    dev = logits.device
+    if out is None:
+        out = (torch.empty(nb * B, dtype=torch.int32, device=dev), torch.empty(nb, dtype=torch.int32, device=dev),
+               torch.empty((nb, B), dtype=torch.int32, device=dev), torch.empty(nb, dtype=torch.int32, device=dev))
+    am, n_acc, path, bonus = out
+    rc = lib().tv_accept(_p(logits), V, _p(draft), _p(parent), _p(mask), B, nb, _p(am), _p(n_acc), _p(path),
+                         _p(bonus), _p(status), _stream(stream))
+    _check(rc, "tv_accept")
+    return am, n_acc, path, bonus

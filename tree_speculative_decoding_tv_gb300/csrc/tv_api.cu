@@ -1,0 +1,137 @@
+// C ABI of libtreeverify: argument validation and kernel dispatch.
+// Entry points and their contracts are declared and documented in
+// include/treeverify.h.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "tv_internal.h"
+
+namespace {
+
+constexpr int kMaxB = 256;
+constexpr int kHeadDim = 128;
+constexpr int kPageSize = 16;
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool group_supported(int G) { return G == 1 || G == 2 || G == 4 || G == 8 || G == 16; }
+
+int sm_count()
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    return n;
+}
+
+// Validates everything about tv_attn_args that can be checked on the host.
+int32_t check_attn(const tv_attn_args *a)
+{
+    if (!a) return TV_ERR_INVALID_ARG;
+    if (a->nb < 0) return TV_ERR_INVALID_ARG;
+    if (a->B < 1 || a->B > kMaxB) return TV_ERR_UNSUPPORTED_SHAPE;
+    if (a->D != kHeadDim || a->page_size != kPageSize) return TV_ERR_UNSUPPORTED_SHAPE;
+    if (a->Hq < 1 || a->Hkv < 1 || a->Hq % a->Hkv != 0) return TV_ERR_INVALID_ARG;
+    if (!group_supported(a->Hq / a->Hkv)) return TV_ERR_UNSUPPORTED_SHAPE;
+    if (a->num_blocks < 1 || a->max_pages < 1) return TV_ERR_INVALID_ARG;
+    if ((long long)a->max_pages * kPageSize >= (1ll << 30)) return TV_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)a->num_blocks * a->Hkv * kPageSize >= (1ll << 31)) return TV_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)a->nb * a->B * a->Hq >= (1ll << 31)) return TV_ERR_UNSUPPORTED_SHAPE;
+    if (a->num_ctas < 0) return TV_ERR_INVALID_ARG;
+    if (!a->q_d || !a->k_cache_d || !a->v_cache_d || !a->block_table_d || !a->prefix_lens_d || !a->mask_d ||
+        !a->o_d || !a->lse_d)
+        return TV_ERR_INVALID_ARG;
+    if (!aligned(a->q_d, 16) || !aligned(a->k_cache_d, 16) || !aligned(a->v_cache_d, 16) || !aligned(a->o_d, 16))
+        return TV_ERR_INVALID_ARG;
+    if (!aligned(a->block_table_d, 4) || !aligned(a->prefix_lens_d, 4) || !aligned(a->mask_d, 4) ||
+        !aligned(a->lse_d, 4) || !aligned(a->dev_status_d, 4))
+        return TV_ERR_INVALID_ARG;
+    return TV_OK;
+}
+
+int attn_ctas(const tv_attn_args *a)
+{
+    if (a->num_ctas > 0) return a->num_ctas;
+    return sm_count();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *tv_status_str(int32_t s)
+{
+    switch (s) {
+    case TV_OK: return "TV_OK";
+    case TV_ERR_INVALID_ARG: return "TV_ERR_INVALID_ARG";
+    case TV_ERR_NOT_TOPOLOGICAL: return "TV_ERR_NOT_TOPOLOGICAL";
+    case TV_ERR_UNSUPPORTED_SHAPE: return "TV_ERR_UNSUPPORTED_SHAPE";
+    case TV_ERR_CUDA: return "TV_ERR_CUDA";
+    case TV_ERR_TIMEOUT: return "TV_ERR_TIMEOUT";
+    case TV_ERR_UNIMPLEMENTED: return "TV_ERR_UNIMPLEMENTED";
+    default: return "TV_ERR_UNKNOWN";
+    }
+}
+
+int32_t tv_version(void) { return 100; }
+
+int32_t tv_build_mask(const int32_t *parent_d, int32_t B, int32_t nb, uint32_t *mask_d, int32_t *depth_d,
+                      int32_t *dev_status_d, void *stream)
+{
+    if (nb < 0) return TV_ERR_INVALID_ARG;
+    if (B < 1 || B > kMaxB) return TV_ERR_UNSUPPORTED_SHAPE;
+    if (!parent_d || !mask_d) return TV_ERR_INVALID_ARG;
+    if (!aligned(parent_d, 4) || !aligned(mask_d, 4) || !aligned(depth_d, 4) || !aligned(dev_status_d, 4))
+        return TV_ERR_INVALID_ARG;
+    if (nb == 0) return TV_OK;
+    cudaError_t e = tv::launch_build_mask(parent_d, B, nb, mask_d, depth_d, dev_status_d,
+                                          static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
+size_t tv_attn_workspace_size(const tv_attn_args *args)
+{
+    if (check_attn(args) != TV_OK) return 0;
+    const int ctas = attn_ctas(args);
+    if (ctas < 1) return 0;
+    return tv::attn_workspace_bytes(ctas);
+}
+
+int32_t tv_attn(const tv_attn_args *args, void *workspace_d, size_t workspace_bytes, void *stream)
+{
+    const int32_t rc = check_attn(args);
+    if (rc != TV_OK) return rc;
+    if (args->nb == 0) return TV_OK;
+    const int ctas = attn_ctas(args);
+    if (ctas < 1) return TV_ERR_CUDA;
+    if (!workspace_d || !aligned(workspace_d, 16) || workspace_bytes < tv::attn_workspace_bytes(ctas))
+        return TV_ERR_INVALID_ARG;
+    cudaError_t e;
+    return tv::launch_attn(args, ctas, workspace_d, static_cast<cudaStream_t>(stream), &e);
+}
+
+int32_t tv_accept(const uint16_t *logits_d, int32_t V, const int32_t *draft_tokens_d, const int32_t *parent_d,
+                  const uint32_t *mask_d, int32_t B, int32_t nb, int32_t *argmax_d, int32_t *n_acc_d,
+                  int32_t *path_d, int32_t *bonus_d, int32_t *dev_status_d, void *stream)
+{
+    if (nb < 0 || V < 1) return TV_ERR_INVALID_ARG;
+    if (B < 1 || B > kMaxB) return TV_ERR_UNSUPPORTED_SHAPE;
+    if (!logits_d || !draft_tokens_d || !parent_d || !mask_d || !argmax_d || !n_acc_d || !path_d || !bonus_d)
+        return TV_ERR_INVALID_ARG;
+    if (!aligned(logits_d, 2) || !aligned(draft_tokens_d, 4) || !aligned(parent_d, 4) || !aligned(mask_d, 4) ||
+        !aligned(argmax_d, 4) || !aligned(n_acc_d, 4) || !aligned(path_d, 4) || !aligned(bonus_d, 4) ||
+        !aligned(dev_status_d, 4))
+        return TV_ERR_INVALID_ARG;
+    if ((long long)nb * B * 8 >= (1ll << 31)) return TV_ERR_UNSUPPORTED_SHAPE;
+    if (nb == 0) return TV_OK;
+    cudaError_t e = tv::launch_accept(logits_d, V, draft_tokens_d, parent_d, mask_d, B, nb, argmax_d, n_acc_d,
+                                      path_d, bonus_d, dev_status_d, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
+}  // extern "C"

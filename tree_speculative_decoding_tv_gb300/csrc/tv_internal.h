@@ -1,0 +1,27 @@
+// Internal launch interface between the C ABI (tv_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/treeverify.h"
+
+namespace tv {
+
+cudaError_t launch_build_mask(const int32_t *parent, int B, int nb, uint32_t *mask, int32_t *depth, int32_t *status,
+                              cudaStream_t stream);
+
+cudaError_t launch_accept(const uint16_t *logits, int V, const int32_t *draft, const int32_t *parent,
+                          const uint32_t *mask, int B, int nb, int32_t *am, int32_t *n_acc, int32_t *path,
+                          int32_t *bonus, int32_t *status, cudaStream_t stream);
+
+// Workspace bytes the attention needs with `ctas` CTAs.
+size_t attn_workspace_bytes(int ctas);
+
+// Encodes the TMA descriptors and launches the attention and merge kernels.
+// Returns TV_OK or TV_ERR_CUDA (with *cuda_err set).
+int32_t launch_attn(const tv_attn_args *a, int ctas, void *workspace, cudaStream_t stream, cudaError_t *cuda_err);
+
+}  // namespace tv
