@@ -1,0 +1,391 @@
+"""Benchmark of one tree-verification step on GB300.
+
+A step is the whole hot path over one batch: ancestor masks (tv_build_mask),
+tree-causal paged attention with split-KV merge (tv_attn), vocab argmax and
+greedy acceptance (tv_accept), for one layer's attention.  The metric is
+verified tree nodes per second per layer (nb * B / step time).
+
+Default workload: 1 sequence, Qwen3-8B attention shape (32 q / 8 kv heads,
+head dim 128, bf16), 4096-token prefix in shuffled 16-token pages, a 256-node
+best-first draft tree, 151936-entry bf16 logits.  Inputs are seeded synthetic
+tensors of those shapes, resident in HBM; L2 is flushed (a 512 MB write)
+before every timed step.
+
+  python bench.py [--gpus N --steps K --warmup W] [--config 1..5] [--impl reference]
+
+Under torchrun (N > 1) every rank runs an independent replica (the step has no
+cross-GPU exchange); value = all ranks' nodes / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "tree-verify attn verified nodes/s per layer; % of roofline (HBM or TC)"
+UNIT = "nodes/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- bookkeeping
+
+def tree_depth(parent: np.ndarray) -> np.ndarray:
+    d = np.zeros(len(parent), dtype=np.int64)
+    for i in range(1, len(parent)):
+        d[i] = d[parent[i]] + 1
+    return d
+
+
+def attn_bytes(w: wl.Workload) -> int:
+    """K+V read once per (sequence, kv head) + Q + O (bf16) + LSE (fp32)."""
+    kv = 2 * int(np.sum(w.prefix_lens.astype(np.int64) + w.B)) * w.Hkv * w.D * 2
+    return kv + 2 * w.nb * w.B * w.Hq * w.D * 2 + w.nb * w.B * w.Hq * 4
+
+
+def attn_flops(w: wl.Workload) -> int:
+    """QK^T and PV over the prefix (dense) and over ancestor pairs only inside the tree."""
+    tot = 0
+    for b in range(w.nb):
+        tot += 4 * w.Hq * w.D * (w.B * int(w.prefix_lens[b]) + int(np.sum(tree_depth(w.parent[b]) + 1)))
+    return tot
+
+
+def accept_bytes(w: wl.Workload) -> int:
+    return w.nb * w.B * w.V * 2
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured (MEASURED_PEAKS.json)"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback (no MEASURED_PEAKS.json)"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms in the background."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.t0 = time.time()
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self, t_begin: float, t_end: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        n = 0
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            n += 1
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        # samples come ~100 ms apart from t0; keep the ones inside the timed window when there are any
+        dt = (time.time() - self.t0) / max(1, len(rows))
+        times = [self.t0 + (k + 0.5) * dt for k in range(len(rows))]
+        inside = [r for r, t in zip(rows, times) if t_begin <= t <= t_end]
+        sel = inside if inside else rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in sel for k in range(4) if r[2][k].lower().startswith("active")})
+        return {"sm_mhz": float(np.median([r[0] for r in sel])), "sm_max_mhz": max(r[1] for r in sel),
+                "reasons": reasons, "samples": len(sel), "window": "timed" if inside else "whole run"}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+class Step:
+    """Device-resident inputs, preallocated outputs and one verify step through the C ABI."""
+
+    def __init__(self, w: wl.Workload, dev: str):
+        import torch
+        import tree_speculative_decoding_tv_gb300 as tv
+        self.torch, self.tv, self.w = torch, tv, w
+
+        def bf(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+        def i32(a):
+            return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+        self.q, self.k, self.v = bf(w.q), bf(w.k_cache), bf(w.v_cache)
+        self.bt, self.pl, self.parent, self.draft = i32(w.block_table), i32(w.prefix_lens), i32(w.parent), i32(w.draft)
+        self.logits = bf(w.logits)
+        W = (w.B + 31) // 32
+        self.mask = torch.empty((w.nb, w.B, W), dtype=torch.int32, device=dev)
+        self.depth = torch.empty((w.nb, w.B), dtype=torch.int32, device=dev)
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty((w.nb * w.B, w.Hq), dtype=torch.float32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        args = tv.attn_args(self.q, self.k, self.v, self.bt, self.pl, self.mask, self.o, self.lse, self.status)
+        self.ws = torch.empty(tv.attn_workspace_size(args), dtype=torch.uint8, device=dev)
+        self.acc_out = (torch.empty(w.nb * w.B, dtype=torch.int32, device=dev),
+                        torch.empty(w.nb, dtype=torch.int32, device=dev),
+                        torch.empty((w.nb, w.B), dtype=torch.int32, device=dev),
+                        torch.empty(w.nb, dtype=torch.int32, device=dev))
+        self.acc_ws = torch.empty(tv.accept_workspace_size(w.V, w.B, w.nb), dtype=torch.uint8, device=dev)
+        self.launches_per_step = 4  # mask, attention, argmax partials, argmax finish + acceptance walk
+
+    def run(self, ev=None):
+        tv = self.tv
+        if ev is not None:
+            ev[0].record()
+        tv.build_mask(self.parent, status=self.status, mask=self.mask, depth=self.depth)
+        tv.attn(self.q, self.k, self.v, self.bt, self.pl, self.mask, status=self.status, o=self.o, lse=self.lse,
+                workspace=self.ws)
+        if ev is not None:
+            ev[1].record()
+        tv.accept(self.logits, self.draft, self.parent, self.mask, status=self.status, out=self.acc_out,
+                  workspace=self.acc_ws)
+        if ev is not None:
+            ev[2].record()
+
+
+def run_gpu(args, rank: int, world: int, local_rank: int):
+    import torch
+    import torch.distributed as dist
+
+    torch.cuda.set_device(local_rank)
+    dev = f"cuda:{local_rank}"
+    w = wl.config(args.config, seed=1234 + rank)
+    st = Step(w, dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    sampler = ClockSampler(local_rank)
+
+    for _ in range(args.warmup):
+        st.run()
+    torch.cuda.synchronize()
+    if st.status.item() != 0:
+        raise RuntimeError(f"device status {st.status.item()} during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_begin = time.time()
+    for k in range(args.steps):
+        flush.zero_()
+        st.run(evs[k])
+    torch.cuda.synchronize()
+    t_end = time.time()
+    if world > 1:
+        dist.barrier()
+    step_ms = [e[0].elapsed_time(e[2]) for e in evs]
+    attn_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    acc_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    total_ms = float(np.sum(step_ms))
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    clocks = sampler.stop(t_begin, t_end)
+    if st.status.item() != 0:
+        raise RuntimeError(f"device status {st.status.item()} in the timed region")
+
+    # end to end: host (pinned) inputs -> device, step, results -> host, every step
+    h_in = {n: getattr(st, n).cpu().pin_memory() for n in ("q", "logits", "parent", "draft", "bt", "pl")}
+    h_out = {n: torch.empty(getattr(st, n).shape, dtype=getattr(st, n).dtype).pin_memory() for n in ("o", "lse")}
+    h_acc = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in st.acc_out[1:]]
+    bi = sum(t.numel() * t.element_size() for t in h_in.values())
+    bo = sum(t.numel() * t.element_size() for t in h_out.values()) + sum(t.numel() * t.element_size() for t in h_acc)
+
+    def e2e_step():
+        for n, t in h_in.items():
+            getattr(st, n).copy_(t, non_blocking=True)
+        st.run()
+        for n, t in h_out.items():
+            t.copy_(getattr(st, n), non_blocking=True)
+        for t, s in zip(h_acc, st.acc_out[1:]):
+            t.copy_(s, non_blocking=True)
+
+    for _ in range(max(1, min(args.warmup, 3))):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for k in range(args.steps):
+        flush.zero_()
+        e2e_ev[k][0].record()
+        e2e_step()
+        e2e_ev[k][1].record()
+    torch.cuda.synchronize()
+    e2e_ms = float(np.sum([a.elapsed_time(b) for a, b in e2e_ev]))
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        return
+    nodes = w.nb * w.B
+    ms_per_step = total_ms / args.steps
+    peaks, peak_src = load_peaks()
+    t_attn = float(np.mean(attn_ms)) * 1e-3
+    t_acc = float(np.mean(acc_ms)) * 1e-3
+    ab, af, lb = attn_bytes(w), attn_flops(w), accept_bytes(w)
+    attn_tc = af / (peaks["bf16_tflops"] * 1e12)
+    attn_hbm = ab / (peaks["hbm_gbs"] * 1e9)
+    if attn_tc >= attn_hbm:
+        attn_roof = {"kernel": "tree_attn_kernel", "bound": "tensor",
+                     "achieved": af / t_attn / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    else:
+        attn_roof = {"kernel": "tree_attn_kernel", "bound": "hbm",
+                     "achieved": ab / t_attn / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    acc_roof = {"kernel": "argmax_partial_kernel + accept_kernel", "bound": "hbm", "achieved": lb / t_acc / 1e9,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    for r in (attn_roof, acc_roof):
+        r["frac"] = r["achieved"] / r["peak"]
+        r["peak_source"] = peak_src + " burst"
+        r["traffic"] = None
+    roof = attn_roof if t_attn >= t_acc else acc_roof
+    out = {
+        "metric": METRIC, "value": nodes * world / (total_ms / args.steps * 1e-3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; shapes of the pages' Qwen3 workloads, random values)",
+        "config": {"workload": wl.CONFIG_NAMES[args.config], "nb": w.nb, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
+                   "D": w.D, "prefix_lens": [int(x) for x in w.prefix_lens][:8], "V": w.V,
+                   "l2": "flushed before every timed step (512 MB write)", "parallelism": f"replicas x{world}"},
+        "roofline": roof,
+        "breakdown": {
+            "attention_ms": float(np.mean(attn_ms)), "accept_ms": float(np.mean(acc_ms)),
+            "attention_nodes_per_s": nodes / t_attn, "attention_roofline": attn_roof, "accept_roofline": acc_roof,
+            "attention_bytes": ab, "attention_flops": af, "accept_bytes": lb,
+        },
+        "clocks": clocks,
+        "gpu_launches": st.launches_per_step * args.steps,
+        "e2e": {"value": nodes * world / (e2e_ms / args.steps * 1e-3), "unit": UNIT, "h2d_bytes_per_step": bi,
+                "d2h_bytes_per_step": bo,
+                "note": "per step: q, logits, parent, draft tokens, block table, prefix lengths copied in from "
+                        "pinned host memory; O, LSE, accepted length, path and bonus copied out; the paged KV "
+                        "cache is resident model state"},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(out), flush=True)
+
+
+# ----------------------------------------------------------------------------- CPU oracle legs
+
+def oracle_step(w: wl.Workload, heads: int):
+    """One oracle verify step on a head sample; returns (wall seconds for the full step, threads, note)."""
+    import oracle
+    G = w.G
+    groups = max(1, heads // G)
+    t0 = time.perf_counter()
+    oracle.build_mask(w.parent)
+    t1 = time.perf_counter()
+    q = np.ascontiguousarray(w.q[:, :groups * G])
+    kc = np.ascontiguousarray(w.k_cache[:, :groups])
+    vc = np.ascontiguousarray(w.v_cache[:, :groups])
+    t2 = time.perf_counter()
+    _, _, threads = oracle.attn(q, kc, vc, w.block_table, w.prefix_lens, w.parent, groups * G, groups,
+                                return_threads=True)
+    t3 = time.perf_counter()
+    oracle.accept(w.logits, w.draft, w.parent)
+    t4 = time.perf_counter()
+    full = (t1 - t0) + (t3 - t2) * (w.Hq / (groups * G)) + (t4 - t3)
+    return full, threads, groups * G
+
+
+def cpu_baseline(w: wl.Workload, heads: int | None = None):
+    heads = heads or w.Hq
+    full, threads, used = oracle_step(w, heads)
+    return {"value": w.nb * w.B / full, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "host_cores": os.cpu_count(),
+            "sample": f"one full step of the same workload (mask, attention on {used} of {w.Hq} query heads "
+                      f"scaled by {w.Hq / used:g}, argmax + acceptance over all {w.nb * w.B} logits rows); "
+                      f"fp64 C oracle, wall clock"}
+
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return
+    w = wl.config(args.config, seed=1234)
+    # a head sample that keeps every host core busy (whole kv-head groups) and each step to seconds
+    heads = args.ref_heads or min(w.Hq, max(w.G, ((os.cpu_count() or 1) // w.G) * w.G))
+    for _ in range(args.warmup):
+        oracle_step(w, heads)
+    times = []
+    threads = 0
+    used = heads
+    for _ in range(args.steps):
+        t, threads, used = oracle_step(w, heads)
+        times.append(t)
+    ms = float(np.mean(times)) * 1e3
+    v = w.nb * w.B / (ms * 1e-3)
+    out = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+           "config": {"workload": wl.CONFIG_NAMES[args.config], "nb": w.nb, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
+                      "D": w.D, "V": w.V},
+           "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+                            "sample": f"each step: mask, attention on {used} of {w.Hq} query heads scaled by "
+                                      f"{w.Hq / used:g}, argmax + acceptance over all rows; fp64 C oracle"},
+           "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--ref-heads", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    import torch.distributed as dist
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local_rank}"))
+    try:
+        run_gpu(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -22,9 +22,11 @@
  *
  * Conventions for every entry point
  *   - All pointers with a _d meaning are DEVICE pointers on the current
- *     device; the caller allocates and owns every buffer.  The library
- *     allocates no device memory, keeps no pointer after a call returns and
- *     holds no state (it encodes TMA descriptors on every call).
+ *     device; the caller allocates and owns every buffer (workspaces
+ *     included).  The library allocates no device memory, keeps no pointer
+ *     after a call returns and encodes TMA descriptors on every call; its only
+ *     host state is a per-device SM-count cache and the attention's ticket
+ *     epoch counter.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Every call only enqueues work on `stream` and returns; results
  *     are ready when the stream reaches that point.
@@ -127,10 +129,13 @@ typedef struct tv_attn_args {
  * arguments are invalid. */
 TV_API size_t tv_attn_workspace_size(const tv_attn_args *args);
 
-/* Enqueue the attention.  workspace_d: device buffer of at least
- * tv_attn_workspace_size(args) bytes, 256-byte aligned, contents ignored on
- * entry (it carries split-KV partial results between the two kernels of one
- * call, so concurrent calls need separate workspaces).
+/* Enqueue the attention (one kernel launch).  workspace_d: device buffer of at
+ * least tv_attn_workspace_size(args) bytes, 16-byte aligned, contents ignored
+ * on entry.  It holds split-KV partial results and the per-row-tile tickets
+ * whose last holder merges them; concurrent calls need separate workspaces.
+ * The library keeps one process-wide counter that gives every call a distinct
+ * ticket epoch, so tickets left by an earlier or interrupted call are never
+ * counted again.
  * Returns TV_OK, TV_ERR_INVALID_ARG, TV_ERR_UNSUPPORTED_SHAPE or TV_ERR_CUDA.
  * nb == 0 is a no-op. */
 TV_API int32_t tv_attn(const tv_attn_args *args, void *workspace_d, size_t workspace_bytes, void *stream);
@@ -153,12 +158,19 @@ TV_API int32_t tv_attn(const tv_attn_args *args, void *workspace_d, size_t works
  *   mask_d         uint32 [nb][B][ceil(B/32)] from tv_build_mask for the same parent
  *   argmax_d       int32 [nb*B] (out), n_acc_d int32 [nb], path_d int32 [nb][B],
  *   bonus_d        int32 [nb] (out)
+ *   workspace_d    device buffer of at least tv_accept_workspace_size(V, B, nb)
+ *                  bytes, 8-byte aligned, contents ignored on entry (it carries
+ *                  per-chunk argmax partials between the call's two kernels, so
+ *                  concurrent calls need separate workspaces)
  * Returns TV_OK, TV_ERR_INVALID_ARG, TV_ERR_UNSUPPORTED_SHAPE or TV_ERR_CUDA.
+ * A parent array that is not topological is reported through dev_status_d.
  */
+TV_API size_t tv_accept_workspace_size(int32_t V, int32_t B, int32_t nb);
+
 TV_API int32_t tv_accept(const uint16_t *logits_d, int32_t V, const int32_t *draft_tokens_d,
-                  const int32_t *parent_d, const uint32_t *mask_d, int32_t B, int32_t nb,
-                  int32_t *argmax_d, int32_t *n_acc_d, int32_t *path_d, int32_t *bonus_d,
-                  int32_t *dev_status_d, void *stream);
+                         const int32_t *parent_d, const uint32_t *mask_d, int32_t B, int32_t nb,
+                         int32_t *argmax_d, int32_t *n_acc_d, int32_t *path_d, int32_t *bonus_d,
+                         int32_t *dev_status_d, void *workspace_d, size_t workspace_bytes, void *stream);
 
 #ifdef __cplusplus
 }

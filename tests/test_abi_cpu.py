@@ -94,7 +94,8 @@ def test_accept_argument_checks(L):
     def call(**kw):
         d = dict(base)
         d.update(kw)
-        return L.tv_accept(d["logits"], d["V"], d["draft"], d["parent"], d["mask"], d["B"], d["nb"], *ok, None, None)
+        return L.tv_accept(d["logits"], d["V"], d["draft"], d["parent"], d["mask"], d["B"], d["nb"], *ok, None,
+                           d.get("ws", P(FAKE)), d.get("ws_bytes", 1 << 30), None)
 
     assert call(nb=0) == 0
     assert call(V=0) == 1
@@ -102,6 +103,9 @@ def test_accept_argument_checks(L):
     assert call(logits=None) == 1 and call(mask=None) == 1
     assert call(logits=P(FAKE + 1)) == 1
     assert call(draft=P(FAKE + 2)) == 1
+    assert call(ws=None) == 1 and call(ws_bytes=8) == 1 and call(ws=P(FAKE + 4)) == 1
+    assert L.tv_accept_workspace_size(151936, 256, 1) == 256 * 19 * 8
+    assert L.tv_accept_workspace_size(0, 16, 1) == 0 and L.tv_accept_workspace_size(10, 300, 1) == 0
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

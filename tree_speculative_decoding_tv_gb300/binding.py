@@ -23,7 +23,8 @@ TV_ERR_CUDA = 4
 TV_ERR_TIMEOUT = 5
 TV_ERR_UNIMPLEMENTED = 6
 
-EXPORTED = ("tv_status_str", "tv_version", "tv_build_mask", "tv_attn_workspace_size", "tv_attn", "tv_accept")
+EXPORTED = ("tv_status_str", "tv_version", "tv_build_mask", "tv_attn_workspace_size", "tv_attn",
+            "tv_accept_workspace_size", "tv_accept")
 
 
 class TVError(RuntimeError):
@@ -65,7 +66,9 @@ def lib() -> C.CDLL:
         L.tv_attn_workspace_size.restype = C.c_size_t
         L.tv_attn.argtypes = [C.POINTER(AttnArgs), P, C.c_size_t, P]
         L.tv_attn.restype = I
-        L.tv_accept.argtypes = [P, I, P, P, P, I, I, P, P, P, P, P, P]
+        L.tv_accept_workspace_size.argtypes = [I, I, I]
+        L.tv_accept_workspace_size.restype = C.c_size_t
+        L.tv_accept.argtypes = [P, I, P, P, P, I, I, P, P, P, P, P, P, C.c_size_t, P]
         L.tv_accept.restype = I
         _lib = L
     return _lib
@@ -141,7 +144,11 @@ def attn(q, k_cache, v_cache, block_table, prefix_lens, mask, status=None, scale
     return o, lse
 
 
-def accept(logits, draft, parent, mask, status=None, out=None, stream=None):
+def accept_workspace_size(V: int, B: int, nb: int) -> int:
+    return int(lib().tv_accept_workspace_size(int(V), int(B), int(nb)))
+
+
+def accept(logits, draft, parent, mask, status=None, out=None, workspace=None, stream=None):
     """tv_accept: returns (argmax [nb*B], n_acc [nb], path [nb][B], bonus [nb]) int32 tensors."""
     nb, B = parent.shape
     V = logits.shape[-1]
@@ -150,7 +157,11 @@ def accept(logits, draft, parent, mask, status=None, out=None, stream=None):
         out = (torch.empty(nb * B, dtype=torch.int32, device=dev), torch.empty(nb, dtype=torch.int32, device=dev),
                torch.empty((nb, B), dtype=torch.int32, device=dev), torch.empty(nb, dtype=torch.int32, device=dev))
     am, n_acc, path, bonus = out
+    need = accept_workspace_size(V, B, nb)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 8), dtype=torch.uint8, device=dev)
     rc = lib().tv_accept(_p(logits), V, _p(draft), _p(parent), _p(mask), B, nb, _p(am), _p(n_acc), _p(path),
-                         _p(bonus), _p(status), _stream(stream))
+                         _p(bonus), _p(status), _p(workspace), workspace.numel() * workspace.element_size(),
+                         _stream(stream))
     _check(rc, "tv_accept")
     return am, n_acc, path, bonus

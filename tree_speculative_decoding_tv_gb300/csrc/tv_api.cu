@@ -99,7 +99,7 @@ size_t tv_attn_workspace_size(const tv_attn_args *args)
     if (check_attn(args) != TV_OK) return 0;
     const int ctas = attn_ctas(args);
     if (ctas < 1) return 0;
-    return tv::attn_workspace_bytes(ctas);
+    return tv::attn_workspace_bytes(ctas, tv::attn_row_tiles(args));
 }
 
 int32_t tv_attn(const tv_attn_args *args, void *workspace_d, size_t workspace_bytes, void *stream)
@@ -109,15 +109,22 @@ int32_t tv_attn(const tv_attn_args *args, void *workspace_d, size_t workspace_by
     if (args->nb == 0) return TV_OK;
     const int ctas = attn_ctas(args);
     if (ctas < 1) return TV_ERR_CUDA;
-    if (!workspace_d || !aligned(workspace_d, 16) || workspace_bytes < tv::attn_workspace_bytes(ctas))
+    if (!workspace_d || !aligned(workspace_d, 16) || workspace_bytes < tv::attn_workspace_bytes(ctas, tv::attn_row_tiles(args)))
         return TV_ERR_INVALID_ARG;
     cudaError_t e;
     return tv::launch_attn(args, ctas, workspace_d, static_cast<cudaStream_t>(stream), &e);
 }
 
+size_t tv_accept_workspace_size(int32_t V, int32_t B, int32_t nb)
+{
+    if (V < 1 || B < 1 || B > kMaxB || nb < 0) return 0;
+    return tv::accept_workspace_bytes(V, B, nb);
+}
+
 int32_t tv_accept(const uint16_t *logits_d, int32_t V, const int32_t *draft_tokens_d, const int32_t *parent_d,
                   const uint32_t *mask_d, int32_t B, int32_t nb, int32_t *argmax_d, int32_t *n_acc_d,
-                  int32_t *path_d, int32_t *bonus_d, int32_t *dev_status_d, void *stream)
+                  int32_t *path_d, int32_t *bonus_d, int32_t *dev_status_d, void *workspace_d,
+                  size_t workspace_bytes, void *stream)
 {
     if (nb < 0 || V < 1) return TV_ERR_INVALID_ARG;
     if (B < 1 || B > kMaxB) return TV_ERR_UNSUPPORTED_SHAPE;
@@ -127,10 +134,15 @@ int32_t tv_accept(const uint16_t *logits_d, int32_t V, const int32_t *draft_toke
         !aligned(argmax_d, 4) || !aligned(n_acc_d, 4) || !aligned(path_d, 4) || !aligned(bonus_d, 4) ||
         !aligned(dev_status_d, 4))
         return TV_ERR_INVALID_ARG;
-    if ((long long)nb * B * 8 >= (1ll << 31)) return TV_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)nb * B * (((long long)V + 8191) / 8192) >= (1ll << 40)) return TV_ERR_UNSUPPORTED_SHAPE;
     if (nb == 0) return TV_OK;
+    if (!workspace_d || !aligned(workspace_d, 8) || workspace_bytes < tv::accept_workspace_bytes(V, B, nb))
+        return TV_ERR_INVALID_ARG;
+    const int sms = sm_count();
+    if (sms < 1) return TV_ERR_CUDA;
     cudaError_t e = tv::launch_accept(logits_d, V, draft_tokens_d, parent_d, mask_d, B, nb, argmax_d, n_acc_d,
-                                      path_d, bonus_d, dev_status_d, static_cast<cudaStream_t>(stream));
+                                      path_d, bonus_d, dev_status_d, workspace_d, sms,
+                                      static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
 

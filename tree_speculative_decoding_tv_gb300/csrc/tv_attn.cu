@@ -17,7 +17,9 @@
 //     contiguous share of all (row tile, KV tile) pairs, computed in-kernel
 //     from prefix_lens (ragged prefixes balance by construction).  A row tile
 //     cut between CTAs leaves fp32 partials (normalised O, LSE) in the
-//     workspace; the merge kernel combines them.
+//     workspace; each piece then takes a ticket (an epoch-tagged counter per
+//     row tile) and the last piece to arrive merges them, so no CTA ever
+//     waits for another and no extra launch is needed.
 //   * Warp roles per CTA (256 threads): warp 0 issues TMA (Q once per row tile
 //     through a 4-D map whose node axis stops at B; K and V one 16-key page x
 //     64-column box at a time through a 2-D map over [pages*Hkv*16][D], page ids
@@ -37,6 +39,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstring>
 
@@ -99,6 +102,8 @@ struct AttnParams {
     int32_t *status;
     float *ws_o;    // [2 * grid][128][128] fp32 partial O (normalised)
     float *ws_lse;  // [2 * grid][128]
+    unsigned long long *tickets;  // [nb * Hkv * MT]: (epoch << 32) | pieces that have arrived
+    uint32_t epoch;               // distinct for every call
     int nb, B, Hq, Hkv, G, NT, MT, W, max_pages, num_blocks;
     float scale_log2;
 };
@@ -140,18 +145,6 @@ __device__ long long sched_total(const Sched &s, int lane)
     for (int base = 0; base < s.nb; base += 32) {
         const int b = base + lane;
         const long long t = (b < s.nb) ? (long long)s.Hkv * head_tiles(s, __ldg(s.prefix_lens + b)) : 0;
-        tot += warp_sum_ll(t);
-    }
-    return tot;
-}
-
-// Pairs that belong to sequences before `b_end`.  Whole warp.
-__device__ long long sched_prefix(const Sched &s, int b_end, int lane)
-{
-    long long tot = 0;
-    for (int base = 0; base < b_end; base += 32) {
-        const int b = base + lane;
-        const long long t = (b < b_end) ? (long long)s.Hkv * head_tiles(s, __ldg(s.prefix_lens + b)) : 0;
         tot += warp_sum_ll(t);
     }
     return tot;
@@ -276,6 +269,10 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
     int *sh_b0 = reinterpret_cast<int *>(gbase + kOffMisc + 8);
     long long *sh_off0 = reinterpret_cast<long long *>(gbase + kOffMisc + 16);
     long long *sh_left = reinterpret_cast<long long *>(gbase + kOffMisc + 24);
+    long long *sh_total = reinterpret_cast<long long *>(gbase + kOffMisc + 32);
+    long long *sh_ctas = reinterpret_cast<long long *>(gbase + kOffMisc + 40);
+    long long *sh_t0 = reinterpret_cast<long long *>(gbase + kOffMisc + 48);
+    volatile int *sh_last = reinterpret_cast<volatile int *>(gbase + kOffMisc + 56);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -325,6 +322,9 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
             *sh_b0 = b0;
             *sh_off0 = off0;
             *sh_left = t1 - t0;
+            *sh_total = total;
+            *sh_ctas = C;
+            *sh_t0 = t0;
         }
         if (blockIdx.x == 0) {
             for (int b = lane; b < sch.nb; b += 32) {
@@ -460,6 +460,9 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const int node_local = row / p.G;
         const int hg = row - node_local * p.G;
+        const float sl2 = p.scale_log2;
+        const long long total = *sh_total, C = *sh_ctas;
+        long long seg_start = *sh_t0;  // global pair index of the current segment's first tile
         Cursor cur = cur0;
         Seg sg;
         uint32_t gt = 0, seg_i = 0;
@@ -469,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
             const bool valid = i < p.B;
             const uint32_t *mrow = p.mask + ((size_t)sg.b * p.B + (valid ? i : 0)) * p.W;
             const int n = sg.j1 - sg.j0;
-            float m_run = -INFINITY, l_run = 0.f;
+            float m_run = -INFINITY, l_run = 0.f;  // m_run in log2 units of the scaled score
             for (int t = 0; t < n; ++t) {
                 const uint32_t g_t = gt + t;
                 const int buf = g_t & 1;
@@ -484,21 +487,24 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                 reg_order(s[2]);
                 reg_order(s[3]);
 
-                // scale to log2 units, mask, row max
-                const bool dense = valid && (k0 + kN <= sg.P);
-                float tmax = -INFINITY;
+                // tree / tail mask (prefix-only tiles skip it), then the row max of the raw scores
+                if (!(valid && k0 + kN <= sg.P)) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint32_t vis =
-                        dense ? 0xffffffffu : (valid ? visible_bits(k0 + 32 * c, sg.P, p.B, mrow, p.W) : 0u);
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t vis = valid ? visible_bits(k0 + 32 * c, sg.P, p.B, mrow, p.W) : 0u;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        float x = __uint_as_float(s[c][e]) * p.scale_log2;
-                        x = ((vis >> e) & 1u) ? x : -INFINITY;
-                        s[c][e] = __float_as_uint(x);
-                        tmax = fmaxf(tmax, x);
+                        for (int e = 0; e < 32; ++e) s[c][e] = ((vis >> e) & 1u) ? s[c][e] : 0xff800000u;
                     }
                 }
+                float mx[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(s[c][e]));
+                const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
 
                 // move the running max only when it grows by more than 2^8
                 const float m_new = fmaxf(m_run, tmax);
@@ -525,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                     l_run *= alpha;
                     m_run = m_new;
                 }
-                const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+                const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
 
                 // P_j may overwrite its buffer once the PV two tiles back is done
                 if (g_t >= 2 &&
@@ -534,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                     break;
                 }
                 const uint32_t prow = sP + buf * kTileBytes + row * 128;
-                float lsum = 0.f;
+                float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
 #pragma unroll
@@ -542,9 +548,10 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                         uint32_t w[4];
 #pragma unroll
                         for (int e2 = 0; e2 < 4; ++e2) {
-                            const float a = ex2_approx(__uint_as_float(s[c][q * 8 + 2 * e2]) - m_use);
-                            const float b = ex2_approx(__uint_as_float(s[c][q * 8 + 2 * e2 + 1]) - m_use);
-                            lsum += a + b;
+                            const float a = ex2_approx(fmaf(__uint_as_float(s[c][q * 8 + 2 * e2]), sl2, neg_m));
+                            const float b = ex2_approx(fmaf(__uint_as_float(s[c][q * 8 + 2 * e2 + 1]), sl2, neg_m));
+                            ls[2 * e2] += a;
+                            ls[2 * e2 + 1] += b;
                             w[e2] = pack_bf16x2(a, b);
                         }
                         const uint32_t chunk = (uint32_t)((c & 1) * 4 + q);  // 16-byte chunk in the 128-byte row
@@ -552,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                                      w[2], w[3]);
                     }
                 }
-                l_run += lsum;
+                l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(BAR(BAR_P_FULL + buf));
@@ -574,13 +581,13 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
             tc_fence_before();
             mbar_arrive(BAR(BAR_O_EMPTY));
 
-            if (valid) {
-                const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-                const float lse2 = l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
-                const int h = sg.g * p.G + hg;
-                const size_t orow = ((size_t)sg.b * p.B + i) * p.Hq + h;
-                if (sg.j0 == 0 && sg.j1 == sg.n_row) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + orow * kHeadDim);
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            const float lse_nat = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+            const int h = sg.g * p.G + hg;
+            const size_t orow = ((size_t)sg.b * p.B + i) * p.Hq + h;
+            uint4 *dst_o = reinterpret_cast<uint4 *>(p.o + orow * kHeadDim);
+            if (sg.j0 == 0 && sg.j1 == sg.n_row) {
+                if (valid) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
 #pragma unroll
@@ -590,25 +597,93 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                             v.y = pack_bf16x2(__uint_as_float(o[c][q * 8 + 2]) * inv, __uint_as_float(o[c][q * 8 + 3]) * inv);
                             v.z = pack_bf16x2(__uint_as_float(o[c][q * 8 + 4]) * inv, __uint_as_float(o[c][q * 8 + 5]) * inv);
                             v.w = pack_bf16x2(__uint_as_float(o[c][q * 8 + 6]) * inv, __uint_as_float(o[c][q * 8 + 7]) * inv);
-                            dst[c * 4 + q] = v;
+                            dst_o[c * 4 + q] = v;
                         }
                     }
-                    p.lse[orow] = lse2 * kLn2;
-                } else {
-                    const size_t slot = 2 * (size_t)blockIdx.x + (seg_i == 0 ? 0 : 1);
+                    p.lse[orow] = lse_nat;
+                }
+            } else {
+                // A piece of a row tile cut between CTAs c0..c1: park it, take a ticket,
+                // and merge all pieces if this one arrived last.
+                const long long r0 = seg_start - sg.j0;
+                const long long r1 = r0 + sg.n_row;
+                const int c0 = (int)(((r0 + 1) * C - 1) / total);
+                const int c1 = (int)((r1 * C - 1) / total);
+                const size_t slot = 2 * (size_t)blockIdx.x + (seg_i == 0 ? 0 : 1);
+                if (valid) {
                     float4 *dst = reinterpret_cast<float4 *>(p.ws_o + (slot * kM + row) * kHeadDim);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < 4; ++c)
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) {
+                        for (int q = 0; q < 8; ++q)
                             dst[c * 8 + q] = make_float4(
                                 __uint_as_float(o[c][q * 4 + 0]) * inv, __uint_as_float(o[c][q * 4 + 1]) * inv,
                                 __uint_as_float(o[c][q * 4 + 2]) * inv, __uint_as_float(o[c][q * 4 + 3]) * inv);
+                    p.ws_lse[slot * kM + row] = lse_nat;
+                }
+                __threadfence();
+                named_bar_sync(1, kM);
+                if (row == 0) {
+                    unsigned long long *tk = p.tickets + ((size_t)sg.b * p.Hkv + sg.g) * p.MT + sg.mt;
+                    unsigned long long cur_t = *reinterpret_cast<volatile unsigned long long *>(tk);
+                    unsigned long long next;
+                    for (;;) {
+                        next = ((uint32_t)(cur_t >> 32) == p.epoch) ? cur_t + 1
+                                                                    : (((unsigned long long)p.epoch << 32) | 1ull);
+                        const unsigned long long seen = atomicCAS(tk, cur_t, next);
+                        if (seen == cur_t) break;
+                        cur_t = seen;
+                    }
+                    *sh_last = ((int)(next & 0xffffffffull) == c1 - c0 + 1) ? 1 : 0;
+                }
+                named_bar_sync(1, kM);
+                if (*sh_last && valid) {
+                    __threadfence();
+                    const int slot0 = (r0 == total * c0 / C) ? 2 * c0 : 2 * c0 + 1;
+                    float m = -INFINITY;
+                    for (int c = c0; c <= c1; ++c)
+                        m = fmaxf(m, __ldcg(p.ws_lse + (size_t)(c == c0 ? slot0 : 2 * c) * kM + row));
+                    float lse_all = -INFINITY;
+                    float wsum = 0.f;
+                    if (m != -INFINITY) {
+                        for (int c = c0; c <= c1; ++c)
+                            wsum += expf(__ldcg(p.ws_lse + (size_t)(c == c0 ? slot0 : 2 * c) * kM + row) - m);
+                        lse_all = m + logf(wsum);
+                    }
+                    for (int part = 0; part < kHeadDim / 32; ++part) {  // 32 output columns at a time
+                        float acc[32];
+#pragma unroll
+                        for (int d = 0; d < 32; ++d) acc[d] = 0.f;
+                        if (m != -INFINITY) {
+                            for (int c = c0; c <= c1; ++c) {
+                                const size_t sl = (size_t)(c == c0 ? slot0 : 2 * c);
+                                const float wgt = expf(__ldcg(p.ws_lse + sl * kM + row) - lse_all);
+                                const float4 *src =
+                                    reinterpret_cast<const float4 *>(p.ws_o + (sl * kM + row) * kHeadDim + part * 32);
+#pragma unroll
+                                for (int q = 0; q < 8; ++q) {
+                                    const float4 v = __ldcg(src + q);
+                                    acc[4 * q + 0] = fmaf(wgt, v.x, acc[4 * q + 0]);
+                                    acc[4 * q + 1] = fmaf(wgt, v.y, acc[4 * q + 1]);
+                                    acc[4 * q + 2] = fmaf(wgt, v.z, acc[4 * q + 2]);
+                                    acc[4 * q + 3] = fmaf(wgt, v.w, acc[4 * q + 3]);
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint4 v;
+                            v.x = pack_bf16x2(acc[8 * q + 0], acc[8 * q + 1]);
+                            v.y = pack_bf16x2(acc[8 * q + 2], acc[8 * q + 3]);
+                            v.z = pack_bf16x2(acc[8 * q + 4], acc[8 * q + 5]);
+                            v.w = pack_bf16x2(acc[8 * q + 6], acc[8 * q + 7]);
+                            dst_o[part * 4 + q] = v;
                         }
                     }
-                    p.ws_lse[slot * kM + row] = lse2 * kLn2;
+                    p.lse[orow] = lse_all;
                 }
             }
+            seg_start += n;
             ++seg_i;
         }
     }
@@ -620,85 +695,6 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
         tmem_dealloc(tmem, kTmemCols);
     }
 #undef BAR
-}
-
-struct MergeParams {
-    const int32_t *prefix_lens;
-    const float *ws_o;
-    const float *ws_lse;
-    uint16_t *o;
-    float *lse;
-    int nb, B, Hq, Hkv, G, NT, MT, max_pages, attn_grid;
-};
-
-// Combines the partials of every row tile that the stream-K split cut
-// between CTAs: lse = ln sum_u e^{lse_u}, O = sum_u e^{lse_u - lse} O_u.
-// One CTA per row tile; the row tile's pieces sit in consecutive CTAs
-// c0..c1 of the attention grid: in c0's last slot (or first, when the row
-// tile starts c0's share) and in the first slot of c0+1..c1.
-__global__ void __launch_bounds__(kHeadDim) tree_attn_merge_kernel(const MergeParams mp)
-{
-    __shared__ int sh_c0, sh_c1, sh_slot0;
-    const int id = blockIdx.x;
-    const int b = id / (mp.Hkv * mp.MT);
-    const int g = (id / mp.MT) % mp.Hkv;
-    const int mt = id % mp.MT;
-    const int tid = threadIdx.x;
-    const Sched sch{mp.prefix_lens, mp.nb, mp.B, mp.Hkv, mp.NT, mp.MT, mp.max_pages * kPage};
-
-    if (tid < 32) {
-        const long long total = sched_total(sch, tid);
-        const long long C = active_ctas(total, mp.attn_grid);
-        const long long start_b = sched_prefix(sch, b, tid);
-        const int P = __ldg(mp.prefix_lens + b);
-        const int ht = head_tiles(sch, P);
-        int c0 = 0, c1 = 0, slot0 = 0;
-        if (ht > 0 && total > 0) {
-            long long r0 = start_b + (long long)g * ht;
-            for (int m = 0; m < mt; ++m) r0 += rowtile_tiles(P, mp.B, mp.NT, m);
-            const long long r1 = r0 + rowtile_tiles(P, mp.B, mp.NT, mt);
-            c0 = (int)(((r0 + 1) * C - 1) / total);
-            c1 = (int)((r1 * C - 1) / total);
-            slot0 = (r0 == total * c0 / C) ? 2 * c0 : 2 * c0 + 1;
-        }
-        if (tid == 0) {
-            sh_c0 = c0;
-            sh_c1 = c1;
-            sh_slot0 = slot0;
-        }
-    }
-    __syncthreads();
-    const int c0 = sh_c0, c1 = sh_c1, slot0 = sh_slot0;
-    if (c0 == c1) return;  // the attention kernel wrote this row tile itself
-
-    for (int row = 0; row < kM; ++row) {
-        const int i = mt * mp.NT + row / mp.G;
-        if (i >= mp.B) break;
-        const int h = g * mp.G + row % mp.G;
-        float m = -INFINITY;
-        for (int c = c0; c <= c1; ++c) {
-            const int slot = (c == c0) ? slot0 : 2 * c;
-            m = fmaxf(m, mp.ws_lse[(size_t)slot * kM + row]);
-        }
-        float lse = -INFINITY, acc = 0.f;
-        if (m != -INFINITY) {
-            float sum = 0.f;
-            for (int c = c0; c <= c1; ++c) {
-                const int slot = (c == c0) ? slot0 : 2 * c;
-                sum += expf(mp.ws_lse[(size_t)slot * kM + row] - m);
-            }
-            lse = m + logf(sum);
-            for (int c = c0; c <= c1; ++c) {
-                const int slot = (c == c0) ? slot0 : 2 * c;
-                const float w = expf(mp.ws_lse[(size_t)slot * kM + row] - lse);
-                acc += w * mp.ws_o[((size_t)slot * kM + row) * kHeadDim + tid];
-            }
-        }
-        const size_t orow = ((size_t)b * mp.B + i) * mp.Hq + h;
-        const uint32_t bits = pack_bf16x2(acc, 0.f) & 0xFFFFu;
-        mp.o[orow * kHeadDim + tid] = (uint16_t)bits;
-        if (tid == 0) mp.lse[orow] = lse;
-    }
 }
 
 // ------------------------------------------------------------------ host side
@@ -721,7 +717,26 @@ static EncodeTiledFn encode_fn()
     return fn;
 }
 
-size_t attn_workspace_bytes(int ctas) { return (size_t)2 * ctas * kM * (kHeadDim + 1) * sizeof(float); }
+size_t attn_workspace_bytes(int ctas, int row_tiles)
+{
+    return (size_t)2 * ctas * kM * (kHeadDim + 1) * sizeof(float) + (size_t)row_tiles * sizeof(unsigned long long);
+}
+
+int attn_row_tiles(const tv_attn_args *a)
+{
+    const int NT = kM / (a->Hq / a->Hkv);
+    return a->nb * a->Hkv * ((a->B + NT - 1) / NT);
+}
+
+// Every call gets its own ticket epoch, so tickets left by an earlier (even an
+// interrupted) call never count towards this one.
+static uint32_t next_epoch()
+{
+    static std::atomic<uint32_t> counter{0};
+    uint32_t e = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+    if (e == 0) e = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+    return e;
+}
 
 int32_t launch_attn(const tv_attn_args *a, int ctas, void *workspace, cudaStream_t stream, cudaError_t *cuda_err)
 {
@@ -772,6 +787,8 @@ int32_t launch_attn(const tv_attn_args *a, int ctas, void *workspace, cudaStream
     p.status = a->dev_status_d;
     p.ws_o = static_cast<float *>(workspace);
     p.ws_lse = p.ws_o + (size_t)2 * ctas * kM * kHeadDim;
+    p.tickets = reinterpret_cast<unsigned long long *>(p.ws_lse + (size_t)2 * ctas * kM);
+    p.epoch = next_epoch();
     p.nb = a->nb;
     p.B = a->B;
     p.Hq = a->Hq;
@@ -788,12 +805,6 @@ int32_t launch_attn(const tv_attn_args *a, int ctas, void *workspace, cudaStream
     cudaError_t e = cudaFuncSetAttribute(tree_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e == cudaSuccess) {
         tree_attn_kernel<<<ctas, kThreads, kSmemBytes, stream>>>(p);
-        e = cudaGetLastError();
-    }
-    if (e == cudaSuccess) {
-        MergeParams mp{a->prefix_lens_d, p.ws_o, p.ws_lse, p.o, p.lse, p.nb, p.B, p.Hq, p.Hkv, p.G, p.NT, p.MT,
-                       p.max_pages, ctas};
-        tree_attn_merge_kernel<<<a->nb * a->Hkv * p.MT, kHeadDim, 0, stream>>>(mp);
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) {

@@ -13,14 +13,19 @@ namespace tv {
 cudaError_t launch_build_mask(const int32_t *parent, int B, int nb, uint32_t *mask, int32_t *depth, int32_t *status,
                               cudaStream_t stream);
 
+// Workspace bytes tv_accept needs: one 8-byte partial per (row, 8192-logit chunk).
+size_t accept_workspace_bytes(int V, int B, int nb);
+
 cudaError_t launch_accept(const uint16_t *logits, int V, const int32_t *draft, const int32_t *parent,
                           const uint32_t *mask, int B, int nb, int32_t *am, int32_t *n_acc, int32_t *path,
-                          int32_t *bonus, int32_t *status, cudaStream_t stream);
+                          int32_t *bonus, int32_t *status, void *workspace, int num_sms, cudaStream_t stream);
 
-// Workspace bytes the attention needs with `ctas` CTAs.
-size_t attn_workspace_bytes(int ctas);
+// Workspace bytes the attention needs with `ctas` CTAs over `row_tiles`
+// (sequence, kv head, 128-row tile) units, and that unit count for `a`.
+size_t attn_workspace_bytes(int ctas, int row_tiles);
+int attn_row_tiles(const tv_attn_args *a);
 
-// Encodes the TMA descriptors and launches the attention and merge kernels.
+// Encodes the TMA descriptors and launches the attention kernel.
 // Returns TV_OK or TV_ERR_CUDA (with *cuda_err set).
 int32_t launch_attn(const tv_attn_args *a, int ctas, void *workspace, cudaStream_t stream, cudaError_t *cuda_err);
 
