@@ -6,13 +6,14 @@
 // draft token equals the target argmax at the parent; the deepest accepted
 // node wins, ties to the smallest index.
 //
-// argmax (kernel 1): the logits are cut into (row, 8192-element chunk) units
-// and a one-wave grid walks them, so every SM streams the same number of
-// bytes whatever the row count.  A unit is one 16-byte-vector batch per
-// thread: bf16x2 NaN-propagating max instructions reduce it (about one per two
-// logits), the CTA agrees on the unit's maximum, and only the threads that
-// hold it search for its first position.  One (value, index) partial per unit
-// goes to the caller's workspace.
+// argmax (kernel 1): the logits are cut into (row, 2048-element chunk) units,
+// one warp per unit, and a one-wave grid walks them, so every SM streams the
+// same number of bytes whatever the row count.  A lane holds 8 16-byte vectors
+// of its unit in registers (all in flight at once); bf16x2 NaN-propagating max
+// instructions reduce them (about one per two logits), the warp agrees on the
+// unit's maximum with shuffles, and only the lanes holding it look for its
+// first position.  One (value, index) partial per unit goes to the caller's
+// workspace.
 //
 // accept (kernel 2): one CTA per sequence, one thread per node.  Each thread
 // finishes its row's argmax from the chunk partials, then ok[] is packed into
@@ -28,8 +29,8 @@
 namespace tv {
 
 constexpr int kArgThreads = 256;
-constexpr int kArgChunk = 8192;   // logits per unit (16 KB)
-constexpr int kArgBatch = 4;      // 16-byte vectors per thread per batch
+constexpr int kArgVec = 8;                    // 16-byte vectors per lane per unit
+constexpr int kArgChunk = 32 * kArgVec * 8;   // logits per unit (4 KB): one warp
 constexpr int kArgCtasPerSm = 8;
 constexpr int kMaxB = 256;
 constexpr int kMaxW = kMaxB / 32;
@@ -45,6 +46,14 @@ __device__ __forceinline__ bool beats(float av, int ai, float bv, int bi)
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
+// Streaming 16-byte load (evict-first); volatile so a batch of them is issued back to back.
+__device__ __forceinline__ uint4 ld_stream_v4(const uint4 *p)
+{
+    uint4 v;
+    asm volatile("ld.global.cs.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ unsigned long long pack_best(float v, int i)
 {
     return ((unsigned long long)(uint32_t)i << 32) | __float_as_uint(v);
@@ -53,21 +62,23 @@ __device__ __forceinline__ unsigned long long pack_best(float v, int i)
 // max with a NaN counting as the largest value
 __device__ __forceinline__ float max_nan(float a, float b) { return (a != a) ? a : ((b != b) ? b : fmaxf(a, b)); }
 
-// One unit = one batch: every thread holds its kArgBatch vectors in registers,
-// the CTA first agrees on the unit's maximum value, and only the threads that
-// hold that value look for its first position.
+// One unit = kArgChunk logits of one row = one warp: each lane holds kArgVec
+// 16-byte vectors in registers (all loads in flight at once) and keeps the
+// maximum of each vector; the warp agrees on the unit's maximum with shuffles,
+// and the lanes holding it find its first position in two steps (first vector
+// whose maximum matches, then the element inside it).  No block-level
+// synchronisation.
 __global__ void __launch_bounds__(kArgThreads) argmax_partial_kernel(const uint16_t *__restrict__ logits, long long V,
                                                                      int nchunk, long long units,
                                                                      unsigned long long *__restrict__ part)
 {
-    static_assert(kArgChunk == kArgThreads * kArgBatch * 8, "one batch per unit");
-    __shared__ float s_v[kArgThreads / 32];
-    __shared__ int s_i[kArgThreads / 32];
-    const int tid = threadIdx.x;
-    const int lane = tid & 31, wid = tid >> 5;
+    static_assert(kArgChunk == 32 * kArgVec * 8, "one warp per unit");
+    static_assert(kArgVec == 8, "the dependency point below lists 8 vectors");
+    const int lane = threadIdx.x & 31;
+    const long long warps = (long long)gridDim.x * (kArgThreads / 32);
     const float NEG_INF = -__int_as_float(0x7f800000);
 
-    for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+    for (long long u = (long long)blockIdx.x * (kArgThreads / 32) + (threadIdx.x >> 5); u < units; u += warps) {
         const long long row_id = u / nchunk;
         const long long lo = (u - row_id * nchunk) * (long long)kArgChunk;
         const long long hi = (lo + kArgChunk < V) ? lo + kArgChunk : V;
@@ -77,68 +88,80 @@ __global__ void __launch_bounds__(kArgThreads) argmax_partial_kernel(const uint1
         long long head = (long long)(((16u - ((uint32_t)(uintptr_t)(row + lo) & 15u)) & 15u) >> 1);
         if (head > hi - lo) head = hi - lo;
         const long long vstart = lo + head;
-        const long long nvec = (hi - vstart) / 8;
-        const long long tail = vstart + nvec * 8;
+        const int nvec = (int)((hi - vstart) / 8);
+        const long long tail = vstart + (long long)nvec * 8;
         const uint4 *vp = reinterpret_cast<const uint4 *>(row + vstart);
-        uint4 v[kArgBatch];
-        bool valid[kArgBatch];
+        uint4 v[kArgVec];
+        if (nvec > 0) {
 #pragma unroll
-        for (int k = 0; k < kArgBatch; ++k) {
-            const long long idx = tid + (long long)k * kArgThreads;
-            valid[k] = idx < nvec;
-            v[k] = valid[k] ? __ldcs(vp + idx) : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+            for (int k = 0; k < kArgVec; ++k) {
+                const int idx = lane + k * 32;
+                v[k] = ld_stream_v4(vp + (idx < nvec ? idx : nvec - 1));
+            }
+            // one dependency point for all loads: nothing below is scheduled between them
+            asm volatile("" : "+r"(v[0].x), "+r"(v[0].y), "+r"(v[0].z), "+r"(v[0].w), "+r"(v[1].x), "+r"(v[1].y),
+                         "+r"(v[1].z), "+r"(v[1].w), "+r"(v[2].x), "+r"(v[2].y), "+r"(v[2].z), "+r"(v[2].w),
+                         "+r"(v[3].x), "+r"(v[3].y), "+r"(v[3].z), "+r"(v[3].w), "+r"(v[4].x), "+r"(v[4].y),
+                         "+r"(v[4].z), "+r"(v[4].w), "+r"(v[5].x), "+r"(v[5].y), "+r"(v[5].z), "+r"(v[5].w),
+                         "+r"(v[6].x), "+r"(v[6].y), "+r"(v[6].z), "+r"(v[6].w), "+r"(v[7].x), "+r"(v[7].y),
+                         "+r"(v[7].z), "+r"(v[7].w));
         }
-        const bool has_head = tid < head, has_tail = tid < hi - tail;
-        const float xh = has_head ? bf16_bits_to_float(row[lo + tid]) : NEG_INF;
-        const float xt = has_tail ? bf16_bits_to_float(row[tail + tid]) : NEG_INF;
+        const bool has_head = lane < head, has_tail = lane < hi - tail;
+        const float xh = has_head ? bf16_bits_to_float(row[lo + lane]) : NEG_INF;
+        const float xt = has_tail ? bf16_bits_to_float(row[tail + lane]) : NEG_INF;
 
-        __nv_bfloat162 m2 = *reinterpret_cast<__nv_bfloat162 *>(&v[0].x);
+        float vm[kArgVec];  // maximum of each vector (NaN-propagating)
+        float tm = max_nan(xh, xt);
 #pragma unroll
-        for (int k = 0; k < kArgBatch; ++k) {
-            m2 = __hmax2_nan(m2, *reinterpret_cast<__nv_bfloat162 *>(&v[k].x));
-            m2 = __hmax2_nan(m2, *reinterpret_cast<__nv_bfloat162 *>(&v[k].y));
-            m2 = __hmax2_nan(m2, *reinterpret_cast<__nv_bfloat162 *>(&v[k].z));
-            m2 = __hmax2_nan(m2, *reinterpret_cast<__nv_bfloat162 *>(&v[k].w));
+        for (int k = 0; k < kArgVec; ++k) {
+            if (lane + k * 32 < nvec) {
+                __nv_bfloat162 a = __hmax2_nan(*reinterpret_cast<__nv_bfloat162 *>(&v[k].x),
+                                               *reinterpret_cast<__nv_bfloat162 *>(&v[k].y));
+                const __nv_bfloat162 c = __hmax2_nan(*reinterpret_cast<__nv_bfloat162 *>(&v[k].z),
+                                                     *reinterpret_cast<__nv_bfloat162 *>(&v[k].w));
+                a = __hmax2_nan(a, c);
+                vm[k] = __bfloat162float(__hmax_nan(a.x, a.y));
+            } else {
+                vm[k] = NEG_INF;
+            }
+            tm = max_nan(tm, vm[k]);
         }
-        float tm = max_nan(max_nan(__bfloat162float(__hmax_nan(m2.x, m2.y)), xh), xt);
-
-        // the unit's maximum value
         float bm = tm;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) bm = max_nan(bm, __shfl_xor_sync(0xffffffffu, bm, o));
-        if (lane == 0) s_v[wid] = bm;
-        __syncthreads();
-        bm = s_v[0];
-#pragma unroll
-        for (int w = 1; w < kArgThreads / 32; ++w) bm = max_nan(bm, s_v[w]);
         const bool bm_nan = bm != bm;
 
-        // the first position holding it (elements in index order: head, vectors, tail)
+        // first position of the unit maximum (elements in index order: head, vectors, tail)
         int idx = 0x7fffffff;
         if (bm_nan ? (tm != tm) : (tm == bm)) {
-            if (has_head && (bm_nan ? (xh != xh) : (xh == bm))) idx = (int)(lo + tid);
+            if (has_head && (bm_nan ? (xh != xh) : (xh == bm))) {
+                idx = (int)(lo + lane);
+            } else {
+                int kf = -1;
 #pragma unroll
-            for (int k = 0; k < kArgBatch; ++k) {
-                const uint32_t w4[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+                for (int k = kArgVec - 1; k >= 0; --k)
+                    if (lane + k * 32 < nvec && (bm_nan ? (vm[k] != vm[k]) : (vm[k] == bm))) kf = k;
+                if (kf >= 0) {
+                    uint4 w = v[0];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float x = bf16_bits_to_float((w4[e >> 1] >> ((e & 1) * 16)) & 0xFFFFu);
-                    const int pos = (int)(vstart + (tid + (long long)k * kArgThreads) * 8 + e);
-                    if (valid[k] && (bm_nan ? (x != x) : (x == bm))) idx = min(idx, pos);
+                    for (int k = 1; k < kArgVec; ++k)
+                        if (k == kf) w = v[k];
+                    const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+                    int e_first = 8;
+#pragma unroll
+                    for (int e = 7; e >= 0; --e) {
+                        const float x = bf16_bits_to_float((w4[e >> 1] >> ((e & 1) * 16)) & 0xFFFFu);
+                        if (bm_nan ? (x != x) : (x == bm)) e_first = e;
+                    }
+                    idx = (int)(vstart + (long long)(lane + kf * 32) * 8 + e_first);
+                } else if (has_tail) {
+                    idx = (int)(tail + lane);
                 }
             }
-            if (has_tail && (bm_nan ? (xt != xt) : (xt == bm))) idx = min(idx, (int)(tail + tid));
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) idx = min(idx, __shfl_xor_sync(0xffffffffu, idx, o));
-        if (lane == 0) s_i[wid] = idx;
-        __syncthreads();
-        if (tid == 0) {
-#pragma unroll
-            for (int w = 1; w < kArgThreads / 32; ++w) idx = min(idx, s_i[w]);
-            part[u] = pack_best(bm, idx);
-        }
-        __syncthreads();
+        if (lane == 0) part[u] = pack_best(bm, idx);
     }
 }
 
@@ -161,23 +184,39 @@ __global__ void __launch_bounds__(kMaxB) accept_kernel(const unsigned long long 
     const int lane = i & 31, wid = i >> 5;
     if (i == 0) s_bad = 0;
 
-    // finish the argmax of row (b, i) from its chunk partials
-    if (i < B) {
-        const unsigned long long *pr = part + ((size_t)b * B + i) * nchunk;
-        unsigned long long pk = pr[0];
-        float bv = __uint_as_float((uint32_t)pk);
-        int bi = (int)(pk >> 32);
-        for (int c = 1; c < nchunk; ++c) {
-            pk = pr[c];
-            const float v = __uint_as_float((uint32_t)pk);
-            const int ix = (int)(pk >> 32);
-            if (beats(v, ix, bv, bi)) {
-                bv = v;
-                bi = ix;
+    // finish every row's argmax from its chunk partials: lpr threads per row,
+    // each striding over the partials, then a shuffle reduction within the group
+    {
+        int lpr = 1;
+        while (lpr < 32 && lpr * 2 * B <= (int)blockDim.x) lpr *= 2;
+        const int r = i / lpr, sub = i % lpr;
+        float bv = __int_as_float(0xff800000);
+        int bi = 0x7fffffff;
+        if (r < B) {
+            const unsigned long long *pr = part + ((size_t)b * B + r) * nchunk;
+#pragma unroll 4
+            for (int c = sub; c < nchunk; c += lpr) {
+                const unsigned long long pk = __ldcg(pr + c);
+                const float v = __uint_as_float((uint32_t)pk);
+                const int ix = (int)(pk >> 32);
+                if (beats(v, ix, bv, bi)) {
+                    bv = v;
+                    bi = ix;
+                }
             }
         }
-        s_am[i] = bi;
-        am[(size_t)b * B + i] = bi;
+        for (int o = lpr >> 1; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (beats(ov, oi, bv, bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if (r < B && sub == 0) {
+            s_am[r] = bi;
+            am[(size_t)b * B + r] = bi;
+        }
     }
     __syncthreads();
 
@@ -253,15 +292,15 @@ cudaError_t launch_accept(const uint16_t *logits, int V, const int32_t *draft, c
     const int nchunk = (int)(((long long)V + kArgChunk - 1) / kArgChunk);
     const long long units = (long long)nb * B * nchunk;
     long long grid = (long long)num_sms * kArgCtasPerSm;
-    if (grid > units) grid = units;
+    const long long need = (units + kArgThreads / 32 - 1) / (kArgThreads / 32);
+    if (grid > need) grid = need;
     if (grid < 1) grid = 1;
     unsigned long long *part = static_cast<unsigned long long *>(workspace);
     argmax_partial_kernel<<<(unsigned)grid, kArgThreads, 0, stream>>>(logits, V, nchunk, units, part);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int W = (B + 31) / 32;
-    const int threads = ((B + 31) / 32) * 32;
-    accept_kernel<<<nb, threads, 0, stream>>>(part, nchunk, draft, parent, mask, B, W, am, n_acc, path, bonus,
+    accept_kernel<<<nb, kMaxB, 0, stream>>>(part, nchunk, draft, parent, mask, B, W, am, n_acc, path, bonus,
                                               status);
     return cudaGetLastError();
 }

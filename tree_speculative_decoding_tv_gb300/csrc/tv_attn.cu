@@ -9,31 +9,40 @@
 // the paged cache; O in bf16, LSE = ln sum exp(scaled scores) in fp32.
 //
 // GB300 design
-//   * Work unit ("row tile"): one (sequence, kv head, M tile) with the queries
-//     of all G query heads of that kv head packed node-major into 128 rows
-//     (row = node_local * G + head_in_group), so each K/V page is read once per
-//     (sequence, kv head) and QK^T / PV are 128 x 128 x 128 tcgen05 MMAs.
-//   * Stream-K over KV tiles of 128 keys (8 pages): every CTA takes an equal
-//     contiguous share of all (row tile, KV tile) pairs, computed in-kernel
-//     from prefix_lens (ragged prefixes balance by construction).  A row tile
-//     cut between CTAs leaves fp32 partials (normalised O, LSE) in the
-//     workspace; each piece then takes a ticket (an epoch-tagged counter per
-//     row tile) and the last piece to arrive merges them, so no CTA ever
-//     waits for another and no extra launch is needed.
-//   * Warp roles per CTA (256 threads): warp 0 issues TMA (Q once per row tile
-//     through a 4-D map whose node axis stops at B; K and V one 16-key page x
-//     64-column box at a time through a 2-D map over [pages*Hkv*16][D], page ids
-//     from the block table, OOB rows zero-filled); warp 1 allocates TMEM and
-//     issues tcgen05.mma; warps 4-7 own one TMEM lane = one query row each and
-//     run the masked online softmax and the epilogue.
-//   * TMEM: two S buffers (128 columns each) so QK^T of tile j+1 overlaps the
-//     softmax of tile j, and the O accumulator (128 columns).  P goes to shared
-//     memory (bf16, 128-byte swizzled, K-major) and feeds the PV MMA; V is the
-//     MN-major B operand.
+//   * Rows: the queries of all G query heads of one kv head are packed
+//     node-major into 128-row M tiles (row = node_local * G + head_in_group),
+//     so each K/V page is read once per (sequence, kv head).  A CTA works on a
+//     PAIR of M tiles (A = 2mp, B = 2mp + 1) of the same (sequence, kv head):
+//     every K/V tile it loads feeds both, halving K/V traffic per MMA.
+//   * Stream-K: the (pair tile, 128-key KV tile) items of all sequences are
+//     cut into equal contiguous shares, one per CTA, computed in-kernel from
+//     prefix_lens, so ragged prefixes balance by construction.  A pair tile cut
+//     between CTAs leaves fp32 partials (normalised O, LSE) in the workspace,
+//     and a merge kernel launched as a programmatic dependent of this one
+//     combines them with every SM at once (its launch overlaps this kernel's
+//     tail; no CTA ever waits on another).
+//   * Warp roles (384 threads): warp 0 issues TMA (Q by a 4-D map whose node
+//     axis stops at B; K/V one 16-key page x 64 columns per copy through a 2-D
+//     map over [pages*Hkv*16][D], page ids from the block table, rows past the
+//     needed keys zero-filled); warp 1 owns TMEM and issues tcgen05.mma;
+//     warpgroups 1 and 2 run the softmax of tiles A and B, one TMEM lane (one
+//     query row) per thread.  setmaxnreg moves registers from warpgroup 0 to
+//     the softmax warpgroups.
+//   * TMEM (512 columns): S_A, O_A, S_B, O_B, 128 columns each.  The softmax
+//     writes P (bf16) back over the first 64 columns of its S and the PV MMA
+//     reads A = P straight from TMEM; V is the MN-major B operand in shared
+//     memory.  Issue order per KV tile j: PV_A(j), QK_A(j+1), PV_B(j),
+//     QK_B(j+1), so each softmax warpgroup works while the tensor core runs the
+//     other tile's two MMAs.
+//   * A pair whose second M tile does not exist (B rows fit one tile) runs in
+//     single-tile mode: both softmax warpgroups serve M tile A, warpgroup x
+//     taking the KV tiles with index % 2 == x into S_x / O_x, and warpgroup A
+//     combines the two halves (O_A, O_B read straight from TMEM) at the end, so
+//     softmax and MMAs still overlap.
 //   * The ancestor bitmask is read only for KV tiles that reach the tree block
-//     [P_b, P_b + B); prefix tiles are unmasked.  The running max is only moved
-//     (and O in TMEM rescaled) when a row's max grows by more than 2^8, so the
-//     rescale is rare after the first tiles.
+//     [P_b, P_b + B); prefix tiles are unmasked.  A row's running max only
+//     moves (and O in TMEM is rescaled) when it grows by more than 2^8.  The
+//     commit behind S(j) also covers PV(j-1), so that rescale needs no wait.
 //   * Every wait is bounded (tv_device.cuh): a stuck pipeline reports
 //     TV_ERR_TIMEOUT and the CTA still frees its TMEM.
 #include <cuda.h>
@@ -48,42 +57,47 @@
 
 namespace tv {
 
-constexpr int kM = 128;        // query rows per tile
+constexpr int kM = 128;        // query rows per M tile
 constexpr int kN = 128;        // keys per KV tile
 constexpr int kHeadDim = 128;  // D
 constexpr int kPage = 16;      // tokens per KV page
-constexpr int kStages = 2;     // K and V ring depth
-constexpr int kThreads = 256;
+constexpr int kSlots = 5;      // K/V ring: K(j) -> slot (2j) % 5, V(j) -> slot (2j + 1) % 5
+constexpr int kThreads = 384;
 constexpr int kMinTilesPerCta = 2;
+constexpr uint32_t kRegsLow = 64;    // warpgroup 0 after setmaxnreg.dec (128 x 64 + 256 x 216 <= 384 x 168)
+constexpr uint32_t kRegsHigh = 216; // softmax warpgroups after setmaxnreg.inc
 
 constexpr uint32_t kTileBytes = kM * kHeadDim * 2;  // 32 KB: a 128 x 128 bf16 tile
 constexpr uint32_t kHalfBytes = kTileBytes / 2;     // one 64-column (128-byte) swizzle column block
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kTileBytes;
-constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
-constexpr uint32_t kOffP = kOffV + kStages * kTileBytes;
-constexpr uint32_t kOffBar = kOffP + 2 * kTileBytes;
+constexpr uint32_t kOffQ = 0;                       // Q_A, Q_B
+constexpr uint32_t kOffKV = kOffQ + 2 * kTileBytes;
+constexpr uint32_t kOffBar = kOffKV + kSlots * kTileBytes;
 
 enum : int {
     BAR_Q_FULL = 0,
     BAR_Q_EMPTY,
-    BAR_K_FULL,                    // + stage
-    BAR_K_EMPTY = BAR_K_FULL + 2,  // + stage
-    BAR_V_FULL = BAR_K_EMPTY + 2,
-    BAR_V_EMPTY = BAR_V_FULL + 2,
-    BAR_S_FULL = BAR_V_EMPTY + 2,  // + S buffer
-    BAR_P_FULL = BAR_S_FULL + 2,   // + P buffer
-    BAR_PV_DONE = BAR_P_FULL + 2,  // + P buffer: PV of that buffer's tile completed
-    BAR_O_EMPTY = BAR_PV_DONE + 2,
-    BAR_MMA_DONE,
+    BAR_KV_FULL,                         // + slot
+    BAR_KV_EMPTY = BAR_KV_FULL + kSlots,  // + slot
+    BAR_S_FULL = BAR_KV_EMPTY + kSlots,   // + tile (A = 0, B = 1)
+    BAR_P_FULL = BAR_S_FULL + 2,    // + tile
+    BAR_PV_DONE = BAR_P_FULL + 2,   // + tile
+    BAR_O_EMPTY = BAR_PV_DONE + 2,  // + tile
+    BAR_MMA_DONE = BAR_O_EMPTY + 2,
+    BAR_ML_FULL,   // single-tile segments: slot 1's (max, sum) are in shared memory
+    BAR_ML_READ,   // single-tile segments: slot 0 has read O_1 and the (max, sum)
     BAR_COUNT
 };
 constexpr uint32_t kOffMisc = kOffBar + BAR_COUNT * 8;
-constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + slack to align the base to 1024 bytes
+constexpr uint32_t kOffML = kOffMisc + 128;  // [2][128] floats: slot 1's row max / sum in single-tile segments
+
+// Position q of the K/V load sequence (q = 2j for K(j), 2j + 1 for V(j)).
+__device__ __forceinline__ uint32_t ring_slot(uint32_t q) { return q % kSlots; }
+__device__ __forceinline__ uint32_t ring_phase(uint32_t q) { return (q / kSlots) & 1; }
+constexpr uint32_t kSmemBytes = kOffML + 1024 + 1024;  // + slack to align the base to 1024 bytes
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 0;    // S buffer x at column x * 128
-constexpr uint32_t kTmemO = 256;  // O accumulator
+__host__ __device__ constexpr uint32_t tmem_s(int x) { return (uint32_t)x * 256; }        // S_x, P_x over its first 64
+__host__ __device__ constexpr uint32_t tmem_o(int x) { return (uint32_t)x * 256 + 128; }  // O_x
 
 constexpr uint32_t kIdescQK = umma_idesc_bf16(kM, kN, 0);        // B = K tile, K-major
 constexpr uint32_t kIdescPV = umma_idesc_bf16(kM, kHeadDim, 1);  // B = V tile, MN-major
@@ -100,10 +114,8 @@ struct AttnParams {
     uint16_t *o;
     float *lse;
     int32_t *status;
-    float *ws_o;    // [2 * grid][128][128] fp32 partial O (normalised)
-    float *ws_lse;  // [2 * grid][128]
-    unsigned long long *tickets;  // [nb * Hkv * MT]: (epoch << 32) | pieces that have arrived
-    uint32_t epoch;               // distinct for every call
+    float *ws_o;    // [2 * grid][2 tiles][32 chunks][128 rows][4] fp32 partial O (normalised)
+    float *ws_lse;  // [2 * grid][2 tiles][128]
     int nb, B, Hq, Hkv, G, NT, MT, W, max_pages, num_blocks;
     float scale_log2;
 };
@@ -115,19 +127,25 @@ struct Sched {
     int nb, B, Hkv, NT, MT, max_tokens;
 };
 
-__device__ __forceinline__ int rowtile_tiles(int P, int B, int NT, int mt)
+__device__ __forceinline__ int mtile_tiles(int P, int B, int NT, int mt)
 {
     const int kv_end = min(B, (mt + 1) * NT);  // tree keys a node of this M tile can see end here
     return (P + kv_end + kN - 1) / kN;
 }
 
-// KV tiles of one (sequence, kv head); 0 for a sequence whose prefix does not
-// fit its block table (reported as TV_ERR_INVALID_ARG).
+// KV tiles of pair tile mp (its later M tile needs the most keys).
+__device__ __forceinline__ int pair_tiles(const Sched &s, int P, int mp)
+{
+    return mtile_tiles(P, s.B, s.NT, min(2 * mp + 1, s.MT - 1));
+}
+
+// Items of one (sequence, kv head); 0 for a sequence whose prefix does not fit
+// its block table (reported as TV_ERR_INVALID_ARG).
 __device__ __forceinline__ int head_tiles(const Sched &s, int P)
 {
     if (P < 0 || P > s.max_tokens - s.B) return 0;
     int t = 0;
-    for (int mt = 0; mt < s.MT; ++mt) t += rowtile_tiles(P, s.B, s.NT, mt);
+    for (int mp = 0; 2 * mp < s.MT; ++mp) t += pair_tiles(s, P, mp);
     return t;
 }
 
@@ -138,7 +156,7 @@ __device__ __forceinline__ long long warp_sum_ll(long long v)
     return v;
 }
 
-// Total (row tile, KV tile) pairs.  Whole warp.
+// Total items.  Whole warp.
 __device__ long long sched_total(const Sched &s, int lane)
 {
     long long tot = 0;
@@ -150,7 +168,7 @@ __device__ long long sched_total(const Sched &s, int lane)
     return tot;
 }
 
-// Sequence and offset inside it of global pair index t (t < total).  Whole warp.
+// Sequence and offset inside it of global item index t (t < total).  Whole warp.
 __device__ void sched_locate(const Sched &s, long long t, int lane, int &b_out, long long &off_out)
 {
     long long acc = 0;
@@ -177,7 +195,7 @@ __device__ void sched_locate(const Sched &s, long long t, int lane, int &b_out, 
     off_out = 0;
 }
 
-// CTAs that get work: at least kMinTilesPerCta pairs each, at most the grid.
+// CTAs that get work: at least kMinTilesPerCta items each, at most the grid.
 __device__ __forceinline__ long long active_ctas(long long total, int grid)
 {
     long long c = (total + kMinTilesPerCta - 1) / kMinTilesPerCta;
@@ -187,16 +205,17 @@ __device__ __forceinline__ long long active_ctas(long long total, int grid)
 
 struct Cursor {
     int b;
-    long long off;   // pair offset inside sequence b
-    long long left;  // pairs this CTA still has to visit
+    long long off;   // item offset inside sequence b
+    long long left;  // items this CTA still has to visit
 };
 
 struct Seg {
-    int b, g, mt, j0, j1, n_row, P;
+    int b, g, mp, j0, j1, n_row, P;
+    bool has_b;
 };
 
-// Next segment (a run of KV tiles of one row tile) of this CTA's share.
-// Row tiles are ordered (sequence, kv head, M tile), KV tiles ascending.
+// Next segment (a run of KV tiles of one pair tile) of this CTA's share.
+// Pair tiles are ordered (sequence, kv head, pair), KV tiles ascending.
 __device__ __forceinline__ bool next_seg(const Sched &s, Cursor &c, Seg &sg)
 {
     while (c.left > 0 && c.b < s.nb) {
@@ -209,21 +228,22 @@ __device__ __forceinline__ bool next_seg(const Sched &s, Cursor &c, Seg &sg)
         }
         const int g = (int)(c.off / ht);
         int rem = (int)(c.off - (long long)g * ht);
-        int mt = 0;
-        int n = rowtile_tiles(P, s.B, s.NT, 0);
+        int mp = 0;
+        int n = pair_tiles(s, P, 0);
         while (rem >= n) {
             rem -= n;
-            ++mt;
-            n = rowtile_tiles(P, s.B, s.NT, mt);
+            ++mp;
+            n = pair_tiles(s, P, mp);
         }
         const int take = (int)min((long long)(n - rem), c.left);
         sg.b = c.b;
         sg.g = g;
-        sg.mt = mt;
+        sg.mp = mp;
         sg.j0 = rem;
         sg.j1 = rem + take;
         sg.n_row = n;
         sg.P = P;
+        sg.has_b = 2 * mp + 1 < s.MT;
         c.off += take;
         c.left -= take;
         return true;
@@ -253,7 +273,7 @@ __device__ __forceinline__ uint32_t visible_bits(int kstart, int P, int B, const
     return v;
 }
 
-// ------------------------------------------------------------------ kernels
+// ------------------------------------------------------------------ kernel
 
 __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_constant__ AttnParams p)
 {
@@ -261,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
-    const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV, sP = base + kOffP;
+    const uint32_t sQ = base + kOffQ, sKV = base + kOffKV;
     const uint32_t sBar = base + kOffBar;
 #define BAR(i) (sBar + 8u * (uint32_t)(i))
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kOffMisc);
@@ -269,10 +289,6 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
     int *sh_b0 = reinterpret_cast<int *>(gbase + kOffMisc + 8);
     long long *sh_off0 = reinterpret_cast<long long *>(gbase + kOffMisc + 16);
     long long *sh_left = reinterpret_cast<long long *>(gbase + kOffMisc + 24);
-    long long *sh_total = reinterpret_cast<long long *>(gbase + kOffMisc + 32);
-    long long *sh_ctas = reinterpret_cast<long long *>(gbase + kOffMisc + 40);
-    long long *sh_t0 = reinterpret_cast<long long *>(gbase + kOffMisc + 48);
-    volatile int *sh_last = reinterpret_cast<volatile int *>(gbase + kOffMisc + 56);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -281,19 +297,19 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
     if (threadIdx.x == 0) {
         mbar_init(BAR(BAR_Q_FULL), 1);
         mbar_init(BAR(BAR_Q_EMPTY), 1);
-        for (int st = 0; st < kStages; ++st) {
-            mbar_init(BAR(BAR_K_FULL + st), 1);
-            mbar_init(BAR(BAR_K_EMPTY + st), 1);
-            mbar_init(BAR(BAR_V_FULL + st), 1);
-            mbar_init(BAR(BAR_V_EMPTY + st), 1);
+        for (int q = 0; q < kSlots; ++q) {
+            mbar_init(BAR(BAR_KV_FULL + q), 1);
+            mbar_init(BAR(BAR_KV_EMPTY + q), 1);
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(BAR(BAR_S_FULL + x), 1);
             mbar_init(BAR(BAR_P_FULL + x), kM);
             mbar_init(BAR(BAR_PV_DONE + x), 1);
+            mbar_init(BAR(BAR_O_EMPTY + x), kM);
         }
-        mbar_init(BAR(BAR_O_EMPTY), kM);
         mbar_init(BAR(BAR_MMA_DONE), 1);
+        mbar_init(BAR(BAR_ML_FULL), kM);
+        mbar_init(BAR(BAR_ML_READ), kM);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -322,9 +338,6 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
             *sh_b0 = b0;
             *sh_off0 = off0;
             *sh_left = t1 - t0;
-            *sh_total = total;
-            *sh_ctas = C;
-            *sh_t0 = t0;
         }
         if (blockIdx.x == 0) {
             for (int b = lane; b < sch.nb; b += 32) {
@@ -338,46 +351,67 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const Cursor cur0{*sh_b0, *sh_off0, *sh_left};
+    pdl_launch_dependents();
 
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
+        regs_decrease<kRegsLow>();
         Cursor cur = cur0;
         Seg sg;
-        uint32_t gt = 0, seg_i = 0;
+        uint32_t kv = 0, seg_i = 0;
         bool ok = true;
         const int oob_row = p.num_blocks * p.Hkv * kPage;  // first row past the cache: zero fill
         while (ok && next_seg(sch, cur, sg)) {
             if (seg_i > 0 && !mbar_wait(BAR(BAR_Q_EMPTY), (seg_i - 1) & 1, abort_flag, p.status)) break;
             if (lane == 0) {
-                mbar_arrive_expect_tx(BAR(BAR_Q_FULL), kTileBytes);
-                tma_load_4d(sQ, &p.tm_q, 0, sg.g * p.G, sg.mt * p.NT, sg.b, BAR(BAR_Q_FULL));
-                tma_load_4d(sQ + kHalfBytes, &p.tm_q, 64, sg.g * p.G, sg.mt * p.NT, sg.b, BAR(BAR_Q_FULL));
-            }
-            const int kv_len = sg.P + min(p.B, (sg.mt + 1) * p.NT);
-            for (int j = sg.j0; j < sg.j1; ++j, ++gt) {
-                const int st = gt & 1;
-                const uint32_t ph = (gt >> 1) & 1;
-                int row = oob_row;
-                if (lane < kN / kPage) {
-                    const int pg = j * (kN / kPage) + lane;
-                    if (pg * kPage < kv_len) {
-                        const int id = __ldg(p.block_table + (size_t)sg.b * p.max_pages + pg);
-                        if (id >= 0 && id < p.num_blocks)
-                            row = (id * p.Hkv + sg.g) * kPage;
-                        else
-                            report_status(p.status, TV_ERR_INVALID_ARG);
-                    }
+                mbar_arrive_expect_tx(BAR(BAR_Q_FULL), kTileBytes * (sg.has_b ? 2 : 1));
+                for (int x = 0; x < (sg.has_b ? 2 : 1); ++x) {
+                    const int node0 = (2 * sg.mp + x) * p.NT;
+                    tma_load_4d(sQ + x * kTileBytes, &p.tm_q, 0, sg.g * p.G, node0, sg.b, BAR(BAR_Q_FULL));
+                    tma_load_4d(sQ + x * kTileBytes + kHalfBytes, &p.tm_q, 64, sg.g * p.G, node0, sg.b,
+                                BAR(BAR_Q_FULL));
                 }
-                const int my_row = __shfl_sync(0xffffffffu, row, lane >> 1);
+            }
+            const int kv_len = sg.P + min(p.B, (2 * sg.mp + (sg.has_b ? 2 : 1)) * p.NT);
+            // Physical row of page pg for this kv head, or the zero-filled row past the cache.
+            // Lane l holds page (jb * 8 + l) of a 4-tile batch starting at tile jb; the next
+            // batch is requested one batch ahead so block-table latency stays off the TMA path.
+            auto page_row = [&](int jb) -> int {
+                const int pg = jb * (kN / kPage) + lane;
+                int r = oob_row;
+                if (pg * kPage < kv_len) {
+                    const int id = __ldg(p.block_table + (size_t)sg.b * p.max_pages + pg);
+                    if (id >= 0 && id < p.num_blocks)
+                        r = (id * p.Hkv + sg.g) * kPage;
+                    else
+                        report_status(p.status, TV_ERR_INVALID_ARG);
+                }
+                return r;
+            };
+            int rows_cur = page_row(sg.j0);
+            int rows_nxt = (sg.j0 + 4 < sg.j1) ? page_row(sg.j0 + 4) : oob_row;
+            for (int j = sg.j0; j < sg.j1; ++j, ++kv) {
+                const int in_batch = (j - sg.j0) & 3;
+                if (in_batch == 0 && j != sg.j0) {
+                    rows_cur = rows_nxt;
+                    rows_nxt = (j + 4 < sg.j1) ? page_row(j + 4) : oob_row;
+                }
+                const int my_row = __shfl_sync(0xffffffffu, rows_cur, in_batch * 8 + (lane >> 1));
                 const uint32_t dst_off = (uint32_t)(lane & 1) * kHalfBytes + (uint32_t)(lane >> 1) * (kPage * 128);
-                if (!mbar_wait(BAR(BAR_K_EMPTY + st), ph ^ 1, abort_flag, p.status)) { ok = false; break; }
-                if (lane == 0) mbar_arrive_expect_tx(BAR(BAR_K_FULL + st), kTileBytes);
-                __syncwarp();
-                if (lane < 16) tma_load_2d(sK + st * kTileBytes + dst_off, &p.tm_k, (lane & 1) * 64, my_row, BAR(BAR_K_FULL + st));
-                if (!mbar_wait(BAR(BAR_V_EMPTY + st), ph ^ 1, abort_flag, p.status)) { ok = false; break; }
-                if (lane == 0) mbar_arrive_expect_tx(BAR(BAR_V_FULL + st), kTileBytes);
-                __syncwarp();
-                if (lane < 16) tma_load_2d(sV + st * kTileBytes + dst_off, &p.tm_v, (lane & 1) * 64, my_row, BAR(BAR_V_FULL + st));
+                for (int kvh = 0; kvh < 2; ++kvh) {  // K(j), then V(j)
+                    const uint32_t q = 2 * kv + kvh;
+                    const uint32_t sl = ring_slot(q);
+                    if (!mbar_wait(BAR(BAR_KV_EMPTY + sl), ring_phase(q) ^ 1, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) mbar_arrive_expect_tx(BAR(BAR_KV_FULL + sl), kTileBytes);
+                    __syncwarp();
+                    if (lane < 16)
+                        tma_load_2d(sKV + sl * kTileBytes + dst_off, kvh ? (const void *)&p.tm_v : (const void *)&p.tm_k,
+                                    (lane & 1) * 64, my_row, BAR(BAR_KV_FULL + sl));
+                }
+                if (!ok) break;
             }
             ++seg_i;
         }
@@ -388,63 +422,103 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // Slots x = 0, 1 own S_x / O_x.  Pair segments: slot x is M tile x over every
+        // KV tile.  Single-tile segments: both slots use Q tile A, slot x takes the
+        // KV tiles t with t % 2 == x, and the softmax warpgroups merge at the end.
+        regs_decrease<kRegsLow>();
         Cursor cur = cur0;
         Seg sg;
-        uint32_t gt = 0, seg_i = 0;
+        uint32_t kv = 0, seg_i = 0;
+        uint32_t gs[2] = {0, 0}, sc[2] = {0, 0};  // tiles and segments per slot so far (barrier phases)
         bool ok = true;
-        auto issue_s = [&](uint32_t t) -> bool {
-            const int st = t & 1;
-            if (!mbar_wait(BAR(BAR_K_FULL + st), (t >> 1) & 1, abort_flag, p.status)) return false;
-            tc_fence_after();
-            if (lane == 0) {
-                const uint32_t kb = sK + st * kTileBytes;
+        auto issue_qk = [&](int x, int qx, uint32_t kt) {
+            const uint32_t qb = sQ + qx * kTileBytes, kb = sKV + ring_slot(2 * kt) * kTileBytes;
 #pragma unroll
-                for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                    umma_bf16_ss(tmem + kTmemS + st * 128, sdesc_kmajor_sw128(sQ + off),
-                                 sdesc_kmajor_sw128(kb + off), kIdescQK, kk > 0 ? 1u : 0u);
-                }
-                umma_commit(BAR(BAR_S_FULL + st));
-                umma_commit(BAR(BAR_K_EMPTY + st));
+            for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                umma_bf16_ss(tmem + tmem_s(x), sdesc_kmajor_sw128(qb + off), sdesc_kmajor_sw128(kb + off), kIdescQK,
+                             kk > 0 ? 1u : 0u);
             }
-            __syncwarp();
-            return true;
+            umma_commit(BAR(BAR_S_FULL + x));
+        };
+        auto issue_pv = [&](int x, uint32_t kt, bool accumulate) {
+            const uint32_t vb = sKV + ring_slot(2 * kt + 1) * kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < kN / 16; ++kk)
+                umma_bf16_ts(tmem + tmem_o(x), tmem + tmem_s(x) + kk * 8, sdesc_mnmajor_sw128(vb + kk * 2048, kHalfBytes),
+                             kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+            umma_commit(BAR(BAR_PV_DONE + x));
+        };
+        auto wait_k = [&](uint32_t kt) {
+            return mbar_wait(BAR(BAR_KV_FULL + ring_slot(2 * kt)), ring_phase(2 * kt), abort_flag, p.status);
         };
         while (ok && next_seg(sch, cur, sg)) {
             const int n = sg.j1 - sg.j0;
-            if (!mbar_wait(BAR(BAR_Q_FULL), seg_i & 1, abort_flag, p.status)) { ok = false; break; }
+            const bool pair = sg.has_b;
+            const int nx0 = pair ? n : (n + 1) / 2, nx1 = pair ? n : n / 2;
+            if (!mbar_wait(BAR(BAR_Q_FULL), seg_i & 1, abort_flag, p.status) || !wait_k(kv)) { ok = false; break; }
             tc_fence_after();
-            if (!issue_s(gt)) { ok = false; break; }
-            for (int t = 0; t < n; ++t) {
-                const uint32_t g_t = gt + t;
-                const int buf = g_t & 1;
-                if (t + 1 < n && !issue_s(g_t + 1)) { ok = false; break; }
-                if (t + 1 == n) {
-                    if (lane == 0) umma_commit(BAR(BAR_Q_EMPTY));
-                    __syncwarp();
-                }
-                if (!mbar_wait(BAR(BAR_P_FULL + buf), (g_t >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
-                if (t == 0 && seg_i > 0 && !mbar_wait(BAR(BAR_O_EMPTY), (seg_i - 1) & 1, abort_flag, p.status)) {
-                    ok = false;
-                    break;
-                }
-                if (!mbar_wait(BAR(BAR_V_FULL + buf), (g_t >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+            if (lane == 0) {
+                issue_qk(0, 0, kv);
+                if (pair) issue_qk(1, 1, kv);
+                umma_commit(BAR(BAR_KV_EMPTY + ring_slot(2 * kv)));
+            }
+            __syncwarp();
+            if (!pair && n > 1) {
+                if (!wait_k(kv + 1)) { ok = false; break; }
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t pb = sP + buf * kTileBytes;
-                    const uint32_t vb = sV + buf * kTileBytes;
-#pragma unroll
-                    for (int kk = 0; kk < kN / 16; ++kk) {
-                        umma_bf16_ss(tmem + kTmemO, sdesc_kmajor_sw128(pb + (kk >> 2) * kHalfBytes + (kk & 3) * 32),
-                                     sdesc_mnmajor_sw128(vb + kk * 2048, kHalfBytes), kIdescPV,
-                                     (t > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    umma_commit(BAR(BAR_V_EMPTY + buf));
-                    umma_commit(BAR(BAR_PV_DONE + buf));
+                    issue_qk(1, 0, kv + 1);
+                    umma_commit(BAR(BAR_KV_EMPTY + ring_slot(2 * kv + 2)));
                 }
                 __syncwarp();
             }
-            gt += n;
+            if (lane == 0 && ((pair && n == 1) || (!pair && n <= 2))) umma_commit(BAR(BAR_Q_EMPTY));
+            for (int t = 0; t < n && ok; ++t) {
+                const uint32_t kt = kv + t;
+                const int tn = t + (pair ? 1 : 2);  // the slot's next KV tile
+                for (int xi = 0; xi < (pair ? 2 : 1); ++xi) {
+                    const int x = pair ? xi : (t & 1);
+                    const int lx = pair ? t : (t >> 1);
+                    if (!mbar_wait(BAR(BAR_P_FULL + x), (gs[x] + lx) & 1, abort_flag, p.status)) { ok = false; break; }
+                    if (lx == 0 && sc[x] > 0 &&
+                        !mbar_wait(BAR(BAR_O_EMPTY + x), (sc[x] - 1) & 1, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    if (xi == 0 && !mbar_wait(BAR(BAR_KV_FULL + ring_slot(2 * kt + 1)), ring_phase(2 * kt + 1),
+                                              abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (lane == 0) issue_pv(x, kt, lx > 0);
+                    __syncwarp();
+                    // the next QK of this slot only waits for its K tile after PV(t) is queued
+                    if (tn < n) {
+                        if (xi == 0 && !wait_k(kv + tn)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        if (lane == 0) issue_qk(x, pair ? x : 0, kv + tn);
+                        __syncwarp();
+                    }
+                }
+                if (!ok) break;
+                if (lane == 0) {
+                    umma_commit(BAR(BAR_KV_EMPTY + ring_slot(2 * kt + 1)));
+                    if (tn < n) umma_commit(BAR(BAR_KV_EMPTY + ring_slot(2 * (kv + tn))));
+                    if (t + (pair ? 2 : 3) == n) umma_commit(BAR(BAR_Q_EMPTY));
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            kv += n;
+            gs[0] += nx0;
+            gs[1] += nx1;
+            if (nx0 > 0) ++sc[0];
+            if (nx1 > 0) ++sc[1];
             ++seg_i;
         }
         // Every MMA this CTA issued completes before TMEM is released.
@@ -454,34 +528,48 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
             const uint64_t t0 = global_timer_ns();
             while (!mbar_try_wait(BAR(BAR_MMA_DONE), 0) && global_timer_ns() - t0 < kWaitLimitNs) { }
         }
-    } else if (warp >= 4) {
-        // -------------------------------------------------- softmax and epilogue
-        const int row = threadIdx.x - 128;
+    } else if (warp < 4) {
+        regs_decrease<kRegsLow>();
+    } else {
+        // ------------------------------------------------ softmax + epilogue of slot x
+        regs_increase<kRegsHigh>();
+        const int x = (warp - 4) >> 2;
+        const int row = threadIdx.x - 128 * (1 + x);
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const uint32_t col_s = tmem_s(x), col_o = tmem_o(x);
         const int node_local = row / p.G;
         const int hg = row - node_local * p.G;
         const float sl2 = p.scale_log2;
-        const long long total = *sh_total, C = *sh_ctas;
-        long long seg_start = *sh_t0;  // global pair index of the current segment's first tile
+        float *sh_m = reinterpret_cast<float *>(gbase + kOffML);  // slot 1's running max / sum per row
+        float *sh_l = sh_m + kM;
         Cursor cur = cur0;
         Seg sg;
-        uint32_t gt = 0, seg_i = 0;
+        uint32_t gx = 0, seg_i = 0, n_merge = 0;  // n_merge: single-tile hand-overs so far (ML_* phases)
         bool ok = true;
         while (ok && next_seg(sch, cur, sg)) {
-            const int i = sg.mt * p.NT + node_local;
+            const int n = sg.j1 - sg.j0;
+            const bool pair = sg.has_b;
+            const int nx = pair ? n : (x == 0 ? (n + 1) / 2 : n / 2);
+            if (nx == 0) {  // slot unused in this segment
+                ++seg_i;
+                continue;
+            }
+            const int i = (2 * sg.mp + (pair ? x : 0)) * p.NT + node_local;
             const bool valid = i < p.B;
             const uint32_t *mrow = p.mask + ((size_t)sg.b * p.B + (valid ? i : 0)) * p.W;
-            const int n = sg.j1 - sg.j0;
             float m_run = -INFINITY, l_run = 0.f;  // m_run in log2 units of the scaled score
-            for (int t = 0; t < n; ++t) {
-                const uint32_t g_t = gt + t;
-                const int buf = g_t & 1;
+            for (int lx = 0; lx < nx; ++lx) {
+                const int t = pair ? lx : 2 * lx + x;
+                const uint32_t g_t = gx + lx;
                 const int k0 = (sg.j0 + t) * kN;
-                if (!mbar_wait(BAR(BAR_S_FULL + buf), (g_t >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+                if (!__all_sync(0xffffffffu, mbar_wait(BAR(BAR_S_FULL + x), g_t & 1, abort_flag, p.status))) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
                 uint32_t s[4][32];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + kTmemS + buf * 128 + c * 32, s[c]);
+                for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + col_s + c * 32, s[c]);
                 tmem_ld_wait(s[0]);
                 reg_order(s[1]);
                 reg_order(s[2]);
@@ -506,80 +594,111 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                 const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                          fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
 
-                // move the running max only when it grows by more than 2^8
+                // move the running max only when it grows by more than 2^8; the commit
+                // behind S(t) also covered this slot's previous PV, so O_x is stable here
                 const float m_new = fmaxf(m_run, tmax);
-                if (m_new > m_run + kRescaleLog2) {
-                    const float alpha = ex2_approx(m_run - m_new);
-                    if (l_run > 0.f) {
-                        const uint32_t prev = g_t - 1;
-                        if (!mbar_wait(BAR(BAR_PV_DONE + (prev & 1)), (prev >> 1) & 1, abort_flag, p.status)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            uint32_t o[32];
-                            tmem_ld32(lane_addr + kTmemO + c * 32, o);
-                            tmem_ld_wait(o);
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                            tmem_st32(lane_addr + kTmemO + c * 32, o);
-                        }
-                        tmem_st_wait();
-                    }
+                const bool rescale = m_new > m_run + kRescaleLog2;
+                float alpha = 1.f;
+                if (rescale) {
+                    alpha = ex2_approx(m_run - m_new);
                     l_run *= alpha;
                     m_run = m_new;
                 }
                 const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
 
-                // P_j may overwrite its buffer once the PV two tiles back is done
-                if (g_t >= 2 &&
-                    !mbar_wait(BAR(BAR_PV_DONE + buf), ((g_t - 2) >> 1) & 1, abort_flag, p.status)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t prow = sP + buf * kTileBytes + row * 128;
+                // P = exp2(s * scale * log2 e - m) as bf16 pairs over the first 64 columns of S
                 float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t pw[32];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t w[4];
+                    for (int c2 = 0; c2 < 2; ++c2) {
+                        const int c = 2 * hh + c2;
 #pragma unroll
-                        for (int e2 = 0; e2 < 4; ++e2) {
-                            const float a = ex2_approx(fmaf(__uint_as_float(s[c][q * 8 + 2 * e2]), sl2, neg_m));
-                            const float b = ex2_approx(fmaf(__uint_as_float(s[c][q * 8 + 2 * e2 + 1]), sl2, neg_m));
-                            ls[2 * e2] += a;
-                            ls[2 * e2 + 1] += b;
-                            w[e2] = pack_bf16x2(a, b);
+                        for (int e2 = 0; e2 < 16; ++e2) {
+                            const float a = ex2_approx(fmaf(__uint_as_float(s[c][2 * e2]), sl2, neg_m));
+                            const float b = ex2_approx(fmaf(__uint_as_float(s[c][2 * e2 + 1]), sl2, neg_m));
+                            ls[(2 * e2) & 7] += a;
+                            ls[(2 * e2 + 1) & 7] += b;
+                            pw[c2 * 16 + e2] = pack_bf16x2(a, b);
                         }
-                        const uint32_t chunk = (uint32_t)((c & 1) * 4 + q);  // 16-byte chunk in the 128-byte row
-                        st_shared_v4(prow + (c >> 1) * kHalfBytes + ((chunk ^ (uint32_t)(row & 7)) << 4), w[0], w[1],
-                                     w[2], w[3]);
                     }
+                    tmem_st32(lane_addr + col_s + hh * 32, pw);
                 }
                 l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-                fence_proxy_async_smem();
+                // O_x *= alpha before PV(t) adds this tile (PV(t) waits for P_FULL below).  TMEM
+                // loads/stores are warp-wide (.sync.aligned), so the whole warp takes the branch
+                // when any lane needs it, each lane with its own factor.  Before this slot's first
+                // PV of the segment O_x holds nothing (that PV overwrites it).
+                if (lx > 0 && __any_sync(0xffffffffu, rescale && alpha < 1.f)) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(lane_addr + col_o + c * 32, o);
+                        tmem_ld_wait(o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(lane_addr + col_o + c * 32, o);
+                    }
+                }
+                tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(BAR(BAR_P_FULL + buf));
+                mbar_arrive(BAR(BAR_P_FULL + x));
             }
             if (!ok) break;
-            gt += n;
 
-            // epilogue: O of this row tile is complete once the last PV lands
-            const uint32_t last = gt - 1;
-            if (!mbar_wait(BAR(BAR_PV_DONE + (last & 1)), (last >> 1) & 1, abort_flag, p.status)) break;
+            // epilogue: O_x of this segment is complete once its last PV lands
+            const uint32_t last = gx + nx - 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(BAR(BAR_PV_DONE + x), last & 1, abort_flag, p.status))) break;
+            const bool merge_slots = !pair && n > 1;  // slot 1 holds the odd KV tiles of the same rows
+            if (merge_slots && x == 1) {
+                // hand the row's (max, sum) to slot 0, which reads O_1 from TMEM itself
+                sh_m[row] = m_run;
+                sh_l[row] = l_run;
+                tc_fence_before();
+                mbar_arrive(BAR(BAR_ML_FULL));
+                if (!mbar_wait(BAR(BAR_ML_READ), n_merge & 1, abort_flag, p.status)) break;
+                tc_fence_after();
+                mbar_arrive(BAR(BAR_O_EMPTY + 1));
+                gx += nx;
+                ++seg_i;
+                ++n_merge;
+                continue;
+            }
+            if (merge_slots &&
+                !__all_sync(0xffffffffu, mbar_wait(BAR(BAR_ML_FULL), n_merge & 1, abort_flag, p.status)))
+                break;
             tc_fence_after();
             uint32_t o[4][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + kTmemO + c * 32, o[c]);
+            for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + col_o + c * 32, o[c]);
             tmem_ld_wait(o[0]);
             reg_order(o[1]);
             reg_order(o[2]);
             reg_order(o[3]);
+            if (merge_slots) {
+                // O = (O_0 a + O_1 b) / (l_0 a + l_1 b) with a, b moving both to the larger max
+                const float m1 = sh_m[row], l1 = sh_l[row];
+                const float mm = fmaxf(m_run, m1);
+                const float a0 = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - mm);
+                const float a1 = (m1 == -INFINITY) ? 0.f : ex2_approx(m1 - mm);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t o1[32];
+                    tmem_ld32(lane_addr + tmem_o(1) + c * 32, o1);
+                    tmem_ld_wait(o1);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        o[c][e] = __float_as_uint(fmaf(__uint_as_float(o[c][e]), a0, __uint_as_float(o1[e]) * a1));
+                }
+                l_run = l_run * a0 + l1 * a1;
+                m_run = (mm == -INFINITY) ? m_run : mm;
+                tc_fence_before();
+                mbar_arrive(BAR(BAR_ML_READ));
+                ++n_merge;
+            }
             tc_fence_before();
-            mbar_arrive(BAR(BAR_O_EMPTY));
+            mbar_arrive(BAR(BAR_O_EMPTY + x));
 
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
             const float lse_nat = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
@@ -602,88 +721,22 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                     }
                     p.lse[orow] = lse_nat;
                 }
-            } else {
-                // A piece of a row tile cut between CTAs c0..c1: park it, take a ticket,
-                // and merge all pieces if this one arrived last.
-                const long long r0 = seg_start - sg.j0;
-                const long long r1 = r0 + sg.n_row;
-                const int c0 = (int)(((r0 + 1) * C - 1) / total);
-                const int c1 = (int)((r1 * C - 1) / total);
-                const size_t slot = 2 * (size_t)blockIdx.x + (seg_i == 0 ? 0 : 1);
-                if (valid) {
-                    float4 *dst = reinterpret_cast<float4 *>(p.ws_o + (slot * kM + row) * kHeadDim);
+            } else if (valid) {
+                // A piece of a pair tile cut between CTAs: park it for the merge kernel.
+                // Chunk-major: float4 chunk k of row r at [slot][k][r], so a warp's 32 rows
+                // store 512 contiguous bytes per instruction.
+                const size_t slot = (2 * (size_t)blockIdx.x + (seg_i == 0 ? 0 : 1)) * 2 + x;
+                float4 *dst = reinterpret_cast<float4 *>(p.ws_o) + slot * (kHeadDim / 4) * kM + row;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
+                for (int c = 0; c < 4; ++c)
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            dst[c * 8 + q] = make_float4(
-                                __uint_as_float(o[c][q * 4 + 0]) * inv, __uint_as_float(o[c][q * 4 + 1]) * inv,
-                                __uint_as_float(o[c][q * 4 + 2]) * inv, __uint_as_float(o[c][q * 4 + 3]) * inv);
-                    p.ws_lse[slot * kM + row] = lse_nat;
-                }
-                __threadfence();
-                named_bar_sync(1, kM);
-                if (row == 0) {
-                    unsigned long long *tk = p.tickets + ((size_t)sg.b * p.Hkv + sg.g) * p.MT + sg.mt;
-                    unsigned long long cur_t = *reinterpret_cast<volatile unsigned long long *>(tk);
-                    unsigned long long next;
-                    for (;;) {
-                        next = ((uint32_t)(cur_t >> 32) == p.epoch) ? cur_t + 1
-                                                                    : (((unsigned long long)p.epoch << 32) | 1ull);
-                        const unsigned long long seen = atomicCAS(tk, cur_t, next);
-                        if (seen == cur_t) break;
-                        cur_t = seen;
-                    }
-                    *sh_last = ((int)(next & 0xffffffffull) == c1 - c0 + 1) ? 1 : 0;
-                }
-                named_bar_sync(1, kM);
-                if (*sh_last && valid) {
-                    __threadfence();
-                    const int slot0 = (r0 == total * c0 / C) ? 2 * c0 : 2 * c0 + 1;
-                    float m = -INFINITY;
-                    for (int c = c0; c <= c1; ++c)
-                        m = fmaxf(m, __ldcg(p.ws_lse + (size_t)(c == c0 ? slot0 : 2 * c) * kM + row));
-                    float lse_all = -INFINITY;
-                    float wsum = 0.f;
-                    if (m != -INFINITY) {
-                        for (int c = c0; c <= c1; ++c)
-                            wsum += expf(__ldcg(p.ws_lse + (size_t)(c == c0 ? slot0 : 2 * c) * kM + row) - m);
-                        lse_all = m + logf(wsum);
-                    }
-                    for (int part = 0; part < kHeadDim / 32; ++part) {  // 32 output columns at a time
-                        float acc[32];
-#pragma unroll
-                        for (int d = 0; d < 32; ++d) acc[d] = 0.f;
-                        if (m != -INFINITY) {
-                            for (int c = c0; c <= c1; ++c) {
-                                const size_t sl = (size_t)(c == c0 ? slot0 : 2 * c);
-                                const float wgt = expf(__ldcg(p.ws_lse + sl * kM + row) - lse_all);
-                                const float4 *src =
-                                    reinterpret_cast<const float4 *>(p.ws_o + (sl * kM + row) * kHeadDim + part * 32);
-#pragma unroll
-                                for (int q = 0; q < 8; ++q) {
-                                    const float4 v = __ldcg(src + q);
-                                    acc[4 * q + 0] = fmaf(wgt, v.x, acc[4 * q + 0]);
-                                    acc[4 * q + 1] = fmaf(wgt, v.y, acc[4 * q + 1]);
-                                    acc[4 * q + 2] = fmaf(wgt, v.z, acc[4 * q + 2]);
-                                    acc[4 * q + 3] = fmaf(wgt, v.w, acc[4 * q + 3]);
-                                }
-                            }
-                        }
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint4 v;
-                            v.x = pack_bf16x2(acc[8 * q + 0], acc[8 * q + 1]);
-                            v.y = pack_bf16x2(acc[8 * q + 2], acc[8 * q + 3]);
-                            v.z = pack_bf16x2(acc[8 * q + 4], acc[8 * q + 5]);
-                            v.w = pack_bf16x2(acc[8 * q + 6], acc[8 * q + 7]);
-                            dst_o[part * 4 + q] = v;
-                        }
-                    }
-                    p.lse[orow] = lse_all;
-                }
+                    for (int q = 0; q < 8; ++q)
+                        dst[(size_t)(c * 8 + q) * kM] = make_float4(
+                            __uint_as_float(o[c][q * 4 + 0]) * inv, __uint_as_float(o[c][q * 4 + 1]) * inv,
+                            __uint_as_float(o[c][q * 4 + 2]) * inv, __uint_as_float(o[c][q * 4 + 3]) * inv);
+                p.ws_lse[slot * kM + row] = lse_nat;
             }
-            seg_start += n;
+            gx += nx;
             ++seg_i;
         }
     }
@@ -695,6 +748,133 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
         tmem_dealloc(tmem, kTmemCols);
     }
 #undef BAR
+}
+
+// ------------------------------------------------------------------ merge
+
+constexpr int kMergeThreads = kM;  // one thread per row of the M tile
+
+// Pieces before sequence b_end.  Whole warp.
+__device__ long long sched_prefix(const Sched &s, int b_end, int lane)
+{
+    long long tot = 0;
+    for (int base = 0; base < b_end; base += 32) {
+        const int b = base + lane;
+        const long long t = (b < b_end) ? (long long)s.Hkv * head_tiles(s, __ldg(s.prefix_lens + b)) : 0;
+        tot += warp_sum_ll(t);
+    }
+    return tot;
+}
+
+struct MergeParams {
+    const int32_t *prefix_lens;
+    const float *ws_o;
+    const float *ws_lse;
+    uint16_t *o;
+    float *lse;
+    int nb, B, Hq, Hkv, G, NT, MT, max_pages, attn_grid;
+};
+
+// One CTA per M tile (sequence, kv head, mt), one thread per row.  An M tile
+// whose pair was cut between CTAs c0..c1 of the attention grid has one piece
+// in each: in c0's last slot (or its first, when the pair starts c0's share)
+// and in the first slot of c0+1 .. c1.  lse = ln sum_u e^{lse_u},
+// O = sum_u e^{lse_u - lse} O_u.  Partials are chunk-major, so the 128 threads
+// read 512 contiguous bytes per warp and load; two pieces' loads are in flight
+// together.
+__global__ void __launch_bounds__(kMergeThreads) tree_attn_merge_kernel(const MergeParams mp)
+{
+    __shared__ int s_c0, s_c1, s_first0;
+    const int id = blockIdx.x;
+    const int b = id / (mp.Hkv * mp.MT);
+    const int g = (id / mp.MT) % mp.Hkv;
+    const int mt = id % mp.MT;
+    const int x = mt & 1;
+    const int pm = mt >> 1;
+    const int r = threadIdx.x, lane = r & 31, warp = r >> 5;
+    const Sched sch{mp.prefix_lens, mp.nb, mp.B, mp.Hkv, mp.NT, mp.MT, mp.max_pages * kPage};
+
+    if (warp == 0) {  // prefix_lens is an input of both kernels: safe to read before the dependency wait
+        const long long total = sched_total(sch, lane);
+        const long long C = active_ctas(total, mp.attn_grid);
+        const long long start_b = sched_prefix(sch, b, lane);
+        const int P = __ldg(mp.prefix_lens + b);
+        const int ht = head_tiles(sch, P);
+        int c0 = 0, c1 = 0, first0 = 0;
+        if (ht > 0 && total > 0) {
+            long long r0 = start_b + (long long)g * ht;
+            for (int m = 0; m < pm; ++m) r0 += pair_tiles(sch, P, m);
+            const long long r1 = r0 + pair_tiles(sch, P, pm);
+            c0 = (int)(((r0 + 1) * C - 1) / total);
+            c1 = (int)((r1 * C - 1) / total);
+            first0 = (r0 == total * c0 / C) ? 0 : 1;
+        }
+        if (lane == 0) {
+            s_c0 = c0;
+            s_c1 = c1;
+            s_first0 = first0;
+        }
+    }
+    __syncthreads();
+    const int c0 = s_c0, c1 = s_c1, first0 = s_first0;
+    // Every CTA waits for the attention grid (so this grid never completes before it);
+    // past this point the partials are complete and visible.
+    pdl_wait_primary();
+    if (c0 == c1) return;                      // the attention kernel wrote this M tile itself
+    const int i = mt * mp.NT + r / mp.G;
+    if (i >= mp.B) return;                     // a row past the tree
+
+    auto slot_of = [&](int c) -> size_t { return (2 * (size_t)c + (c == c0 ? first0 : 0)) * 2 + x; };
+    float m = -INFINITY;
+#pragma unroll 4
+    for (int c = c0; c <= c1; ++c) m = fmaxf(m, __ldcg(mp.ws_lse + slot_of(c) * kM + r));
+    float wsum = 0.f;
+    if (m != -INFINITY) {
+#pragma unroll 4
+        for (int c = c0; c <= c1; ++c) wsum += expf(__ldcg(mp.ws_lse + slot_of(c) * kM + r) - m);
+    }
+    const float inv = m != -INFINITY ? 1.f / wsum : 0.f;
+    const size_t orow = ((size_t)b * mp.B + i) * mp.Hq + g * mp.G + r % mp.G;
+    uint4 *dst = reinterpret_cast<uint4 *>(mp.o + orow * kHeadDim);
+
+    for (int half = 0; half < 2; ++half) {  // 16 of the 32 four-column chunks at a time
+        float4 acc[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (m != -INFINITY) {
+            for (int c = c0; c <= c1; c += 2) {
+                const bool two = c + 1 <= c1;
+                const float w0 = expf(__ldcg(mp.ws_lse + slot_of(c) * kM + r) - m) * inv;
+                const float w1 = two ? expf(__ldcg(mp.ws_lse + slot_of(c + 1) * kM + r) - m) * inv : 0.f;
+                const float4 *s0 = reinterpret_cast<const float4 *>(mp.ws_o) + (slot_of(c) * 32 + half * 16) * kM + r;
+                const float4 *s1 = reinterpret_cast<const float4 *>(mp.ws_o) +
+                                   (slot_of(two ? c + 1 : c) * 32 + half * 16) * kM + r;
+                float4 v0[16], v1[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    v0[k] = __ldcg(s0 + (size_t)k * kM);
+                    v1[k] = two ? __ldcg(s1 + (size_t)k * kM) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    acc[k].x = fmaf(w0, v0[k].x, fmaf(w1, v1[k].x, acc[k].x));
+                    acc[k].y = fmaf(w0, v0[k].y, fmaf(w1, v1[k].y, acc[k].y));
+                    acc[k].z = fmaf(w0, v0[k].z, fmaf(w1, v1[k].z, acc[k].z));
+                    acc[k].w = fmaf(w0, v0[k].w, fmaf(w1, v1[k].w, acc[k].w));
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            uint4 w4;
+            w4.x = pack_bf16x2(acc[2 * k].x, acc[2 * k].y);
+            w4.y = pack_bf16x2(acc[2 * k].z, acc[2 * k].w);
+            w4.z = pack_bf16x2(acc[2 * k + 1].x, acc[2 * k + 1].y);
+            w4.w = pack_bf16x2(acc[2 * k + 1].z, acc[2 * k + 1].w);
+            dst[half * 8 + k] = w4;
+        }
+    }
+    mp.lse[orow] = m != -INFINITY ? m + logf(wsum) : -INFINITY;
 }
 
 // ------------------------------------------------------------------ host side
@@ -719,7 +899,8 @@ static EncodeTiledFn encode_fn()
 
 size_t attn_workspace_bytes(int ctas, int row_tiles)
 {
-    return (size_t)2 * ctas * kM * (kHeadDim + 1) * sizeof(float) + (size_t)row_tiles * sizeof(unsigned long long);
+    (void)row_tiles;
+    return (size_t)4 * ctas * kM * (kHeadDim + 1) * sizeof(float);
 }
 
 int attn_row_tiles(const tv_attn_args *a)
@@ -728,13 +909,17 @@ int attn_row_tiles(const tv_attn_args *a)
     return a->nb * a->Hkv * ((a->B + NT - 1) / NT);
 }
 
-// Every call gets its own ticket epoch, so tickets left by an earlier (even an
-// interrupted) call never count towards this one.
-static uint32_t next_epoch()
+// The attention kernel's shared-memory opt-in, once per device.
+static cudaError_t attn_smem_opt_in()
 {
-    static std::atomic<uint32_t> counter{0};
-    uint32_t e = counter.fetch_add(1, std::memory_order_relaxed) + 1;
-    if (e == 0) e = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+    static std::atomic<uint64_t> done_mask{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0;
+    if (bit && (done_mask.load(std::memory_order_relaxed) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(tree_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess && bit) done_mask.fetch_or(bit, std::memory_order_relaxed);
     return e;
 }
 
@@ -786,9 +971,7 @@ int32_t launch_attn(const tv_attn_args *a, int ctas, void *workspace, cudaStream
     p.lse = a->lse_d;
     p.status = a->dev_status_d;
     p.ws_o = static_cast<float *>(workspace);
-    p.ws_lse = p.ws_o + (size_t)2 * ctas * kM * kHeadDim;
-    p.tickets = reinterpret_cast<unsigned long long *>(p.ws_lse + (size_t)2 * ctas * kM);
-    p.epoch = next_epoch();
+    p.ws_lse = p.ws_o + (size_t)4 * ctas * kM * kHeadDim;
     p.nb = a->nb;
     p.B = a->B;
     p.Hq = a->Hq;
@@ -802,10 +985,27 @@ int32_t launch_attn(const tv_attn_args *a, int ctas, void *workspace, cudaStream
     const float scale = a->scale > 0.f ? a->scale : 1.0f / sqrtf((float)kHeadDim);
     p.scale_log2 = scale * 1.4426950408889634f;
 
-    cudaError_t e = cudaFuncSetAttribute(tree_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = attn_smem_opt_in();
     if (e == cudaSuccess) {
         tree_attn_kernel<<<ctas, kThreads, kSmemBytes, stream>>>(p);
         e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) {
+        // The merge kernel is a programmatic dependent: it may be scheduled while the
+        // attention grid drains and waits (griddepcontrol.wait) before reading partials.
+        MergeParams mp{a->prefix_lens_d, p.ws_o, p.ws_lse, p.o, p.lse, p.nb, p.B, p.Hq, p.Hkv, p.G, p.NT, p.MT,
+                       p.max_pages, ctas};
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(a->nb * a->Hkv * p.MT));
+        cfg.blockDim = dim3(kMergeThreads);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, tree_attn_merge_kernel, mp);
     }
     if (e != cudaSuccess) {
         *cuda_err = e;

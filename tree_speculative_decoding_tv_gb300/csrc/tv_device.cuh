@@ -171,6 +171,11 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
         : "memory");
 }
 
+// Programmatic dependent launch: let the next kernel in the stream start
+// launching / wait until the previous kernel has completed and flushed.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Hand registers between warpgroups (every thread of the warpgroup executes it).
 template <uint32_t N>
 __device__ __forceinline__ void regs_decrease()

@@ -25,7 +25,7 @@ cudaError_t launch_accept(const uint16_t *logits, int V, const int32_t *draft, c
 size_t attn_workspace_bytes(int ctas, int row_tiles);
 int attn_row_tiles(const tv_attn_args *a);
 
-// Encodes the TMA descriptors and launches the attention kernel.
+// Encodes the TMA descriptors and launches the attention kernel and its merge kernel.
 // Returns TV_OK or TV_ERR_CUDA (with *cuda_err set).
 int32_t launch_attn(const tv_attn_args *a, int ctas, void *workspace, cudaStream_t stream, cudaError_t *cuda_err);
 
