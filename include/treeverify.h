@@ -159,9 +159,9 @@ TV_API int32_t tv_attn(const tv_attn_args *args, void *workspace_d, size_t works
  *   argmax_d       int32 [nb*B] (out), n_acc_d int32 [nb], path_d int32 [nb][B],
  *   bonus_d        int32 [nb] (out)
  *   workspace_d    device buffer of at least tv_accept_workspace_size(V, B, nb)
- *                  bytes, 8-byte aligned, contents ignored on entry (it carries
- *                  per-chunk argmax partials between the call's two kernels, so
- *                  concurrent calls need separate workspaces)
+ *                  bytes (8 per logits row), 8-byte aligned, contents ignored on
+ *                  entry (the call zeroes it and combines per-chunk argmax results
+ *                  there, so concurrent calls need separate workspaces)
  * Returns TV_OK, TV_ERR_INVALID_ARG, TV_ERR_UNSUPPORTED_SHAPE or TV_ERR_CUDA.
  * A parent array that is not topological is reported through dev_status_d.
  */

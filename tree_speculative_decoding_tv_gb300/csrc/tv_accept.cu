@@ -12,11 +12,15 @@
 // of its unit in registers (all in flight at once); bf16x2 NaN-propagating max
 // instructions reduce them (about one per two logits), the warp agrees on the
 // unit's maximum with shuffles, and only the lanes holding it look for its
-// first position.  One (value, index) partial per unit goes to the caller's
-// workspace.
+// first position.
 //
-// accept (kernel 2): one CTA per sequence, one thread per node.  Each thread
-// finishes its row's argmax from the chunk partials, then ok[] is packed into
+// The units of a row meet through one 64-bit atomicMax per unit on an
+// order-preserving key (value rank, then the smaller index) in the caller's
+// workspace, zeroed at the start of every call.
+//
+// accept (kernel 2): one CTA per sequence, one thread per node, launched as a
+// programmatic dependent of the argmax.  Each thread reads its row's key, then
+// ok[] is packed into
 // W ballot words; node i is accepted iff (mask[i] & ~ok) == 0 (the root counts
 // as ok); the best (depth, -index) key is a block max; the path is read off
 // the chosen node's mask bits in ascending order.
@@ -54,9 +58,20 @@ __device__ __forceinline__ uint4 ld_stream_v4(const uint4 *p)
     return v;
 }
 
-__device__ __forceinline__ unsigned long long pack_best(float v, int i)
+// 64-bit key whose unsigned order is the argmax order: the value's rank in the
+// high half (every NaN ranks highest, -0 ranks with +0), then 0xFFFFFFFF - index
+// so that equal values favour the smaller index.
+__device__ __forceinline__ unsigned long long argmax_key(float v, int i)
 {
-    return ((unsigned long long)(uint32_t)i << 32) | __float_as_uint(v);
+    const uint32_t u = __float_as_uint(v);
+    uint32_t rank;
+    if (v != v)
+        rank = 0xFFFFFFFFu;
+    else if (v == 0.f)
+        rank = 0x80000000u;
+    else
+        rank = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ((unsigned long long)rank << 32) | (0xFFFFFFFFu - (uint32_t)i);
 }
 
 // max with a NaN counting as the largest value
@@ -70,13 +85,15 @@ __device__ __forceinline__ float max_nan(float a, float b) { return (a != a) ? a
 // synchronisation.
 __global__ void __launch_bounds__(kArgThreads) argmax_partial_kernel(const uint16_t *__restrict__ logits, long long V,
                                                                      int nchunk, long long units,
-                                                                     unsigned long long *__restrict__ part)
+                                                                     unsigned long long *__restrict__ best)
 {
     static_assert(kArgChunk == 32 * kArgVec * 8, "one warp per unit");
     static_assert(kArgVec == 8, "the dependency point below lists 8 vectors");
     const int lane = threadIdx.x & 31;
     const long long warps = (long long)gridDim.x * (kArgThreads / 32);
     const float NEG_INF = -__int_as_float(0x7f800000);
+    pdl_wait_primary();  // logits and the zeroed keys come from earlier work in the stream
+    pdl_launch_dependents();
 
     for (long long u = (long long)blockIdx.x * (kArgThreads / 32) + (threadIdx.x >> 5); u < units; u += warps) {
         const long long row_id = u / nchunk;
@@ -161,11 +178,11 @@ __global__ void __launch_bounds__(kArgThreads) argmax_partial_kernel(const uint1
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) idx = min(idx, __shfl_xor_sync(0xffffffffu, idx, o));
-        if (lane == 0) part[u] = pack_best(bm, idx);
+        if (lane == 0) atomicMax(best + row_id, argmax_key(bm, idx));
     }
 }
 
-__global__ void __launch_bounds__(kMaxB) accept_kernel(const unsigned long long *__restrict__ part, int nchunk,
+__global__ void __launch_bounds__(kMaxB) accept_kernel(const unsigned long long *__restrict__ best,
                                                        const int32_t *__restrict__ draft,
                                                        const int32_t *__restrict__ parent,
                                                        const uint32_t *__restrict__ mask, int B, int W,
@@ -183,40 +200,13 @@ __global__ void __launch_bounds__(kMaxB) accept_kernel(const unsigned long long 
     const int i = threadIdx.x;
     const int lane = i & 31, wid = i >> 5;
     if (i == 0) s_bad = 0;
+    pdl_wait_primary();  // the argmax keys are complete from here on
 
-    // finish every row's argmax from its chunk partials: lpr threads per row,
-    // each striding over the partials, then a shuffle reduction within the group
-    {
-        int lpr = 1;
-        while (lpr < 32 && lpr * 2 * B <= (int)blockDim.x) lpr *= 2;
-        const int r = i / lpr, sub = i % lpr;
-        float bv = __int_as_float(0xff800000);
-        int bi = 0x7fffffff;
-        if (r < B) {
-            const unsigned long long *pr = part + ((size_t)b * B + r) * nchunk;
-#pragma unroll 4
-            for (int c = sub; c < nchunk; c += lpr) {
-                const unsigned long long pk = __ldcg(pr + c);
-                const float v = __uint_as_float((uint32_t)pk);
-                const int ix = (int)(pk >> 32);
-                if (beats(v, ix, bv, bi)) {
-                    bv = v;
-                    bi = ix;
-                }
-            }
-        }
-        for (int o = lpr >> 1; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (beats(ov, oi, bv, bi)) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-        if (r < B && sub == 0) {
-            s_am[r] = bi;
-            am[(size_t)b * B + r] = bi;
-        }
+    // every row's argmax is the low half of its key: 0xFFFFFFFF - index
+    if (i < B) {
+        const int a = (int)(0xFFFFFFFFu - (uint32_t)__ldcg(best + (size_t)b * B + i));
+        s_am[i] = a;
+        am[(size_t)b * B + i] = a;
     }
     __syncthreads();
 
@@ -256,9 +246,9 @@ __global__ void __launch_bounds__(kMaxB) accept_kernel(const unsigned long long 
         s_best[0] = k;
     }
     __syncthreads();
-    const int best = s_best[0];
-    const int vstar = best >= 0 ? 511 - (best & 511) : 0;
-    const int dep = best >= 0 ? (best >> 9) : 0;
+    const int top = s_best[0];
+    const int vstar = top >= 0 ? 511 - (top & 511) : 0;
+    const int dep = top >= 0 ? (top >> 9) : 0;
     if (i < W) s_vmask[i] = mask[((size_t)b * B + vstar) * W + i];
     __syncthreads();
 
@@ -281,8 +271,8 @@ __global__ void __launch_bounds__(kMaxB) accept_kernel(const unsigned long long 
 
 size_t accept_workspace_bytes(int V, int B, int nb)
 {
-    const long long nchunk = ((long long)V + kArgChunk - 1) / kArgChunk;
-    return (size_t)nb * B * nchunk * sizeof(unsigned long long);
+    (void)V;
+    return (size_t)nb * B * sizeof(unsigned long long);
 }
 
 cudaError_t launch_accept(const uint16_t *logits, int V, const int32_t *draft, const int32_t *parent,
@@ -295,14 +285,16 @@ cudaError_t launch_accept(const uint16_t *logits, int V, const int32_t *draft, c
     const long long need = (units + kArgThreads / 32 - 1) / (kArgThreads / 32);
     if (grid > need) grid = need;
     if (grid < 1) grid = 1;
-    unsigned long long *part = static_cast<unsigned long long *>(workspace);
-    argmax_partial_kernel<<<(unsigned)grid, kArgThreads, 0, stream>>>(logits, V, nchunk, units, part);
-    cudaError_t e = cudaGetLastError();
+    unsigned long long *best = static_cast<unsigned long long *>(workspace);
+    cudaError_t e = cudaMemsetAsync(best, 0, accept_workspace_bytes(V, B, nb), stream);
+    if (e != cudaSuccess) return e;
+    e = launch_dependent(argmax_partial_kernel, dim3((unsigned)grid), dim3(kArgThreads), 0, stream, logits,
+                         (long long)V, nchunk, units, best);
     if (e != cudaSuccess) return e;
     const int W = (B + 31) / 32;
-    accept_kernel<<<nb, kMaxB, 0, stream>>>(part, nchunk, draft, parent, mask, B, W, am, n_acc, path, bonus,
-                                              status);
-    return cudaGetLastError();
+    // its launch overlaps the argmax tail; it waits before reading the keys
+    return launch_dependent(accept_kernel, dim3((unsigned)nb), dim3(kMaxB), 0, stream,
+                            (const unsigned long long *)best, draft, parent, mask, B, W, am, n_acc, path, bonus, status);
 }
 
 }  // namespace tv

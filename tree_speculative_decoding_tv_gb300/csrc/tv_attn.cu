@@ -322,6 +322,9 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
+    // Everything above touches only this CTA; the inputs may come from the previous
+    // kernel in the stream (launched as its programmatic dependent), so wait here.
+    pdl_wait_primary();
     if (warp == 2) {
         const long long total = sched_total(sch, lane);
         const long long C = active_ctas(total, gridDim.x);
@@ -986,26 +989,15 @@ int32_t launch_attn(const tv_attn_args *a, int ctas, void *workspace, cudaStream
     p.scale_log2 = scale * 1.4426950408889634f;
 
     cudaError_t e = attn_smem_opt_in();
+    if (e == cudaSuccess)
+        e = launch_dependent(tree_attn_kernel, dim3(ctas), dim3(kThreads), kSmemBytes, stream, p);
     if (e == cudaSuccess) {
-        tree_attn_kernel<<<ctas, kThreads, kSmemBytes, stream>>>(p);
-        e = cudaGetLastError();
-    }
-    if (e == cudaSuccess) {
-        // The merge kernel is a programmatic dependent: it may be scheduled while the
-        // attention grid drains and waits (griddepcontrol.wait) before reading partials.
+        // The merge kernel may be scheduled while the attention grid drains; it waits
+        // (griddepcontrol.wait) before reading partials.
         MergeParams mp{a->prefix_lens_d, p.ws_o, p.ws_lse, p.o, p.lse, p.nb, p.B, p.Hq, p.Hkv, p.G, p.NT, p.MT,
                        p.max_pages, ctas};
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)(a->nb * a->Hkv * p.MT));
-        cfg.blockDim = dim3(kMergeThreads);
-        cfg.dynamicSmemBytes = 0;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, tree_attn_merge_kernel, mp);
+        e = launch_dependent(tree_attn_merge_kernel, dim3((unsigned)(a->nb * a->Hkv * p.MT)), dim3(kMergeThreads), 0,
+                             stream, mp);
     }
     if (e != cudaSuccess) {
         *cuda_err = e;

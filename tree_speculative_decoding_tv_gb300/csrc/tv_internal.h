@@ -10,6 +10,26 @@
 
 namespace tv {
 
+// Launch `kernel` on `stream` as a programmatic dependent of the stream's previous
+// kernel: it may be scheduled while that kernel drains, and must execute
+// griddepcontrol.wait (pdl_wait_primary) before reading anything that kernel wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 cudaError_t launch_build_mask(const int32_t *parent, int B, int nb, uint32_t *mask, int32_t *depth, int32_t *status,
                               cudaStream_t stream);
 

@@ -29,6 +29,8 @@ __global__ void __launch_bounds__(kMaskMaxB) build_mask_kernel(const int32_t *__
     const int b = blockIdx.x;
     const int i = threadIdx.x;
     if (i == 0) bad = 0;
+    pdl_wait_primary();        // parent[] may come from the previous kernel in the stream
+    pdl_launch_dependents();   // the attention kernel may start its set-up meanwhile
     __syncthreads();
 
     int p = -1;
@@ -71,8 +73,7 @@ cudaError_t launch_build_mask(const int32_t *parent, int B, int nb, uint32_t *ma
 {
     const int W = (B + 31) / 32;
     const int threads = ((B + 31) / 32) * 32;
-    build_mask_kernel<<<nb, threads, 0, stream>>>(parent, B, W, mask, depth, status);
-    return cudaGetLastError();
+    return launch_dependent(build_mask_kernel, dim3(nb), dim3(threads), 0, stream, parent, B, W, mask, depth, status);
 }
 
 }  // namespace tv
