@@ -172,6 +172,38 @@ TV_API int32_t tv_accept(const uint16_t *logits_d, int32_t V, const int32_t *dra
                          int32_t *argmax_d, int32_t *n_acc_d, int32_t *path_d, int32_t *bonus_d,
                          int32_t *dev_status_d, void *workspace_d, size_t workspace_bytes, void *stream);
 
+/*
+ * tv_accept_noalloc — tv_accept for callers that cannot allocate device memory.
+ * (The pages have no counterpart: this is an integration aid, not part of the
+ * method.)
+ *
+ * Some callers cannot call cudaMalloc, and so cannot hand tv_accept a workspace:
+ * code that runs while a stream is being captured into a CUDA graph (an
+ * allocation there is not part of the graph and breaks the capture), and
+ * serving runtimes that plan every device buffer at start-up and forbid
+ * allocation on the decode path.  This entry point takes the same arguments as
+ * tv_accept minus the workspace and computes the same results, with its scratch
+ * (8 bytes per logits row) in a fixed array inside the library image.
+ *
+ *   - Limit: nb * B <= TV_ACCEPT_NOALLOC_MAX_ROWS; larger calls return
+ *     TV_ERR_UNSUPPORTED_SHAPE and enqueue nothing.
+ *   - The array exists once per GPU that loads the library and stays allocated
+ *     until the process exits.
+ *   - The first call on a device looks up the array's device address (with that
+ *     device current) and caches it; make that first call before any stream
+ *     capture.
+ *   - Every call on a device shares the array and leaves its last contents
+ *     there; each call zeroes the part it uses before use.  Calls whose work
+ *     overlaps on the GPU (different streams, no ordering between them) race on
+ *     the array and their results are undefined: order them on one stream.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+#define TV_ACCEPT_NOALLOC_MAX_ROWS 8192
+TV_API int32_t tv_accept_noalloc(const uint16_t *logits_d, int32_t V, const int32_t *draft_tokens_d,
+                                 const int32_t *parent_d, const uint32_t *mask_d, int32_t B, int32_t nb,
+                                 int32_t *argmax_d, int32_t *n_acc_d, int32_t *path_d, int32_t *bonus_d,
+                                 int32_t *dev_status_d, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,7 +24,8 @@ TV_ERR_TIMEOUT = 5
 TV_ERR_UNIMPLEMENTED = 6
 
 EXPORTED = ("tv_status_str", "tv_version", "tv_build_mask", "tv_attn_workspace_size", "tv_attn",
-            "tv_accept_workspace_size", "tv_accept")
+            "tv_accept_workspace_size", "tv_accept", "tv_accept_noalloc")
+NOALLOC_MAX_ROWS = 8192  # TV_ACCEPT_NOALLOC_MAX_ROWS
 
 
 class TVError(RuntimeError):
@@ -70,6 +71,8 @@ def lib() -> C.CDLL:
         L.tv_accept_workspace_size.restype = C.c_size_t
         L.tv_accept.argtypes = [P, I, P, P, P, I, I, P, P, P, P, P, P, C.c_size_t, P]
         L.tv_accept.restype = I
+        L.tv_accept_noalloc.argtypes = [P, I, P, P, P, I, I, P, P, P, P, P, P]
+        L.tv_accept_noalloc.restype = I
         _lib = L
     return _lib
 
@@ -164,4 +167,24 @@ def accept(logits, draft, parent, mask, status=None, out=None, workspace=None, s
                          _p(bonus), _p(status), _p(workspace), workspace.numel() * workspace.element_size(),
                          _stream(stream))
     _check(rc, "tv_accept")
+    return am, n_acc, path, bonus
+
+
+def accept_noalloc(logits, draft, parent, mask, status=None, out=None, stream=None):
+    """tv_accept_noalloc: tv_accept on the library's own fixed scratch (no workspace).
+
+    For callers that cannot allocate device memory (stream capture, runtimes
+    with a fixed memory plan); at most NOALLOC_MAX_ROWS logits rows per call,
+    and calls must not overlap on the GPU (they share the scratch).
+    """
+    nb, B = parent.shape
+    V = logits.shape[-1]
+    dev = logits.device
+    if out is None:
+        out = (torch.empty(nb * B, dtype=torch.int32, device=dev), torch.empty(nb, dtype=torch.int32, device=dev),
+               torch.empty((nb, B), dtype=torch.int32, device=dev), torch.empty(nb, dtype=torch.int32, device=dev))
+    am, n_acc, path, bonus = out
+    rc = lib().tv_accept_noalloc(_p(logits), V, _p(draft), _p(parent), _p(mask), B, nb, _p(am), _p(n_acc), _p(path),
+                                 _p(bonus), _p(status), _stream(stream))
+    _check(rc, "tv_accept_noalloc")
     return am, n_acc, path, bonus

@@ -27,6 +27,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "tv_device.cuh"
 #include "tv_internal.h"
 
@@ -295,6 +297,47 @@ cudaError_t launch_accept(const uint16_t *logits, int V, const int32_t *draft, c
     // its launch overlaps the argmax tail; it waits before reading the keys
     return launch_dependent(accept_kernel, dim3((unsigned)nb), dim3(kMaxB), 0, stream,
                             (const unsigned long long *)best, draft, parent, mask, B, W, am, n_acc, path, bonus, status);
+}
+
+// ------------------------------------------------------ allocation-free variant
+
+// Scratch of tv_accept_noalloc: one 8-byte argmax key per logits row, for at most
+// TV_ACCEPT_NOALLOC_MAX_ROWS rows (64 KB).  It lives in the library image, so every
+// GPU that loads the library holds it until the process exits, and every call of
+// tv_accept_noalloc on that GPU shares it.
+static __device__ __align__(256) unsigned long long g_noalloc_keys[TV_ACCEPT_NOALLOC_MAX_ROWS];
+
+// The device address of g_noalloc_keys on the current device.  Host code only sees a
+// host-side stand-in under that name, so the address is looked up with
+// cudaGetSymbolAddress once per device (with that device current) and cached.
+static cudaError_t noalloc_keys_address(void **out)
+{
+    static std::mutex mu;
+    static void *addr[64] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_keys);
+        if (e != cudaSuccess) return e;
+        addr[dev] = ptr;
+    }
+    *out = addr[dev];
+    return cudaSuccess;
+}
+
+cudaError_t launch_accept_noalloc(const uint16_t *logits, int V, const int32_t *draft, const int32_t *parent,
+                                  const uint32_t *mask, int B, int nb, int32_t *am, int32_t *n_acc, int32_t *path,
+                                  int32_t *bonus, int32_t *status, int num_sms, cudaStream_t stream)
+{
+    void *keys = nullptr;
+    const cudaError_t e = noalloc_keys_address(&keys);
+    if (e != cudaSuccess) return e;
+    // the same kernels as tv_accept; their call zeroes the keys before use
+    return launch_accept(logits, V, draft, parent, mask, B, nb, am, n_acc, path, bonus, status, keys, num_sms, stream);
 }
 
 }  // namespace tv

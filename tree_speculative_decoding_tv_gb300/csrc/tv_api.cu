@@ -146,4 +146,25 @@ int32_t tv_accept(const uint16_t *logits_d, int32_t V, const int32_t *draft_toke
     return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
 
+int32_t tv_accept_noalloc(const uint16_t *logits_d, int32_t V, const int32_t *draft_tokens_d, const int32_t *parent_d,
+                          const uint32_t *mask_d, int32_t B, int32_t nb, int32_t *argmax_d, int32_t *n_acc_d,
+                          int32_t *path_d, int32_t *bonus_d, int32_t *dev_status_d, void *stream)
+{
+    if (nb < 0 || V < 1) return TV_ERR_INVALID_ARG;
+    if (B < 1 || B > kMaxB) return TV_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)nb * B > TV_ACCEPT_NOALLOC_MAX_ROWS) return TV_ERR_UNSUPPORTED_SHAPE;
+    if (!logits_d || !draft_tokens_d || !parent_d || !mask_d || !argmax_d || !n_acc_d || !path_d || !bonus_d)
+        return TV_ERR_INVALID_ARG;
+    if (!aligned(logits_d, 2) || !aligned(draft_tokens_d, 4) || !aligned(parent_d, 4) || !aligned(mask_d, 4) ||
+        !aligned(argmax_d, 4) || !aligned(n_acc_d, 4) || !aligned(path_d, 4) || !aligned(bonus_d, 4) ||
+        !aligned(dev_status_d, 4))
+        return TV_ERR_INVALID_ARG;
+    if (nb == 0) return TV_OK;
+    const int sms = sm_count();
+    if (sms < 1) return TV_ERR_CUDA;
+    cudaError_t e = tv::launch_accept_noalloc(logits_d, V, draft_tokens_d, parent_d, mask_d, B, nb, argmax_d, n_acc_d,
+                                              path_d, bonus_d, dev_status_d, sms, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
 }  // extern "C"

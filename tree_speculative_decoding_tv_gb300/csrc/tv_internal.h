@@ -40,6 +40,11 @@ cudaError_t launch_accept(const uint16_t *logits, int V, const int32_t *draft, c
                           const uint32_t *mask, int B, int nb, int32_t *am, int32_t *n_acc, int32_t *path,
                           int32_t *bonus, int32_t *status, void *workspace, int num_sms, cudaStream_t stream);
 
+// tv_accept on the library's own static scratch (no workspace argument).
+cudaError_t launch_accept_noalloc(const uint16_t *logits, int V, const int32_t *draft, const int32_t *parent,
+                                  const uint32_t *mask, int B, int nb, int32_t *am, int32_t *n_acc, int32_t *path,
+                                  int32_t *bonus, int32_t *status, int num_sms, cudaStream_t stream);
+
 // Workspace bytes the attention needs with `ctas` CTAs over `row_tiles`
 // (sequence, kv head, 128-row tile) units, and that unit count for `a`.
 size_t attn_workspace_bytes(int ctas, int row_tiles);
