@@ -65,6 +65,29 @@ def accept_bytes(w: wl.Workload) -> int:
     return w.nb * w.B * w.V * 2
 
 
+def source_hash(name: str) -> str:
+    import hashlib
+    with open(os.path.join(ROOT, "tree_speculative_decoding_tv_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, src: str, config: int):
+    """DRAM bytes per launch (read + write) from the committed ncu summary of this kernel and
+    workload, or None when there is none or the kernel source changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_config{config}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    fields = dict(line.split(":", 1) for line in text.splitlines() if line.startswith(("source_sha256_16:", "traffic_bytes_per_launch:")))
+    if fields.get("source_sha256_16", "").strip() != source_hash(src):
+        return None
+    try:
+        return float(fields["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -154,11 +177,13 @@ class Step:
                         torch.empty((w.nb, w.B), dtype=torch.int32, device=dev),
                         torch.empty(w.nb, dtype=torch.int32, device=dev))
         self.acc_ws = torch.empty(tv.accept_workspace_size(w.V, w.B, w.nb), dtype=torch.uint8, device=dev)
-        self.launches_per_step = 5  # mask, attention, merge, argmax partials, argmax finish + acceptance walk
+        self.launches_per_step = 5  # mask, attention, merge, argmax, acceptance (plus one memset node)
         self.g_attn = self.g_acc = None
 
-    def _attn_stage(self):
+    def _mask_stage(self):
         self.tv.build_mask(self.parent, status=self.status, mask=self.mask, depth=self.depth)
+
+    def _attn_stage(self):
         self.tv.attn(self.q, self.k, self.v, self.bt, self.pl, self.mask, status=self.status, o=self.o, lse=self.lse,
                      workspace=self.ws)
 
@@ -172,18 +197,21 @@ class Step:
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
+            self._mask_stage()
             self._attn_stage()
             self._accept_stage()
         torch.cuda.current_stream().wait_stream(side)
         torch.cuda.synchronize()
         self.g_attn, self.g_acc = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.g_attn):
+            self._mask_stage()
             self._attn_stage()
         with torch.cuda.graph(self.g_acc):
             self._accept_stage()
         torch.cuda.synchronize()
 
     def run(self, ev=None):
+        """One step; ev = 3 events bracketing the attention stage (mask + tv_attn) and acceptance."""
         if ev is not None:
             ev[0].record()
         self.g_attn.replay()
@@ -279,17 +307,19 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     attn_tc = af / (peaks["bf16_tflops"] * 1e12)
     attn_hbm = ab / (peaks["hbm_gbs"] * 1e9)
     if attn_tc >= attn_hbm:
-        attn_roof = {"kernel": "build_mask_kernel + tree_attn_kernel + tree_attn_merge_kernel", "bound": "tensor",
+        attn_roof = {"kernel": "attention stage: build_mask_kernel + tree_attn_kernel + tree_attn_merge_kernel", "bound": "tensor",
                      "achieved": af / t_attn / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
     else:
-        attn_roof = {"kernel": "build_mask_kernel + tree_attn_kernel + tree_attn_merge_kernel", "bound": "hbm",
+        attn_roof = {"kernel": "attention stage: build_mask_kernel + tree_attn_kernel + tree_attn_merge_kernel", "bound": "hbm",
                      "achieved": ab / t_attn / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    acc_roof = {"kernel": "argmax_partial_kernel + accept_kernel", "bound": "hbm", "achieved": lb / t_acc / 1e9,
-                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    for r in (attn_roof, acc_roof):
+    acc_roof = {"kernel": "argmax_partial_kernel + accept_kernel (tv_accept)", "bound": "hbm",
+                "achieved": lb / t_acc / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    for r, src, name in ((attn_roof, "tv_attn.cu", "tree_attn_kernel"),
+                         (acc_roof, "tv_accept.cu", "argmax_partial_kernel")):
         r["frac"] = r["achieved"] / r["peak"]
         r["peak_source"] = peak_src + " burst"
-        r["traffic"] = None
+        r["traffic"] = profiled_traffic(name, src, args.config)
+        r["algorithmic_bytes"] = ab if src == "tv_attn.cu" else lb
     roof = attn_roof if t_attn >= t_acc else acc_roof
     out = {
         "metric": METRIC, "value": nodes * world / (total_ms / args.steps * 1e-3), "unit": UNIT,
@@ -302,7 +332,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
                    "launch": "each stage replayed from a CUDA graph captured once"},
         "roofline": roof,
         "breakdown": {
-            "attention_ms": float(np.mean(attn_ms)), "accept_ms": float(np.mean(acc_ms)),
+            "attention_stage_ms": float(np.mean(attn_ms)), "accept_ms": float(np.mean(acc_ms)),
             "attention_nodes_per_s": nodes / t_attn, "attention_roofline": attn_roof, "accept_roofline": acc_roof,
             "attention_bytes": ab, "attention_flops": af, "accept_bytes": lb,
         },

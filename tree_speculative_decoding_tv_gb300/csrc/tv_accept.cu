@@ -6,9 +6,9 @@
 // draft token equals the target argmax at the parent; the deepest accepted
 // node wins, ties to the smallest index.
 //
-// argmax (kernel 1): the logits are cut into (row, 2048-element chunk) units,
+// argmax (kernel 1): the logits are cut into (row, 4096-element chunk) units,
 // one warp per unit, and a one-wave grid walks them, so every SM streams the
-// same number of bytes whatever the row count.  A lane holds 8 16-byte vectors
+// same number of bytes whatever the row count.  A lane holds 16 16-byte vectors
 // of its unit in registers (all in flight at once); bf16x2 NaN-propagating max
 // instructions reduce them (about one per two logits), the warp agrees on the
 // unit's maximum with shuffles, and only the lanes holding it look for its
@@ -35,9 +35,9 @@
 namespace tv {
 
 constexpr int kArgThreads = 256;
-constexpr int kArgVec = 8;                    // 16-byte vectors per lane per unit
-constexpr int kArgChunk = 32 * kArgVec * 8;   // logits per unit (4 KB): one warp
-constexpr int kArgCtasPerSm = 8;
+constexpr int kArgVec = 16;                   // 16-byte vectors per lane per unit
+constexpr int kArgChunk = 32 * kArgVec * 8;   // logits per unit (8 KB): one warp
+constexpr int kArgCtasPerSm = 2;  // resident CTAs per SM at the kernel's register use
 constexpr int kMaxB = 256;
 constexpr int kMaxW = kMaxB / 32;
 
@@ -79,72 +79,79 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int i)
 // max with a NaN counting as the largest value
 __device__ __forceinline__ float max_nan(float a, float b) { return (a != a) ? a : ((b != b) ? b : fmaxf(a, b)); }
 
+__device__ __forceinline__ float vec_max(const uint4 &v)
+{
+    __nv_bfloat162 a = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162 *>(&v.x),
+                                   *reinterpret_cast<const __nv_bfloat162 *>(&v.y));
+    const __nv_bfloat162 c = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162 *>(&v.z),
+                                         *reinterpret_cast<const __nv_bfloat162 *>(&v.w));
+    a = __hmax2_nan(a, c);
+    return __bfloat162float(__hmax_nan(a.x, a.y));
+}
+
 // One unit = kArgChunk logits of one row = one warp: each lane holds kArgVec
-// 16-byte vectors in registers (all loads in flight at once) and keeps the
-// maximum of each vector; the warp agrees on the unit's maximum with shuffles,
-// and the lanes holding it find its first position in two steps (first vector
-// whose maximum matches, then the element inside it).  No block-level
-// synchronisation.
-__global__ void __launch_bounds__(kArgThreads) argmax_partial_kernel(const uint16_t *__restrict__ logits, long long V,
-                                                                     int nchunk, long long units,
+// 16-byte vectors in registers (all loads in flight at once), the warp agrees
+// on the unit's maximum with shuffles, and the lanes holding it find its first
+// position in two steps (first vector whose maximum matches, then the element
+// inside it).  No block-level synchronisation; 32-bit index arithmetic.
+__global__ void __launch_bounds__(kArgThreads) argmax_partial_kernel(const uint16_t *__restrict__ logits, int V,
+                                                                     int nchunk, int units,
                                                                      unsigned long long *__restrict__ best)
 {
     static_assert(kArgChunk == 32 * kArgVec * 8, "one warp per unit");
-    static_assert(kArgVec == 8, "the dependency point below lists 8 vectors");
+    static_assert(kArgVec == 16, "the dependency points below list 16 vectors");
     const int lane = threadIdx.x & 31;
-    const long long warps = (long long)gridDim.x * (kArgThreads / 32);
+    const int warps = gridDim.x * (kArgThreads / 32);
     const float NEG_INF = -__int_as_float(0x7f800000);
     pdl_wait_primary();  // logits and the zeroed keys come from earlier work in the stream
     pdl_launch_dependents();
 
-    for (long long u = (long long)blockIdx.x * (kArgThreads / 32) + (threadIdx.x >> 5); u < units; u += warps) {
-        const long long row_id = u / nchunk;
-        const long long lo = (u - row_id * nchunk) * (long long)kArgChunk;
-        const long long hi = (lo + kArgChunk < V) ? lo + kArgChunk : V;
-        const uint16_t *row = logits + row_id * V;
+    for (int u = blockIdx.x * (kArgThreads / 32) + (threadIdx.x >> 5); u < units; u += warps) {
+        const int row_id = u / nchunk;
+        const int lo = (u - row_id * nchunk) * kArgChunk;
+        const int hi = min(lo + kArgChunk, V);
+        const uint16_t *row = logits + (size_t)row_id * V;
 
         // scalar head up to the first 16-byte boundary, 16-byte vectors, scalar tail
-        long long head = (long long)(((16u - ((uint32_t)(uintptr_t)(row + lo) & 15u)) & 15u) >> 1);
-        if (head > hi - lo) head = hi - lo;
-        const long long vstart = lo + head;
-        const int nvec = (int)((hi - vstart) / 8);
-        const long long tail = vstart + (long long)nvec * 8;
+        const int head = min((int)(((16u - ((uint32_t)(uintptr_t)(row + lo) & 15u)) & 15u) >> 1), hi - lo);
+        const int vstart = lo + head;
+        const int nvec = (hi - vstart) >> 3;
+        const int tail = vstart + nvec * 8;
         const uint4 *vp = reinterpret_cast<const uint4 *>(row + vstart);
         uint4 v[kArgVec];
         if (nvec > 0) {
 #pragma unroll
-            for (int k = 0; k < kArgVec; ++k) {
-                const int idx = lane + k * 32;
-                v[k] = ld_stream_v4(vp + (idx < nvec ? idx : nvec - 1));
-            }
-            // one dependency point for all loads: nothing below is scheduled between them
+            for (int k = 0; k < kArgVec; ++k) v[k] = ld_stream_v4(vp + min(lane + k * 32, nvec - 1));
+            // dependency points: every load is issued before any of them is used
             asm volatile("" : "+r"(v[0].x), "+r"(v[0].y), "+r"(v[0].z), "+r"(v[0].w), "+r"(v[1].x), "+r"(v[1].y),
                          "+r"(v[1].z), "+r"(v[1].w), "+r"(v[2].x), "+r"(v[2].y), "+r"(v[2].z), "+r"(v[2].w),
                          "+r"(v[3].x), "+r"(v[3].y), "+r"(v[3].z), "+r"(v[3].w), "+r"(v[4].x), "+r"(v[4].y),
                          "+r"(v[4].z), "+r"(v[4].w), "+r"(v[5].x), "+r"(v[5].y), "+r"(v[5].z), "+r"(v[5].w),
                          "+r"(v[6].x), "+r"(v[6].y), "+r"(v[6].z), "+r"(v[6].w), "+r"(v[7].x), "+r"(v[7].y),
                          "+r"(v[7].z), "+r"(v[7].w));
+            asm volatile("" : "+r"(v[8].x), "+r"(v[8].y), "+r"(v[8].z), "+r"(v[8].w), "+r"(v[9].x), "+r"(v[9].y),
+                         "+r"(v[9].z), "+r"(v[9].w), "+r"(v[10].x), "+r"(v[10].y), "+r"(v[10].z), "+r"(v[10].w),
+                         "+r"(v[11].x), "+r"(v[11].y), "+r"(v[11].z), "+r"(v[11].w), "+r"(v[12].x), "+r"(v[12].y),
+                         "+r"(v[12].z), "+r"(v[12].w), "+r"(v[13].x), "+r"(v[13].y), "+r"(v[13].z), "+r"(v[13].w),
+                         "+r"(v[14].x), "+r"(v[14].y), "+r"(v[14].z), "+r"(v[14].w), "+r"(v[15].x), "+r"(v[15].y),
+                         "+r"(v[15].z), "+r"(v[15].w));
         }
         const bool has_head = lane < head, has_tail = lane < hi - tail;
         const float xh = has_head ? bf16_bits_to_float(row[lo + lane]) : NEG_INF;
         const float xt = has_tail ? bf16_bits_to_float(row[tail + lane]) : NEG_INF;
 
-        float vm[kArgVec];  // maximum of each vector (NaN-propagating)
-        float tm = max_nan(xh, xt);
+        // lane maximum: a packed bf16x2 tree over the valid vectors
+        __nv_bfloat162 m2 = __floats2bfloat162_rn(NEG_INF, NEG_INF);
 #pragma unroll
         for (int k = 0; k < kArgVec; ++k) {
             if (lane + k * 32 < nvec) {
-                __nv_bfloat162 a = __hmax2_nan(*reinterpret_cast<__nv_bfloat162 *>(&v[k].x),
-                                               *reinterpret_cast<__nv_bfloat162 *>(&v[k].y));
-                const __nv_bfloat162 c = __hmax2_nan(*reinterpret_cast<__nv_bfloat162 *>(&v[k].z),
-                                                     *reinterpret_cast<__nv_bfloat162 *>(&v[k].w));
-                a = __hmax2_nan(a, c);
-                vm[k] = __bfloat162float(__hmax_nan(a.x, a.y));
-            } else {
-                vm[k] = NEG_INF;
+                m2 = __hmax2_nan(m2, *reinterpret_cast<__nv_bfloat162 *>(&v[k].x));
+                m2 = __hmax2_nan(m2, *reinterpret_cast<__nv_bfloat162 *>(&v[k].y));
+                m2 = __hmax2_nan(m2, *reinterpret_cast<__nv_bfloat162 *>(&v[k].z));
+                m2 = __hmax2_nan(m2, *reinterpret_cast<__nv_bfloat162 *>(&v[k].w));
             }
-            tm = max_nan(tm, vm[k]);
         }
+        const float tm = max_nan(max_nan(__bfloat162float(__hmax_nan(m2.x, m2.y)), xh), xt);
         float bm = tm;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) bm = max_nan(bm, __shfl_xor_sync(0xffffffffu, bm, o));
@@ -154,12 +161,14 @@ __global__ void __launch_bounds__(kArgThreads) argmax_partial_kernel(const uint1
         int idx = 0x7fffffff;
         if (bm_nan ? (tm != tm) : (tm == bm)) {
             if (has_head && (bm_nan ? (xh != xh) : (xh == bm))) {
-                idx = (int)(lo + lane);
+                idx = lo + lane;
             } else {
                 int kf = -1;
 #pragma unroll
-                for (int k = kArgVec - 1; k >= 0; --k)
-                    if (lane + k * 32 < nvec && (bm_nan ? (vm[k] != vm[k]) : (vm[k] == bm))) kf = k;
+                for (int k = kArgVec - 1; k >= 0; --k) {
+                    const float vm = vec_max(v[k]);
+                    if (lane + k * 32 < nvec && (bm_nan ? (vm != vm) : (vm == bm))) kf = k;
+                }
                 if (kf >= 0) {
                     uint4 w = v[0];
 #pragma unroll
@@ -172,9 +181,9 @@ __global__ void __launch_bounds__(kArgThreads) argmax_partial_kernel(const uint1
                         const float x = bf16_bits_to_float((w4[e >> 1] >> ((e & 1) * 16)) & 0xFFFFu);
                         if (bm_nan ? (x != x) : (x == bm)) e_first = e;
                     }
-                    idx = (int)(vstart + (long long)(lane + kf * 32) * 8 + e_first);
+                    idx = vstart + (lane + kf * 32) * 8 + e_first;
                 } else if (has_tail) {
-                    idx = (int)(tail + lane);
+                    idx = tail + lane;
                 }
             }
         }
@@ -281,17 +290,17 @@ cudaError_t launch_accept(const uint16_t *logits, int V, const int32_t *draft, c
                           const uint32_t *mask, int B, int nb, int32_t *am, int32_t *n_acc, int32_t *path,
                           int32_t *bonus, int32_t *status, void *workspace, int num_sms, cudaStream_t stream)
 {
-    const int nchunk = (int)(((long long)V + kArgChunk - 1) / kArgChunk);
-    const long long units = (long long)nb * B * nchunk;
+    const int nchunk = (V + kArgChunk - 1) / kArgChunk;
+    const int units = nb * B * nchunk;
     long long grid = (long long)num_sms * kArgCtasPerSm;
-    const long long need = (units + kArgThreads / 32 - 1) / (kArgThreads / 32);
+    const long long need = ((long long)units + kArgThreads / 32 - 1) / (kArgThreads / 32);
     if (grid > need) grid = need;
     if (grid < 1) grid = 1;
     unsigned long long *best = static_cast<unsigned long long *>(workspace);
     cudaError_t e = cudaMemsetAsync(best, 0, accept_workspace_bytes(V, B, nb), stream);
     if (e != cudaSuccess) return e;
-    e = launch_dependent(argmax_partial_kernel, dim3((unsigned)grid), dim3(kArgThreads), 0, stream, logits,
-                         (long long)V, nchunk, units, best);
+    e = launch_dependent(argmax_partial_kernel, dim3((unsigned)grid), dim3(kArgThreads), 0, stream, logits, V, nchunk,
+                         units, best);
     if (e != cudaSuccess) return e;
     const int W = (B + 31) / 32;
     // its launch overlaps the argmax tail; it waits before reading the keys

@@ -134,7 +134,7 @@ int32_t tv_accept(const uint16_t *logits_d, int32_t V, const int32_t *draft_toke
         !aligned(argmax_d, 4) || !aligned(n_acc_d, 4) || !aligned(path_d, 4) || !aligned(bonus_d, 4) ||
         !aligned(dev_status_d, 4))
         return TV_ERR_INVALID_ARG;
-    if ((long long)nb * B * (((long long)V + 8191) / 8192) >= (1ll << 40)) return TV_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)nb * B * (((long long)V + 4095) / 4096) >= (1ll << 31)) return TV_ERR_UNSUPPORTED_SHAPE;
     if (nb == 0) return TV_OK;
     if (!workspace_d || !aligned(workspace_d, 8) || workspace_bytes < tv::accept_workspace_bytes(V, B, nb))
         return TV_ERR_INVALID_ARG;

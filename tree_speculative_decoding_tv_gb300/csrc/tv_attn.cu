@@ -755,7 +755,8 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
 
 // ------------------------------------------------------------------ merge
 
-constexpr int kMergeThreads = kM;  // one thread per row of the M tile
+constexpr int kMergeThreads = 128;  // 32 rows x 4 column quarters
+constexpr int kMergeSplit = kM / 32; // CTAs per M tile
 
 // Pieces before sequence b_end.  Whole warp.
 __device__ long long sched_prefix(const Sched &s, int b_end, int lane)
@@ -778,26 +779,27 @@ struct MergeParams {
     int nb, B, Hq, Hkv, G, NT, MT, max_pages, attn_grid;
 };
 
-// One CTA per M tile (sequence, kv head, mt), one thread per row.  An M tile
-// whose pair was cut between CTAs c0..c1 of the attention grid has one piece
-// in each: in c0's last slot (or its first, when the pair starts c0's share)
-// and in the first slot of c0+1 .. c1.  lse = ln sum_u e^{lse_u},
-// O = sum_u e^{lse_u - lse} O_u.  Partials are chunk-major, so the 128 threads
-// read 512 contiguous bytes per warp and load; two pieces' loads are in flight
-// together.
+// kMergeSplit CTAs per M tile (sequence, kv head, mt), each for 32 of its rows;
+// thread (warp q, lane l) owns row 32s + l and the columns 32q .. 32q+31.  An M
+// tile whose pair was cut between CTAs c0..c1 of the attention grid has one
+// piece in each: in c0's last slot (or its first, when the pair starts c0's
+// share) and in the first slot of c0+1 .. c1.  lse = ln sum_u e^{lse_u},
+// O = sum_u e^{lse_u - lse} O_u.  Partials are chunk-major, so a warp's loads
+// are 512 contiguous bytes, and the loads of four pieces are in flight together.
 __global__ void __launch_bounds__(kMergeThreads) tree_attn_merge_kernel(const MergeParams mp)
 {
     __shared__ int s_c0, s_c1, s_first0;
-    const int id = blockIdx.x;
+    const int id = blockIdx.x / kMergeSplit;
+    const int split = blockIdx.x % kMergeSplit;
     const int b = id / (mp.Hkv * mp.MT);
     const int g = (id / mp.MT) % mp.Hkv;
     const int mt = id % mp.MT;
     const int x = mt & 1;
     const int pm = mt >> 1;
-    const int r = threadIdx.x, lane = r & 31, warp = r >> 5;
+    const int lane = threadIdx.x & 31, q = threadIdx.x >> 5;
     const Sched sch{mp.prefix_lens, mp.nb, mp.B, mp.Hkv, mp.NT, mp.MT, mp.max_pages * kPage};
 
-    if (warp == 0) {  // prefix_lens is an input of both kernels: safe to read before the dependency wait
+    if (q == 0) {  // prefix_lens is an input of both kernels: safe to read before the dependency wait
         const long long total = sched_total(sch, lane);
         const long long C = active_ctas(total, mp.attn_grid);
         const long long start_b = sched_prefix(sch, b, lane);
@@ -823,61 +825,62 @@ __global__ void __launch_bounds__(kMergeThreads) tree_attn_merge_kernel(const Me
     // Every CTA waits for the attention grid (so this grid never completes before it);
     // past this point the partials are complete and visible.
     pdl_wait_primary();
-    if (c0 == c1) return;                      // the attention kernel wrote this M tile itself
+    if (c0 == c1) return;  // the attention kernel wrote this M tile itself
+    const int r = split * 32 + lane;
     const int i = mt * mp.NT + r / mp.G;
-    if (i >= mp.B) return;                     // a row past the tree
+    if (i >= mp.B) return;  // a row past the tree
 
     auto slot_of = [&](int c) -> size_t { return (2 * (size_t)c + (c == c0 ? first0 : 0)) * 2 + x; };
     float m = -INFINITY;
-#pragma unroll 4
+#pragma unroll 8
     for (int c = c0; c <= c1; ++c) m = fmaxf(m, __ldcg(mp.ws_lse + slot_of(c) * kM + r));
     float wsum = 0.f;
     if (m != -INFINITY) {
-#pragma unroll 4
+#pragma unroll 8
         for (int c = c0; c <= c1; ++c) wsum += expf(__ldcg(mp.ws_lse + slot_of(c) * kM + r) - m);
     }
     const float inv = m != -INFINITY ? 1.f / wsum : 0.f;
-    const size_t orow = ((size_t)b * mp.B + i) * mp.Hq + g * mp.G + r % mp.G;
-    uint4 *dst = reinterpret_cast<uint4 *>(mp.o + orow * kHeadDim);
 
-    for (int half = 0; half < 2; ++half) {  // 16 of the 32 four-column chunks at a time
-        float4 acc[16];
+    float4 acc[8];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (m != -INFINITY) {
-            for (int c = c0; c <= c1; c += 2) {
-                const bool two = c + 1 <= c1;
-                const float w0 = expf(__ldcg(mp.ws_lse + slot_of(c) * kM + r) - m) * inv;
-                const float w1 = two ? expf(__ldcg(mp.ws_lse + slot_of(c + 1) * kM + r) - m) * inv : 0.f;
-                const float4 *s0 = reinterpret_cast<const float4 *>(mp.ws_o) + (slot_of(c) * 32 + half * 16) * kM + r;
-                const float4 *s1 = reinterpret_cast<const float4 *>(mp.ws_o) +
-                                   (slot_of(two ? c + 1 : c) * 32 + half * 16) * kM + r;
-                float4 v0[16], v1[16];
+    for (int k = 0; k < 8; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (m != -INFINITY) {
+        for (int cb = c0; cb <= c1; cb += 4) {  // four pieces per round
+            float w[4];
+            float4 v[4][8];
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    v0[k] = __ldcg(s0 + (size_t)k * kM);
-                    v1[k] = two ? __ldcg(s1 + (size_t)k * kM) : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
+            for (int u = 0; u < 4; ++u) {
+                const int c = cb + u;
+                const bool in = c <= c1;
+                w[u] = in ? expf(__ldcg(mp.ws_lse + slot_of(c) * kM + r) - m) * inv : 0.f;
+                const float4 *src =
+                    reinterpret_cast<const float4 *>(mp.ws_o) + (slot_of(in ? c : c0) * 32 + q * 8) * kM + r;
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    acc[k].x = fmaf(w0, v0[k].x, fmaf(w1, v1[k].x, acc[k].x));
-                    acc[k].y = fmaf(w0, v0[k].y, fmaf(w1, v1[k].y, acc[k].y));
-                    acc[k].z = fmaf(w0, v0[k].z, fmaf(w1, v1[k].z, acc[k].z));
-                    acc[k].w = fmaf(w0, v0[k].w, fmaf(w1, v1[k].w, acc[k].w));
-                }
+                for (int k = 0; k < 8; ++k) v[u][k] = in ? __ldcg(src + (size_t)k * kM) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
-        }
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            uint4 w4;
-            w4.x = pack_bf16x2(acc[2 * k].x, acc[2 * k].y);
-            w4.y = pack_bf16x2(acc[2 * k].z, acc[2 * k].w);
-            w4.z = pack_bf16x2(acc[2 * k + 1].x, acc[2 * k + 1].y);
-            w4.w = pack_bf16x2(acc[2 * k + 1].z, acc[2 * k + 1].w);
-            dst[half * 8 + k] = w4;
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    acc[k].x = fmaf(w[u], v[u][k].x, acc[k].x);
+                    acc[k].y = fmaf(w[u], v[u][k].y, acc[k].y);
+                    acc[k].z = fmaf(w[u], v[u][k].z, acc[k].z);
+                    acc[k].w = fmaf(w[u], v[u][k].w, acc[k].w);
+                }
         }
     }
-    mp.lse[orow] = m != -INFINITY ? m + logf(wsum) : -INFINITY;
+    const size_t orow = ((size_t)b * mp.B + i) * mp.Hq + g * mp.G + r % mp.G;
+    uint4 *dst = reinterpret_cast<uint4 *>(mp.o + orow * kHeadDim) + q * 4;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        uint4 w4;
+        w4.x = pack_bf16x2(acc[2 * k].x, acc[2 * k].y);
+        w4.y = pack_bf16x2(acc[2 * k].z, acc[2 * k].w);
+        w4.z = pack_bf16x2(acc[2 * k + 1].x, acc[2 * k + 1].y);
+        w4.w = pack_bf16x2(acc[2 * k + 1].z, acc[2 * k + 1].w);
+        dst[k] = w4;
+    }
+    if (q == 0) mp.lse[orow] = m != -INFINITY ? m + logf(wsum) : -INFINITY;
 }
 
 // ------------------------------------------------------------------ host side
@@ -996,8 +999,8 @@ int32_t launch_attn(const tv_attn_args *a, int ctas, void *workspace, cudaStream
         // (griddepcontrol.wait) before reading partials.
         MergeParams mp{a->prefix_lens_d, p.ws_o, p.ws_lse, p.o, p.lse, p.nb, p.B, p.Hq, p.Hkv, p.G, p.NT, p.MT,
                        p.max_pages, ctas};
-        e = launch_dependent(tree_attn_merge_kernel, dim3((unsigned)(a->nb * a->Hkv * p.MT)), dim3(kMergeThreads), 0,
-                             stream, mp);
+        e = launch_dependent(tree_attn_merge_kernel, dim3((unsigned)(a->nb * a->Hkv * p.MT * kMergeSplit)),
+                             dim3(kMergeThreads), 0, stream, mp);
     }
     if (e != cudaSuccess) {
         *cuda_err = e;
