@@ -83,9 +83,10 @@ def test_accept_bit_exact(B, V):
     assert d.status.item() == 0
 
 
-def test_argmax_edge_values():
-    # ties, signed zeros, NaNs, infinities and a V that leaves every row unaligned
-    V = 1003
+@pytest.mark.parametrize("V", [1003, 2048, 4104])
+def test_argmax_edge_values(V):
+    # ties, signed zeros, NaNs, infinities; V = 1003 leaves rows unaligned (warp-unit kernel),
+    # V = 2048 and 4104 take the bulk-copy streaming kernel with slices straddling rows
     rows = np.full((6, V), 0xBF80, dtype=np.uint16)            # -1.0 everywhere
     rows[0, [5, 700]] = 0x4000                                   # tie between 5 and 700 -> 5
     rows[1, :] = 0x8000

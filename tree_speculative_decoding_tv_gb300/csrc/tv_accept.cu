@@ -19,10 +19,11 @@
 // workspace, zeroed at the start of every call.
 //
 // accept (kernel 2): one CTA per sequence, one thread per node, launched as a
-// programmatic dependent of the argmax.  Each thread reads its row's key, then
-// ok[] is packed into
-// W ballot words; node i is accepted iff (mask[i] & ~ok) == 0 (the root counts
-// as ok); the best (depth, -index) key is a block max; the path is read off
+// programmatic dependent of the argmax.  The tree inputs (parent, draft, the
+// mask rows) are loaded into shared memory while the argmax still runs; after
+// the dependency wait each thread reads its row's key, ok[] is packed into W
+// ballot words, node i is accepted iff (mask[i] & ~ok) == 0 (the root counts as
+// ok), the best (depth, -index) key is a block max, and the path is read off
 // the chosen node's mask bits in ascending order.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -89,11 +90,24 @@ __device__ __forceinline__ float vec_max(const uint4 &v)
     return __bfloat162float(__hmax_nan(a.x, a.y));
 }
 
+// Order-preserving 32-bit rank of a value (the high half of its key): every NaN
+// on top, -0 with +0, never 0.
+__device__ __forceinline__ uint32_t value_rank(float v) { return (uint32_t)(argmax_key(v, 0) >> 32); }
+
+__device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t w) { return *reinterpret_cast<__nv_bfloat162 *>(&w); }
+
+__device__ __forceinline__ __nv_bfloat162 vec_max2(const uint4 &v)
+{
+    return __hmax2_nan(__hmax2_nan(as_bf2(v.x), as_bf2(v.y)), __hmax2_nan(as_bf2(v.z), as_bf2(v.w)));
+}
+
 // One unit = kArgChunk logits of one row = one warp: each lane holds kArgVec
-// 16-byte vectors in registers (all loads in flight at once), the warp agrees
-// on the unit's maximum with shuffles, and the lanes holding it find its first
-// position in two steps (first vector whose maximum matches, then the element
-// inside it).  No block-level synchronisation; 32-bit index arithmetic.
+// 16-byte vectors in registers (all loads in flight at once) and folds them as
+// a tree of bf16x2 maxima, keeping each vector's maximum; the warp agrees on the
+// unit's maximum with one integer max-reduction of its rank, the lanes holding
+// it find their first position in two steps (first vector whose maximum
+// matches, then the element inside it), and one integer min-reduction picks the
+// smallest.  No block-level synchronisation; 32-bit index arithmetic.
 __global__ void __launch_bounds__(kArgThreads) argmax_partial_kernel(const uint16_t *__restrict__ logits, int V,
                                                                      int nchunk, int units,
                                                                      unsigned long long *__restrict__ best)
@@ -140,34 +154,35 @@ __global__ void __launch_bounds__(kArgThreads) argmax_partial_kernel(const uint1
         const float xh = has_head ? bf16_bits_to_float(row[lo + lane]) : NEG_INF;
         const float xt = has_tail ? bf16_bits_to_float(row[tail + lane]) : NEG_INF;
 
-        // lane maximum: a packed bf16x2 tree over the valid vectors
-        __nv_bfloat162 m2 = __floats2bfloat162_rn(NEG_INF, NEG_INF);
+        // lane maximum: a bf16x2 tree over the vectors (clamped duplicates of the last
+        // vector do not change it); the vector maxima stay for the search
+        __nv_bfloat162 vm[kArgVec];
 #pragma unroll
-        for (int k = 0; k < kArgVec; ++k) {
-            if (lane + k * 32 < nvec) {
-                m2 = __hmax2_nan(m2, *reinterpret_cast<__nv_bfloat162 *>(&v[k].x));
-                m2 = __hmax2_nan(m2, *reinterpret_cast<__nv_bfloat162 *>(&v[k].y));
-                m2 = __hmax2_nan(m2, *reinterpret_cast<__nv_bfloat162 *>(&v[k].z));
-                m2 = __hmax2_nan(m2, *reinterpret_cast<__nv_bfloat162 *>(&v[k].w));
-            }
-        }
-        const float tm = max_nan(max_nan(__bfloat162float(__hmax_nan(m2.x, m2.y)), xh), xt);
-        float bm = tm;
+        for (int k = 0; k < kArgVec; ++k) vm[k] = vec_max2(v[k]);
+        __nv_bfloat162 t[kArgVec / 2];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) bm = max_nan(bm, __shfl_xor_sync(0xffffffffu, bm, o));
-        const bool bm_nan = bm != bm;
+        for (int k = 0; k < kArgVec / 2; ++k) t[k] = __hmax2_nan(vm[2 * k], vm[2 * k + 1]);
+#pragma unroll
+        for (int w = kArgVec / 4; w > 0; w >>= 1)
+#pragma unroll
+            for (int k = 0; k < w; ++k) t[k] = __hmax2_nan(t[2 * k], t[2 * k + 1]);
+        const float vmax = nvec > 0 ? __bfloat162float(__hmax_nan(t[0].x, t[0].y)) : NEG_INF;
+        const float tm = max_nan(max_nan(vmax, xh), xt);
+        const uint32_t r = value_rank(tm);
+        const uint32_t wr = __reduce_max_sync(0xffffffffu, r);
 
-        // first position of the unit maximum (elements in index order: head, vectors, tail)
-        int idx = 0x7fffffff;
-        if (bm_nan ? (tm != tm) : (tm == bm)) {
-            if (has_head && (bm_nan ? (xh != xh) : (xh == bm))) {
+        // first position of the unit maximum in this lane (index order: head, vectors, tail)
+        uint32_t idx = 0x7fffffffu;
+        if (r == wr) {
+            const bool nan = tm != tm;
+            if (has_head && (nan ? (xh != xh) : (xh == tm))) {
                 idx = lo + lane;
             } else {
                 int kf = -1;
 #pragma unroll
                 for (int k = kArgVec - 1; k >= 0; --k) {
-                    const float vm = vec_max(v[k]);
-                    if (lane + k * 32 < nvec && (bm_nan ? (vm != vm) : (vm == bm))) kf = k;
+                    const float x = __bfloat162float(__hmax_nan(vm[k].x, vm[k].y));
+                    if (lane + k * 32 < nvec && (nan ? (x != x) : (x == tm))) kf = k;
                 }
                 if (kf >= 0) {
                     uint4 w = v[0];
@@ -175,11 +190,11 @@ __global__ void __launch_bounds__(kArgThreads) argmax_partial_kernel(const uint1
                     for (int k = 1; k < kArgVec; ++k)
                         if (k == kf) w = v[k];
                     const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
-                    int e_first = 8;
+                    int e_first = 7;
 #pragma unroll
                     for (int e = 7; e >= 0; --e) {
                         const float x = bf16_bits_to_float((w4[e >> 1] >> ((e & 1) * 16)) & 0xFFFFu);
-                        if (bm_nan ? (x != x) : (x == bm)) e_first = e;
+                        if (nan ? (x != x) : (x == tm)) e_first = e;
                     }
                     idx = vstart + (lane + kf * 32) * 8 + e_first;
                 } else if (has_tail) {
@@ -187,9 +202,8 @@ __global__ void __launch_bounds__(kArgThreads) argmax_partial_kernel(const uint1
                 }
             }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) idx = min(idx, __shfl_xor_sync(0xffffffffu, idx, o));
-        if (lane == 0) atomicMax(best + row_id, argmax_key(bm, idx));
+        idx = __reduce_min_sync(0xffffffffu, idx);
+        if (lane == 0) atomicMax(best + row_id, ((unsigned long long)wr << 32) | (0xFFFFFFFFu - idx));
     }
 }
 
@@ -202,14 +216,30 @@ __global__ void __launch_bounds__(kMaxB) accept_kernel(const unsigned long long 
                                                        int32_t *status)
 {
     __shared__ int s_am[kMaxB];
+    __shared__ uint32_t s_mask[kMaxB * kMaxW];
     __shared__ uint32_t s_ok[kMaxW];
-    __shared__ uint32_t s_vmask[kMaxW];
     __shared__ int s_best[kMaxB / 32];
     __shared__ int s_bad;
 
     const int b = blockIdx.x;
     const int i = threadIdx.x;
     const int lane = i & 31, wid = i >> 5;
+
+    // The tree inputs were written before the argmax kernel began (the key memset
+    // ahead of it completes only after all earlier work), so they are read while
+    // the argmax is still running; only the keys wait for it.
+    int p = -1, d = 0;
+    uint32_t mrow[kMaxW];
+    if (i < B) {
+        p = parent[(size_t)b * B + i];
+        d = draft[(size_t)b * B + i];
+#pragma unroll
+        for (int w = 0; w < kMaxW; ++w)  // all row words in flight at once
+            if (w < W) mrow[w] = mask[((size_t)b * B + i) * W + w];
+#pragma unroll
+        for (int w = 0; w < kMaxW; ++w)
+            if (w < W) s_mask[i * W + w] = mrow[w];
+    }
     if (i == 0) s_bad = 0;
     pdl_wait_primary();  // the argmax keys are complete from here on
 
@@ -223,12 +253,11 @@ __global__ void __launch_bounds__(kMaxB) accept_kernel(const unsigned long long 
 
     bool ok = true;
     if (i > 0 && i < B) {
-        const int p = parent[(size_t)b * B + i];
         if (p < 0 || p >= i) {
             ok = false;
             s_bad = 1;
         } else {
-            ok = draft[(size_t)b * B + i] == s_am[p];
+            ok = d == s_am[p];
         }
     }
     const uint32_t okw = __ballot_sync(0xffffffffu, ok);
@@ -237,38 +266,30 @@ __global__ void __launch_bounds__(kMaxB) accept_kernel(const unsigned long long 
 
     int key = -1;  // depth * 512 + (511 - node) of an accepted node
     if (i < B) {
-        const uint32_t *mrow = mask + ((size_t)b * B + i) * W;
         bool acc = true;
         int bits = 0;
         for (int w = 0; w < W; ++w) {
-            const uint32_t mw = mrow[w];
+            const uint32_t mw = s_mask[i * W + w];
             acc = acc && ((mw & ~s_ok[w]) == 0u);
             bits += __popc(mw);
         }
         if (acc) key = (bits - 1) * 512 + (511 - i);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) key = max(key, __shfl_xor_sync(0xffffffffu, key, o));
+    key = __reduce_max_sync(0xffffffffu, key);
     if (lane == 0) s_best[wid] = key;
     __syncthreads();
-    if (i == 0) {
-        int k = s_best[0];
-        for (int w = 1; w < (int)(blockDim.x >> 5); ++w) k = max(k, s_best[w]);
-        s_best[0] = k;
-    }
-    __syncthreads();
-    const int top = s_best[0];
+    int top = s_best[0];
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) top = max(top, s_best[w]);
     const int vstar = top >= 0 ? 511 - (top & 511) : 0;
     const int dep = top >= 0 ? (top >> 9) : 0;
-    if (i < W) s_vmask[i] = mask[((size_t)b * B + vstar) * W + i];
-    __syncthreads();
+    const uint32_t *vmask = s_mask + vstar * W;
 
     if (i < B) {
         const int w = i >> 5;
-        const uint32_t mw = s_vmask[w];
+        const uint32_t mw = vmask[w];
         if ((mw >> lane) & 1u) {
             int before = __popc(mw & ((1u << lane) - 1u));
-            for (int k = 0; k < w; ++k) before += __popc(s_vmask[k]);
+            for (int k = 0; k < w; ++k) before += __popc(vmask[k]);
             path[(size_t)b * B + before] = i;
         }
         if (i > dep) path[(size_t)b * B + i] = -1;

@@ -115,6 +115,7 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, int3
         : "memory");
 }
 
+// Non-tensor bulk copy global -> shared (both 16-byte aligned, size a multiple of 16).
 // ------------------------------------------------------------------- tcgen05
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
