@@ -784,8 +784,9 @@ struct MergeParams {
 // tile whose pair was cut between CTAs c0..c1 of the attention grid has one
 // piece in each: in c0's last slot (or its first, when the pair starts c0's
 // share) and in the first slot of c0+1 .. c1.  lse = ln sum_u e^{lse_u},
-// O = sum_u e^{lse_u - lse} O_u.  Partials are chunk-major, so a warp's loads
-// are 512 contiguous bytes, and the loads of four pieces are in flight together.
+// O = sum_u e^{lse_u - lse} O_u, in one pass over batches of four pieces whose
+// lse and O loads are all in flight together (chunk-major partials: a warp's
+// loads are 512 contiguous bytes), with a running maximum between batches.
 __global__ void __launch_bounds__(kMergeThreads) tree_attn_merge_kernel(const MergeParams mp)
 {
     __shared__ int s_c0, s_c1, s_first0;
@@ -831,43 +832,57 @@ __global__ void __launch_bounds__(kMergeThreads) tree_attn_merge_kernel(const Me
     if (i >= mp.B) return;  // a row past the tree
 
     auto slot_of = [&](int c) -> size_t { return (2 * (size_t)c + (c == c0 ? first0 : 0)) * 2 + x; };
-    float m = -INFINITY;
-#pragma unroll 8
-    for (int c = c0; c <= c1; ++c) m = fmaxf(m, __ldcg(mp.ws_lse + slot_of(c) * kM + r));
-    float wsum = 0.f;
-    if (m != -INFINITY) {
-#pragma unroll 8
-        for (int c = c0; c <= c1; ++c) wsum += expf(__ldcg(mp.ws_lse + slot_of(c) * kM + r) - m);
-    }
-    const float inv = m != -INFINITY ? 1.f / wsum : 0.f;
-
+    // One pass: each batch's lse and O loads are in flight together; a running
+    // maximum rescales the sums between batches.
+    float m = -INFINITY, wsum = 0.f;
     float4 acc[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (m != -INFINITY) {
-        for (int cb = c0; cb <= c1; cb += 4) {  // four pieces per round
-            float w[4];
-            float4 v[4][8];
+    for (int cb = c0; cb <= c1; cb += 4) {
+        float l[4];
+        float4 v[4][8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int c = cb + u;
-                const bool in = c <= c1;
-                w[u] = in ? expf(__ldcg(mp.ws_lse + slot_of(c) * kM + r) - m) * inv : 0.f;
-                const float4 *src =
-                    reinterpret_cast<const float4 *>(mp.ws_o) + (slot_of(in ? c : c0) * 32 + q * 8) * kM + r;
+        for (int u = 0; u < 4; ++u) {
+            const int c = cb + u;
+            const bool in = c <= c1;
+            const size_t slot = slot_of(in ? c : c0);
+            l[u] = in ? __ldcg(mp.ws_lse + slot * kM + r) : -INFINITY;
+            const float4 *src = reinterpret_cast<const float4 *>(mp.ws_o) + (slot * 32 + q * 8) * kM + r;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) v[u][k] = in ? __ldcg(src + (size_t)k * kM) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    acc[k].x = fmaf(w[u], v[u][k].x, acc[k].x);
-                    acc[k].y = fmaf(w[u], v[u][k].y, acc[k].y);
-                    acc[k].z = fmaf(w[u], v[u][k].z, acc[k].z);
-                    acc[k].w = fmaf(w[u], v[u][k].w, acc[k].w);
-                }
+            for (int k = 0; k < 8; ++k) v[u][k] = in ? __ldcg(src + (size_t)k * kM) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        const float mb = fmaxf(fmaxf(m, fmaxf(l[0], l[1])), fmaxf(l[2], l[3]));
+        if (mb == -INFINITY) continue;  // no piece with a visible key yet
+        const float sc = expf(m - mb);  // 0 while m is still -inf
+        wsum *= sc;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            acc[k].x *= sc;
+            acc[k].y *= sc;
+            acc[k].z *= sc;
+            acc[k].w *= sc;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float w = expf(l[u] - mb);  // 0 for an empty piece
+            wsum += w;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                acc[k].x = fmaf(w, v[u][k].x, acc[k].x);
+                acc[k].y = fmaf(w, v[u][k].y, acc[k].y);
+                acc[k].z = fmaf(w, v[u][k].z, acc[k].z);
+                acc[k].w = fmaf(w, v[u][k].w, acc[k].w);
+            }
+        }
+        m = mb;
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        acc[k].x *= inv;
+        acc[k].y *= inv;
+        acc[k].z *= inv;
+        acc[k].w *= inv;
     }
     const size_t orow = ((size_t)b * mp.B + i) * mp.Hq + g * mp.G + r % mp.G;
     uint4 *dst = reinterpret_cast<uint4 *>(mp.o + orow * kHeadDim) + q * 4;
@@ -880,7 +895,7 @@ __global__ void __launch_bounds__(kMergeThreads) tree_attn_merge_kernel(const Me
         w4.w = pack_bf16x2(acc[2 * k + 1].z, acc[2 * k + 1].w);
         dst[k] = w4;
     }
-    if (q == 0) mp.lse[orow] = m != -INFINITY ? m + logf(wsum) : -INFINITY;
+    if (q == 0) mp.lse[orow] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
 }
 
 // ------------------------------------------------------------------ host side
