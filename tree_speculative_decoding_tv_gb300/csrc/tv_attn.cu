@@ -162,7 +162,7 @@ __device__ long long sched_total(const Sched &s, int lane)
     long long tot = 0;
     for (int base = 0; base < s.nb; base += 32) {
         const int b = base + lane;
-        const long long t = (b < s.nb) ? (long long)s.Hkv * head_tiles(s, __ldg(s.prefix_lens + b)) : 0;
+        const long long t = (b < s.nb) ? (long long)s.Hkv * head_tiles(s, __ldcg(s.prefix_lens + b)) : 0;
         tot += warp_sum_ll(t);
     }
     return tot;
@@ -174,7 +174,7 @@ __device__ void sched_locate(const Sched &s, long long t, int lane, int &b_out, 
     long long acc = 0;
     for (int base = 0; base < s.nb; base += 32) {
         const int b = base + lane;
-        const long long tb = (b < s.nb) ? (long long)s.Hkv * head_tiles(s, __ldg(s.prefix_lens + b)) : 0;
+        const long long tb = (b < s.nb) ? (long long)s.Hkv * head_tiles(s, __ldcg(s.prefix_lens + b)) : 0;
         long long incl = tb;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -219,7 +219,7 @@ struct Seg {
 __device__ __forceinline__ bool next_seg(const Sched &s, Cursor &c, Seg &sg)
 {
     while (c.left > 0 && c.b < s.nb) {
-        const int P = __ldg(s.prefix_lens + c.b);
+        const int P = __ldcg(s.prefix_lens + c.b);
         const int ht = head_tiles(s, P);
         if (c.off >= (long long)ht * s.Hkv) {
             ++c.b;
@@ -322,9 +322,12 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
-    // Everything above touches only this CTA; the inputs may come from the previous
-    // kernel in the stream (launched as its programmatic dependent), so wait here.
-    pdl_wait_primary();
+    // This kernel is launched as a programmatic dependent of the previous kernel in the
+    // stream (normally tv_build_mask), which waits for everything before it and then
+    // lets this grid start.  So q, K/V, the block table and prefix_lens (inputs written
+    // before that kernel) are read at once (through L2: TMA, __ldcg); only the ancestor
+    // masks, which that kernel may still be writing, wait for it (griddepcontrol.wait
+    // before the first masked tile, and in every thread before it exits).
     if (warp == 2) {
         const long long total = sched_total(sch, lane);
         const long long C = active_ctas(total, gridDim.x);
@@ -344,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
         }
         if (blockIdx.x == 0) {
             for (int b = lane; b < sch.nb; b += 32) {
-                const int P = __ldg(sch.prefix_lens + b);
+                const int P = __ldcg(sch.prefix_lens + b);
                 if (P < 0 || P > sch.max_tokens - sch.B) report_status(p.status, TV_ERR_INVALID_ARG);
             }
         }
@@ -383,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                 const int pg = jb * (kN / kPage) + lane;
                 int r = oob_row;
                 if (pg * kPage < kv_len) {
-                    const int id = __ldg(p.block_table + (size_t)sg.b * p.max_pages + pg);
+                    const int id = __ldcg(p.block_table + (size_t)sg.b * p.max_pages + pg);
                     if (id >= 0 && id < p.num_blocks)
                         r = (id * p.Hkv + sg.g) * kPage;
                     else
@@ -426,15 +429,25 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         // Slots x = 0, 1 own S_x / O_x.  Pair segments: slot x is M tile x over every
-        // KV tile.  Single-tile segments: both slots use Q tile A, slot x takes the
-        // KV tiles t with t % 2 == x, and the softmax warpgroups merge at the end.
+        // KV tile.  Single-tile segments: both slots use Q tile A, slot x takes the KV
+        // tiles t with t % 2 == x, and the softmax warpgroups merge at the end.
+        // tcgen05.mma issue stalls while the tensor pipe is busy, so everything this warp
+        // does between two MMA groups is pipe idle time: a slot's PV(t) and its next QK
+        // go out back to back under one commit (S_FULL, which the softmax needs anyway),
+        // a step's K/V waits are done once up front, PV_DONE is committed only after a
+        // slot's last PV of the segment, and ring releases follow both slots' groups.
         regs_decrease<kRegsLow>();
         Cursor cur = cur0;
         Seg sg;
         uint32_t kv = 0, seg_i = 0;
-        uint32_t gs[2] = {0, 0}, sc[2] = {0, 0};  // tiles and segments per slot so far (barrier phases)
+        // tiles and segments per slot so far (barrier phases)
+        uint32_t gs0 = 0, gs1 = 0, sc0 = 0, sc1 = 0;
         bool ok = true;
-        auto issue_qk = [&](int x, int qx, uint32_t kt) {
+        auto wait_bar = [&](int idx, uint32_t parity) { return mbar_wait(BAR(idx), parity, abort_flag, p.status); };
+        // ring position q: K(j) = 2j, V(j) = 2j + 1 (KV tile counter j over the whole CTA)
+        auto full = [&](uint32_t q) { return wait_bar(BAR_KV_FULL + ring_slot(q), ring_phase(q)); };
+        auto release = [&](uint32_t q) { umma_commit(BAR(BAR_KV_EMPTY + ring_slot(q))); };
+        auto qk = [&](int x, int qx, uint32_t kt) {  // S_x = Q_qx K(kt)^T (lane 0)
             const uint32_t qb = sQ + qx * kTileBytes, kb = sKV + ring_slot(2 * kt) * kTileBytes;
 #pragma unroll
             for (int kk = 0; kk < kHeadDim / 16; ++kk) {
@@ -442,86 +455,113 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                 umma_bf16_ss(tmem + tmem_s(x), sdesc_kmajor_sw128(qb + off), sdesc_kmajor_sw128(kb + off), kIdescQK,
                              kk > 0 ? 1u : 0u);
             }
-            umma_commit(BAR(BAR_S_FULL + x));
         };
-        auto issue_pv = [&](int x, uint32_t kt, bool accumulate) {
+        auto pv = [&](int x, uint32_t kt, bool accumulate) {  // O_x (+)= P_x V(kt) (lane 0)
             const uint32_t vb = sKV + ring_slot(2 * kt + 1) * kTileBytes;
 #pragma unroll
             for (int kk = 0; kk < kN / 16; ++kk)
                 umma_bf16_ts(tmem + tmem_o(x), tmem + tmem_s(x) + kk * 8, sdesc_mnmajor_sw128(vb + kk * 2048, kHalfBytes),
                              kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
-            umma_commit(BAR(BAR_PV_DONE + x));
         };
-        auto wait_k = [&](uint32_t kt) {
-            return mbar_wait(BAR(BAR_KV_FULL + ring_slot(2 * kt)), ring_phase(2 * kt), abort_flag, p.status);
+        // P_x of the slot's lx-th tile in the segment is in TMEM; before the slot's first PV
+        // of a segment, the previous segment's epilogue of slot x has read O_x
+        auto wait_p = [&](int x, int lx) -> bool {
+            const uint32_t gsx = x ? gs1 : gs0, scx = x ? sc1 : sc0;
+            if (!wait_bar(BAR_P_FULL + x, (gsx + lx) & 1)) return false;
+            return !(lx == 0 && scx > 0 && !wait_bar(BAR_O_EMPTY + x, (scx - 1) & 1));
         };
         while (ok && next_seg(sch, cur, sg)) {
             const int n = sg.j1 - sg.j0;
             const bool pair = sg.has_b;
             const int nx0 = pair ? n : (n + 1) / 2, nx1 = pair ? n : n / 2;
-            if (!mbar_wait(BAR(BAR_Q_FULL), seg_i & 1, abort_flag, p.status) || !wait_k(kv)) { ok = false; break; }
-            tc_fence_after();
-            if (lane == 0) {
-                issue_qk(0, 0, kv);
-                if (pair) issue_qk(1, 1, kv);
-                umma_commit(BAR(BAR_KV_EMPTY + ring_slot(2 * kv)));
-            }
-            __syncwarp();
-            if (!pair && n > 1) {
-                if (!wait_k(kv + 1)) { ok = false; break; }
+            if (!wait_bar(BAR_Q_FULL, seg_i & 1)) { ok = false; break; }
+            if (pair) {
+                if (!full(2 * kv)) { ok = false; break; }
                 tc_fence_after();
                 if (lane == 0) {
-                    issue_qk(1, 0, kv + 1);
-                    umma_commit(BAR(BAR_KV_EMPTY + ring_slot(2 * kv + 2)));
+                    qk(0, 0, kv);
+                    umma_commit(BAR(BAR_S_FULL + 0));
+                    qk(1, 1, kv);
+                    umma_commit(BAR(BAR_S_FULL + 1));
+                    release(2 * kv);
+                    if (n == 1) umma_commit(BAR(BAR_Q_EMPTY));
                 }
                 __syncwarp();
-            }
-            if (lane == 0 && ((pair && n == 1) || (!pair && n <= 2))) umma_commit(BAR(BAR_Q_EMPTY));
-            for (int t = 0; t < n && ok; ++t) {
-                const uint32_t kt = kv + t;
-                const int tn = t + (pair ? 1 : 2);  // the slot's next KV tile
-                for (int xi = 0; xi < (pair ? 2 : 1); ++xi) {
-                    const int x = pair ? xi : (t & 1);
-                    const int lx = pair ? t : (t >> 1);
-                    if (!mbar_wait(BAR(BAR_P_FULL + x), (gs[x] + lx) & 1, abort_flag, p.status)) { ok = false; break; }
-                    if (lx == 0 && sc[x] > 0 &&
-                        !mbar_wait(BAR(BAR_O_EMPTY + x), (sc[x] - 1) & 1, abort_flag, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    if (xi == 0 && !mbar_wait(BAR(BAR_KV_FULL + ring_slot(2 * kt + 1)), ring_phase(2 * kt + 1),
-                                              abort_flag, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    if (lane == 0) issue_pv(x, kt, lx > 0);
-                    __syncwarp();
-                    // the next QK of this slot only waits for its K tile after PV(t) is queued
-                    if (tn < n) {
-                        if (xi == 0 && !wait_k(kv + tn)) {
-                            ok = false;
-                            break;
-                        }
+                for (int t = 0; t < n; ++t) {
+                    const uint32_t kt = kv + t;
+                    const bool more = t + 1 < n;
+                    if (!full(2 * kt + 1) || (more && !full(2 * kt + 2))) { ok = false; break; }
+                    for (int x = 0; x < 2; ++x) {
+                        if (!wait_p(x, t)) { ok = false; break; }
                         tc_fence_after();
-                        if (lane == 0) issue_qk(x, pair ? x : 0, kv + tn);
+                        if (lane == 0) {
+                            pv(x, kt, t > 0);
+                            if (more) {
+                                qk(x, x, kt + 1);
+                                umma_commit(BAR(BAR_S_FULL + x));
+                            } else {
+                                umma_commit(BAR(BAR_PV_DONE + x));
+                            }
+                        }
+                        __syncwarp();
+                    }
+                    if (!ok) break;
+                    if (lane == 0) {
+                        release(2 * kt + 1);
+                        if (more) release(2 * kt + 2);
+                        if (t + 2 == n) umma_commit(BAR(BAR_Q_EMPTY));
+                    }
+                    __syncwarp();
+                }
+            } else {
+                // issue order: QK_0(0), QK_1(1), then per tile t: PV_{t%2}(t), QK_{t%2}(t+2)
+                if (!full(2 * kv) || (n > 1 && !full(2 * kv + 2))) { ok = false; break; }
+                tc_fence_after();
+                if (lane == 0) {
+                    qk(0, 0, kv);
+                    umma_commit(BAR(BAR_S_FULL + 0));
+                    release(2 * kv);
+                    if (n > 1) {
+                        qk(1, 0, kv + 1);
+                        umma_commit(BAR(BAR_S_FULL + 1));
+                        release(2 * kv + 2);
+                    }
+                    if (n <= 2) umma_commit(BAR(BAR_Q_EMPTY));
+                }
+                __syncwarp();
+                for (int t = 0; t < n; ++t) {
+                    const uint32_t kt = kv + t;
+                    const int x = t & 1;
+                    const bool more = t + 2 < n;
+                    // PV(t) waits only for V(t): these segments are bandwidth-bound, and K(t+2)
+                    // is two tiles further out in the ring
+                    if (!full(2 * kt + 1) || !wait_p(x, t >> 1)) { ok = false; break; }
+                    tc_fence_after();
+                    if (lane == 0) {
+                        pv(x, kt, t > 1);
+                        if (!more) umma_commit(BAR(BAR_PV_DONE + x));
+                        release(2 * kt + 1);
+                    }
+                    __syncwarp();
+                    if (more) {
+                        if (!full(2 * kt + 4)) { ok = false; break; }
+                        tc_fence_after();
+                        if (lane == 0) {
+                            qk(x, 0, kt + 2);
+                            umma_commit(BAR(BAR_S_FULL + x));
+                            release(2 * kt + 4);
+                            if (t + 3 == n) umma_commit(BAR(BAR_Q_EMPTY));
+                        }
                         __syncwarp();
                     }
                 }
-                if (!ok) break;
-                if (lane == 0) {
-                    umma_commit(BAR(BAR_KV_EMPTY + ring_slot(2 * kt + 1)));
-                    if (tn < n) umma_commit(BAR(BAR_KV_EMPTY + ring_slot(2 * (kv + tn))));
-                    if (t + (pair ? 2 : 3) == n) umma_commit(BAR(BAR_Q_EMPTY));
-                }
-                __syncwarp();
             }
             if (!ok) break;
             kv += n;
-            gs[0] += nx0;
-            gs[1] += nx1;
-            if (nx0 > 0) ++sc[0];
-            if (nx1 > 0) ++sc[1];
+            gs0 += nx0;
+            gs1 += nx1;
+            if (nx0 > 0) ++sc0;
+            if (nx1 > 0) ++sc1;
             ++seg_i;
         }
         // Every MMA this CTA issued completes before TMEM is released.
@@ -547,8 +587,10 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
         float *sh_l = sh_m + kM;
         Cursor cur = cur0;
         Seg sg;
-        uint32_t gx = 0, seg_i = 0, n_merge = 0;  // n_merge: single-tile hand-overs so far (ML_* phases)
-        bool ok = true;
+        // gx: this slot's tiles so far; sx: segments with tiles for this slot; n_merge:
+        // single-tile hand-overs so far (ML_* phases)
+        uint32_t gx = 0, sx = 0, seg_i = 0, n_merge = 0;
+        bool ok = true, mask_ready = false;
         while (ok && next_seg(sch, cur, sg)) {
             const int n = sg.j1 - sg.j0;
             const bool pair = sg.has_b;
@@ -580,6 +622,10 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
 
                 // tree / tail mask (prefix-only tiles skip it), then the row max of the raw scores
                 if (!(valid && k0 + kN <= sg.P)) {
+                    if (!mask_ready) {  // the masks may come from the previous kernel
+                        pdl_wait_primary();
+                        mask_ready = true;
+                    }
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const uint32_t vis = valid ? visible_bits(k0 + 32 * c, sg.P, p.B, mrow, p.W) : 0u;
@@ -587,15 +633,16 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                         for (int e = 0; e < 32; ++e) s[c][e] = ((vis >> e) & 1u) ? s[c][e] : 0xff800000u;
                     }
                 }
-                float mx[8];
+                float mx[4];  // four independent chains of 3-input maxima
 #pragma unroll
-                for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
+                for (int c = 0; c < 4; ++c) {
+                    mx[c] = fmax3(__uint_as_float(s[c][0]), __uint_as_float(s[c][1]), __uint_as_float(s[c][2]));
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(s[c][e]));
-                const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+                    for (int e = 3; e < 31; e += 2)
+                        mx[c] = fmax3(mx[c], __uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1]));
+                    mx[c] = fmaxf(mx[c], __uint_as_float(s[c][31]));
+                }
+                const float tmax = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sl2;
 
                 // move the running max only when it grows by more than 2^8; the commit
                 // behind S(t) also covered this slot's previous PV, so O_x is stable here
@@ -609,26 +656,27 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                 }
                 const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
 
-                // P = exp2(s * scale * log2 e - m) as bf16 pairs over the first 64 columns of S
-                float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                // P = exp2(s * scale * log2 e - m) as bf16 pairs, packed in place (pair e of
+                // block c lands in s[c][e], e < 16) and stored over the first 64 columns of S
+                float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t pw[32];
+                for (int c = 0; c < 4; ++c) {
 #pragma unroll
-                    for (int c2 = 0; c2 < 2; ++c2) {
-                        const int c = 2 * hh + c2;
-#pragma unroll
-                        for (int e2 = 0; e2 < 16; ++e2) {
-                            const float a = ex2_approx(fmaf(__uint_as_float(s[c][2 * e2]), sl2, neg_m));
-                            const float b = ex2_approx(fmaf(__uint_as_float(s[c][2 * e2 + 1]), sl2, neg_m));
-                            ls[(2 * e2) & 7] += a;
-                            ls[(2 * e2 + 1) & 7] += b;
-                            pw[c2 * 16 + e2] = pack_bf16x2(a, b);
+                    for (int e2 = 0; e2 < 16; ++e2) {
+                        const float a = ex2_approx(fmaf(__uint_as_float(s[c][2 * e2]), sl2, neg_m));
+                        const float b = ex2_approx(fmaf(__uint_as_float(s[c][2 * e2 + 1]), sl2, neg_m));
+                        if (e2 & 1) {
+                            l2 += a;
+                            l3 += b;
+                        } else {
+                            l0 += a;
+                            l1 += b;
                         }
+                        s[c][e2] = pack_bf16x2(a, b);
                     }
-                    tmem_st32(lane_addr + col_s + hh * 32, pw);
+                    if (c & 1) tmem_st16x2(lane_addr + col_s + (c >> 1) * 32, s[c - 1], s[c]);
                 }
-                l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+                l_run += (l0 + l1) + (l2 + l3);
                 // O_x *= alpha before PV(t) adds this tile (PV(t) waits for P_FULL below).  TMEM
                 // loads/stores are warp-wide (.sync.aligned), so the whole warp takes the branch
                 // when any lane needs it, each lane with its own factor.  Before this slot's first
@@ -650,9 +698,10 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
             }
             if (!ok) break;
 
-            // epilogue: O_x of this segment is complete once its last PV lands
-            const uint32_t last = gx + nx - 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(BAR(BAR_PV_DONE + x), last & 1, abort_flag, p.status))) break;
+            // epilogue: O_x of this segment is complete once its last PV lands (one PV_DONE
+            // phase per segment in which the slot has tiles)
+            if (!__all_sync(0xffffffffu, mbar_wait(BAR(BAR_PV_DONE + x), sx & 1, abort_flag, p.status))) break;
+            ++sx;
             const bool merge_slots = !pair && n > 1;  // slot 1 holds the odd KV tiles of the same rows
             if (merge_slots && x == 1) {
                 // hand the row's (max, sum) to slot 0, which reads O_1 from TMEM itself
@@ -672,78 +721,85 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                 !__all_sync(0xffffffffu, mbar_wait(BAR(BAR_ML_FULL), n_merge & 1, abort_flag, p.status)))
                 break;
             tc_fence_after();
-            uint32_t o[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + col_o + c * 32, o[c]);
-            tmem_ld_wait(o[0]);
-            reg_order(o[1]);
-            reg_order(o[2]);
-            reg_order(o[3]);
+            // O = (O_0 a0 + O_1 a1) / (l_0 a0 + l_1 a1) when slot 1 holds the odd KV tiles of the
+            // same rows (a0, a1 move both halves to the larger max); else O = O_x / l
+            float a0 = 1.f, a1 = 0.f;
             if (merge_slots) {
-                // O = (O_0 a + O_1 b) / (l_0 a + l_1 b) with a, b moving both to the larger max
                 const float m1 = sh_m[row], l1 = sh_l[row];
                 const float mm = fmaxf(m_run, m1);
-                const float a0 = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - mm);
-                const float a1 = (m1 == -INFINITY) ? 0.f : ex2_approx(m1 - mm);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                a0 = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - mm);
+                a1 = (m1 == -INFINITY) ? 0.f : ex2_approx(m1 - mm);
+                l_run = l_run * a0 + l1 * a1;
+                m_run = (mm == -INFINITY) ? m_run : mm;
+            }
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            const float lse_nat = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+            const float w0 = a0 * inv, w1 = a1 * inv;
+            const int h = sg.g * p.G + hg;
+            const size_t orow = ((size_t)sg.b * p.B + i) * p.Hq + h;
+            const bool whole = sg.j0 == 0 && sg.j1 == sg.n_row;  // else a piece cut between CTAs
+            // A piece is parked for the merge kernel chunk-major: float4 chunk k of row r at
+            // [slot][k][r], so a warp's 32 rows store 512 contiguous bytes per instruction.
+            const size_t slot = (2 * (size_t)blockIdx.x + (seg_i == 0 ? 0 : 1)) * 2 + x;
+            uint4 *dst_o = reinterpret_cast<uint4 *>(p.o + orow * kHeadDim);
+            float4 *dst_w = reinterpret_cast<float4 *>(p.ws_o) + slot * (kHeadDim / 4) * kM + row;
+            // 32 columns at a time: TMEM -> registers -> global
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t o[32];
+                tmem_ld32(lane_addr + col_o + c * 32, o);
+                tmem_ld_wait(o);
+                if (merge_slots) {
                     uint32_t o1[32];
                     tmem_ld32(lane_addr + tmem_o(1) + c * 32, o1);
                     tmem_ld_wait(o1);
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
-                        o[c][e] = __float_as_uint(fmaf(__uint_as_float(o[c][e]), a0, __uint_as_float(o1[e]) * a1));
+                        o[e] = __float_as_uint(fmaf(__uint_as_float(o[e]), w0, __uint_as_float(o1[e]) * w1));
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * w0);
                 }
-                l_run = l_run * a0 + l1 * a1;
-                m_run = (mm == -INFINITY) ? m_run : mm;
+                if (!valid) continue;
+                if (whole) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 v;
+                        v.x = pack_bf16x2(__uint_as_float(o[q * 8 + 0]), __uint_as_float(o[q * 8 + 1]));
+                        v.y = pack_bf16x2(__uint_as_float(o[q * 8 + 2]), __uint_as_float(o[q * 8 + 3]));
+                        v.z = pack_bf16x2(__uint_as_float(o[q * 8 + 4]), __uint_as_float(o[q * 8 + 5]));
+                        v.w = pack_bf16x2(__uint_as_float(o[q * 8 + 6]), __uint_as_float(o[q * 8 + 7]));
+                        dst_o[c * 4 + q] = v;
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        dst_w[(size_t)(c * 8 + q) * kM] =
+                            make_float4(__uint_as_float(o[q * 4 + 0]), __uint_as_float(o[q * 4 + 1]),
+                                        __uint_as_float(o[q * 4 + 2]), __uint_as_float(o[q * 4 + 3]));
+                }
+            }
+            if (merge_slots) {
                 tc_fence_before();
                 mbar_arrive(BAR(BAR_ML_READ));
                 ++n_merge;
             }
             tc_fence_before();
             mbar_arrive(BAR(BAR_O_EMPTY + x));
-
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-            const float lse_nat = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
-            const int h = sg.g * p.G + hg;
-            const size_t orow = ((size_t)sg.b * p.B + i) * p.Hq + h;
-            uint4 *dst_o = reinterpret_cast<uint4 *>(p.o + orow * kHeadDim);
-            if (sg.j0 == 0 && sg.j1 == sg.n_row) {
-                if (valid) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint4 v;
-                            v.x = pack_bf16x2(__uint_as_float(o[c][q * 8 + 0]) * inv, __uint_as_float(o[c][q * 8 + 1]) * inv);
-                            v.y = pack_bf16x2(__uint_as_float(o[c][q * 8 + 2]) * inv, __uint_as_float(o[c][q * 8 + 3]) * inv);
-                            v.z = pack_bf16x2(__uint_as_float(o[c][q * 8 + 4]) * inv, __uint_as_float(o[c][q * 8 + 5]) * inv);
-                            v.w = pack_bf16x2(__uint_as_float(o[c][q * 8 + 6]) * inv, __uint_as_float(o[c][q * 8 + 7]) * inv);
-                            dst_o[c * 4 + q] = v;
-                        }
-                    }
+            if (valid) {
+                if (whole)
                     p.lse[orow] = lse_nat;
-                }
-            } else if (valid) {
-                // A piece of a pair tile cut between CTAs: park it for the merge kernel.
-                // Chunk-major: float4 chunk k of row r at [slot][k][r], so a warp's 32 rows
-                // store 512 contiguous bytes per instruction.
-                const size_t slot = (2 * (size_t)blockIdx.x + (seg_i == 0 ? 0 : 1)) * 2 + x;
-                float4 *dst = reinterpret_cast<float4 *>(p.ws_o) + slot * (kHeadDim / 4) * kM + row;
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        dst[(size_t)(c * 8 + q) * kM] = make_float4(
-                            __uint_as_float(o[c][q * 4 + 0]) * inv, __uint_as_float(o[c][q * 4 + 1]) * inv,
-                            __uint_as_float(o[c][q * 4 + 2]) * inv, __uint_as_float(o[c][q * 4 + 3]) * inv);
-                p.ws_lse[slot * kM + row] = lse_nat;
+                else
+                    p.ws_lse[slot * kM + row] = lse_nat;
             }
             gx += nx;
             ++seg_i;
         }
     }
 
+    // no thread exits before the previous kernel has completed, so kernels after this
+    // one (which wait only for it) also see that kernel's results
+    pdl_wait_primary();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -764,7 +820,7 @@ __device__ long long sched_prefix(const Sched &s, int b_end, int lane)
     long long tot = 0;
     for (int base = 0; base < b_end; base += 32) {
         const int b = base + lane;
-        const long long t = (b < b_end) ? (long long)s.Hkv * head_tiles(s, __ldg(s.prefix_lens + b)) : 0;
+        const long long t = (b < b_end) ? (long long)s.Hkv * head_tiles(s, __ldcg(s.prefix_lens + b)) : 0;
         tot += warp_sum_ll(t);
     }
     return tot;
@@ -804,7 +860,7 @@ __global__ void __launch_bounds__(kMergeThreads) tree_attn_merge_kernel(const Me
         const long long total = sched_total(sch, lane);
         const long long C = active_ctas(total, mp.attn_grid);
         const long long start_b = sched_prefix(sch, b, lane);
-        const int P = __ldg(mp.prefix_lens + b);
+        const int P = __ldcg(mp.prefix_lens + b);
         const int ht = head_tiles(sch, P);
         int c0 = 0, c1 = 0, first0 = 0;
         if (ht > 0 && total > 0) {

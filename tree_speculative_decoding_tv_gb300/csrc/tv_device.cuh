@@ -270,7 +270,26 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
+// Stores a[0..15] then b[0..15] as 32 consecutive columns (32 lanes x 32 columns).
+__device__ __forceinline__ void tmem_st16x2(uint32_t taddr, const uint32_t (&a)[32], const uint32_t (&b)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        TV_I8(a, 0), TV_I8(a, 8), TV_I8(b, 0), TV_I8(b, 8)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// max of three floats (a NaN operand is ignored, like fmaxf)
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
 
 __device__ __forceinline__ float ex2_approx(float x)
 {
