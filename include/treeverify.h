@@ -25,8 +25,9 @@
  *     device; the caller allocates and owns every buffer (workspaces
  *     included).  The library allocates no device memory, keeps no pointer
  *     after a call returns and encodes TMA descriptors on every call; its only
- *     host state is a per-device SM-count cache and the attention's ticket
- *     epoch counter.
+ *     host state is per-device: the SM count, the attention kernel's
+ *     shared-memory opt-in and the device address of tv_accept_noalloc's
+ *     scratch array.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Every call only enqueues work on `stream` and returns; results
  *     are ready when the stream reaches that point.
@@ -129,13 +130,21 @@ typedef struct tv_attn_args {
  * arguments are invalid. */
 TV_API size_t tv_attn_workspace_size(const tv_attn_args *args);
 
-/* Enqueue the attention (one kernel launch).  workspace_d: device buffer of at
- * least tv_attn_workspace_size(args) bytes, 16-byte aligned, contents ignored
- * on entry.  It holds split-KV partial results and the per-row-tile tickets
- * whose last holder merges them; concurrent calls need separate workspaces.
- * The library keeps one process-wide counter that gives every call a distinct
- * ticket epoch, so tickets left by an earlier or interrupted call are never
- * counted again.
+/* Enqueue the attention: two kernel launches on `stream`, the attention and a
+ * merge of split-KV pieces.  workspace_d: device buffer of at least
+ * tv_attn_workspace_size(args) bytes, 16-byte aligned, contents ignored on
+ * entry; it holds the normalised partial outputs (fp16) and LSEs (fp32) of row
+ * tiles whose key range was split between CTAs, written by the attention and
+ * read by the merge, so concurrent calls need separate workspaces.
+ *
+ * Ordering: the attention kernel is launched as a programmatic dependent of the
+ * previous kernel on the stream and reads q, the caches, block_table and
+ * prefix_lens before waiting for that kernel to finish (it waits only before
+ * reading mask_d).  So that previous kernel must not be one that writes those
+ * inputs after signalling its dependents early.  Kernels launched without
+ * programmatic dependent launch never signal early, and tv_build_mask (the
+ * natural predecessor) writes only the masks and depths.
+ *
  * Returns TV_OK, TV_ERR_INVALID_ARG, TV_ERR_UNSUPPORTED_SHAPE or TV_ERR_CUDA.
  * nb == 0 is a no-op. */
 TV_API int32_t tv_attn(const tv_attn_args *args, void *workspace_d, size_t workspace_bytes, void *stream);
@@ -159,9 +168,9 @@ TV_API int32_t tv_attn(const tv_attn_args *args, void *workspace_d, size_t works
  *   argmax_d       int32 [nb*B] (out), n_acc_d int32 [nb], path_d int32 [nb][B],
  *   bonus_d        int32 [nb] (out)
  *   workspace_d    device buffer of at least tv_accept_workspace_size(V, B, nb)
- *                  bytes (8 per logits row), 8-byte aligned, contents ignored on
- *                  entry (the call zeroes it and combines per-chunk argmax results
- *                  there, so concurrent calls need separate workspaces)
+ *                  bytes (one 8-byte argmax key per logits row), 8-byte aligned,
+ *                  contents ignored on entry (the call writes every key before
+ *                  reading it; concurrent calls need separate workspaces)
  * Returns TV_OK, TV_ERR_INVALID_ARG, TV_ERR_UNSUPPORTED_SHAPE or TV_ERR_CUDA.
  * A parent array that is not topological is reported through dev_status_d.
  */
@@ -183,7 +192,8 @@ TV_API int32_t tv_accept(const uint16_t *logits_d, int32_t V, const int32_t *dra
  * serving runtimes that plan every device buffer at start-up and forbid
  * allocation on the decode path.  This entry point takes the same arguments as
  * tv_accept minus the workspace and computes the same results, with its scratch
- * (8 bytes per logits row) in a fixed array inside the library image.
+ * (8 bytes per logits row, 64 KB in all) in a fixed array inside the library
+ * image.
  *
  *   - Limit: nb * B <= TV_ACCEPT_NOALLOC_MAX_ROWS; larger calls return
  *     TV_ERR_UNSUPPORTED_SHAPE and enqueue nothing.
@@ -193,7 +203,7 @@ TV_API int32_t tv_accept(const uint16_t *logits_d, int32_t V, const int32_t *dra
  *     device current) and caches it; make that first call before any stream
  *     capture.
  *   - Every call on a device shares the array and leaves its last contents
- *     there; each call zeroes the part it uses before use.  Calls whose work
+ *     there; each call writes every part it reads before reading it.  Calls whose work
  *     overlaps on the GPU (different streams, no ordering between them) race on
  *     the array and their results are undefined: order them on one stream.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.

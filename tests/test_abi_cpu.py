@@ -104,7 +104,9 @@ def test_accept_argument_checks(L):
     assert call(logits=P(FAKE + 1)) == 1
     assert call(draft=P(FAKE + 2)) == 1
     assert call(ws=None) == 1 and call(ws_bytes=8) == 1 and call(ws=P(FAKE + 4)) == 1
+    # one 8-byte argmax key per logits row, whatever V
     assert L.tv_accept_workspace_size(151936, 256, 1) == 256 * 8
+    assert L.tv_accept_workspace_size(4096, 16, 2) == 32 * 8
     assert L.tv_accept_workspace_size(0, 16, 1) == 0 and L.tv_accept_workspace_size(10, 300, 1) == 0
 
 

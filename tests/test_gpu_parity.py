@@ -63,7 +63,7 @@ def test_mask_reports_non_topological_parent():
 
 # ------------------------------------------------------------- a4 + a5 accept
 
-@pytest.mark.parametrize("B,V", [(1, 7), (7, 3), (16, 4096), (33, 1001), (64, 5), (256, 4099)])
+@pytest.mark.parametrize("B,V", [(1, 7), (7, 3), (16, 4096), (33, 1001), (64, 5), (256, 4099), (3, 300001)])
 def test_accept_bit_exact(B, V):
     rng = np.random.default_rng(B * 1000 + V)
     nb = 6
@@ -85,8 +85,8 @@ def test_accept_bit_exact(B, V):
 
 @pytest.mark.parametrize("V", [1003, 2048, 4104])
 def test_argmax_edge_values(V):
-    # ties, signed zeros, NaNs, infinities; V = 1003 leaves rows unaligned (warp-unit kernel),
-    # V = 2048 and 4104 take the bulk-copy streaming kernel with slices straddling rows
+    # ties, signed zeros, NaNs, infinities; V = 1003 leaves rows unaligned, V = 4104 splits each
+    # row over two chunks whose keys the acceptance kernel combines
     rows = np.full((6, V), 0xBF80, dtype=np.uint16)            # -1.0 everywhere
     rows[0, [5, 700]] = 0x4000                                   # tie between 5 and 700 -> 5
     rows[1, :] = 0x8000

@@ -7,16 +7,19 @@
 // node wins, ties to the smallest index.
 //
 // argmax (kernel 1): the logits are cut into (row, 4096-element chunk) units,
-// one warp per unit, and a one-wave grid walks them, so every SM streams the
-// same number of bytes whatever the row count.  A lane holds 16 16-byte vectors
+// one warp per unit, and a grid of at most two CTAs per SM walks them row group
+// by row group.  A lane holds 16 16-byte vectors
 // of its unit in registers (all in flight at once); bf16x2 NaN-propagating max
 // instructions reduce them (about one per two logits), the warp agrees on the
 // unit's maximum with shuffles, and only the lanes holding it look for its
 // first position.
 //
-// The units of a row meet through one 64-bit atomicMax per unit on an
-// order-preserving key (value rank, then the smaller index) in the caller's
-// workspace, zeroed at the start of every call.
+// A CTA owns whole rows: R = max(1, 8 / chunks per row) rows at a time, whose
+// (row, chunk) units its 8 warps share out; each warp folds a unit into a 64-bit
+// order-preserving key (value rank, then the smaller index) and takes the maximum
+// into the row's shared-memory slot, and the CTA stores one key per row in the
+// caller's workspace.  Every key is written by exactly one CTA before the
+// acceptance kernel reads it, so no global atomics and no zeroing are needed.
 //
 // accept (kernel 2): one CTA per sequence, one thread per node, launched as a
 // programmatic dependent of the argmax.  The tree inputs (parent, draft, the
@@ -108,21 +111,26 @@ __device__ __forceinline__ __nv_bfloat162 vec_max2(const uint4 &v)
 // it find their first position in two steps (first vector whose maximum
 // matches, then the element inside it), and one integer min-reduction picks the
 // smallest.  No block-level synchronisation; 32-bit index arithmetic.
-__global__ void __launch_bounds__(kArgThreads) argmax_partial_kernel(const uint16_t *__restrict__ logits, int V,
-                                                                     int nchunk, int units,
-                                                                     unsigned long long *__restrict__ best)
+__global__ void __launch_bounds__(kArgThreads) argmax_rows_kernel(const uint16_t *__restrict__ logits, int V,
+                                                                  int nchunk, int R, int rows,
+                                                                  unsigned long long *__restrict__ best)
 {
+    __shared__ unsigned long long s_key[kArgThreads / 32];  // R <= 8 rows per group
     static_assert(kArgChunk == 32 * kArgVec * 8, "one warp per unit");
     static_assert(kArgVec == 16, "the dependency points below list 16 vectors");
-    const int lane = threadIdx.x & 31;
-    const int warps = gridDim.x * (kArgThreads / 32);
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const float NEG_INF = -__int_as_float(0x7f800000);
-    pdl_wait_primary();  // logits and the zeroed keys come from earlier work in the stream
+    pdl_wait_primary();  // the logits may come from the previous kernel in the stream
     pdl_launch_dependents();
 
-    for (int u = blockIdx.x * (kArgThreads / 32) + (threadIdx.x >> 5); u < units; u += warps) {
-        const int row_id = u / nchunk;
-        const int lo = (u - row_id * nchunk) * kArgChunk;
+    for (int r0 = blockIdx.x * R; r0 < rows; r0 += gridDim.x * R) {
+      const int nr = min(R, rows - r0);
+      if (threadIdx.x < kArgThreads / 32) s_key[threadIdx.x] = 0ull;  // below every real key
+      __syncthreads();
+      for (int u = wid; u < nr * nchunk; u += kArgThreads / 32) {
+        const int lr = u / nchunk;
+        const int row_id = r0 + lr;
+        const int lo = (u - lr * nchunk) * kArgChunk;
         const int hi = min(lo + kArgChunk, V);
         const uint16_t *row = logits + (size_t)row_id * V;
 
@@ -203,7 +211,11 @@ __global__ void __launch_bounds__(kArgThreads) argmax_partial_kernel(const uint1
             }
         }
         idx = __reduce_min_sync(0xffffffffu, idx);
-        if (lane == 0) atomicMax(best + row_id, ((unsigned long long)wr << 32) | (0xFFFFFFFFu - idx));
+        if (lane == 0) atomicMax(&s_key[lr], ((unsigned long long)wr << 32) | (0xFFFFFFFFu - idx));
+      }
+      __syncthreads();
+      if (threadIdx.x < nr) best[r0 + threadIdx.x] = s_key[threadIdx.x];
+      __syncthreads();  // s_key is reset for the next group only after it was read
     }
 }
 
@@ -245,7 +257,8 @@ __global__ void __launch_bounds__(kMaxB) accept_kernel(const unsigned long long 
 
     // every row's argmax is the low half of its key: 0xFFFFFFFF - index
     if (i < B) {
-        const int a = (int)(0xFFFFFFFFu - (uint32_t)__ldcg(best + (size_t)b * B + i));
+        const unsigned long long top = __ldcg(best + (size_t)b * B + i);
+        const int a = (int)(0xFFFFFFFFu - (uint32_t)top);
         s_am[i] = a;
         am[(size_t)b * B + i] = a;
     }
@@ -312,21 +325,22 @@ cudaError_t launch_accept(const uint16_t *logits, int V, const int32_t *draft, c
                           int32_t *bonus, int32_t *status, void *workspace, int num_sms, cudaStream_t stream)
 {
     const int nchunk = (V + kArgChunk - 1) / kArgChunk;
-    const int units = nb * B * nchunk;
+    const int rows = nb * B;
+    const int wpc = kArgThreads / 32;
+    const int R = nchunk >= wpc ? 1 : wpc / nchunk;  // rows per CTA group
     long long grid = (long long)num_sms * kArgCtasPerSm;
-    const long long need = ((long long)units + kArgThreads / 32 - 1) / (kArgThreads / 32);
+    const long long need = ((long long)rows + R - 1) / R;
     if (grid > need) grid = need;
     if (grid < 1) grid = 1;
     unsigned long long *best = static_cast<unsigned long long *>(workspace);
-    cudaError_t e = cudaMemsetAsync(best, 0, accept_workspace_bytes(V, B, nb), stream);
-    if (e != cudaSuccess) return e;
-    e = launch_dependent(argmax_partial_kernel, dim3((unsigned)grid), dim3(kArgThreads), 0, stream, logits, V, nchunk,
-                         units, best);
+    cudaError_t e = launch_dependent(argmax_rows_kernel, dim3((unsigned)grid), dim3(kArgThreads), 0, stream, logits,
+                                     V, nchunk, R, rows, best);
     if (e != cudaSuccess) return e;
     const int W = (B + 31) / 32;
     // its launch overlaps the argmax tail; it waits before reading the keys
     return launch_dependent(accept_kernel, dim3((unsigned)nb), dim3(kMaxB), 0, stream,
-                            (const unsigned long long *)best, draft, parent, mask, B, W, am, n_acc, path, bonus, status);
+                            (const unsigned long long *)best, draft, parent, mask, B, W, am, n_acc, path, bonus,
+                            status);
 }
 
 // ------------------------------------------------------ allocation-free variant
@@ -366,7 +380,7 @@ cudaError_t launch_accept_noalloc(const uint16_t *logits, int V, const int32_t *
     void *keys = nullptr;
     const cudaError_t e = noalloc_keys_address(&keys);
     if (e != cudaSuccess) return e;
-    // the same kernels as tv_accept; their call zeroes the keys before use
+    // the same kernels as tv_accept; every key a call reads is written by that call first
     return launch_accept(logits, V, draft, parent, mask, B, nb, am, n_acc, path, bonus, status, keys, num_sms, stream);
 }
 

@@ -114,7 +114,7 @@ struct AttnParams {
     uint16_t *o;
     float *lse;
     int32_t *status;
-    float *ws_o;    // [2 * grid][2 tiles][32 chunks][128 rows][4] fp32 partial O (normalised)
+    uint4 *ws_o;    // [2 * grid][2 tiles][16 chunks][128 rows] x 8 fp16: partial O (normalised)
     float *ws_lse;  // [2 * grid][2 tiles][128]
     int nb, B, Hq, Hkv, G, NT, MT, W, max_pages, num_blocks;
     float scale_log2;
@@ -738,11 +738,12 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
             const int h = sg.g * p.G + hg;
             const size_t orow = ((size_t)sg.b * p.B + i) * p.Hq + h;
             const bool whole = sg.j0 == 0 && sg.j1 == sg.n_row;  // else a piece cut between CTAs
-            // A piece is parked for the merge kernel chunk-major: float4 chunk k of row r at
-            // [slot][k][r], so a warp's 32 rows store 512 contiguous bytes per instruction.
+            // A piece is parked for the merge kernel in fp16 (it is normalised, |O| <= max|V|),
+            // chunk-major: 8-column chunk k of row r at [slot][k][r], so a warp's 32 rows
+            // store 512 contiguous bytes per instruction.
             const size_t slot = (2 * (size_t)blockIdx.x + (seg_i == 0 ? 0 : 1)) * 2 + x;
             uint4 *dst_o = reinterpret_cast<uint4 *>(p.o + orow * kHeadDim);
-            float4 *dst_w = reinterpret_cast<float4 *>(p.ws_o) + slot * (kHeadDim / 4) * kM + row;
+            uint4 *dst_w = p.ws_o + slot * (kHeadDim / 8) * kM + row;
             // 32 columns at a time: TMEM -> registers -> global
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
@@ -773,10 +774,14 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                     }
                 } else {
 #pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        dst_w[(size_t)(c * 8 + q) * kM] =
-                            make_float4(__uint_as_float(o[q * 4 + 0]), __uint_as_float(o[q * 4 + 1]),
-                                        __uint_as_float(o[q * 4 + 2]), __uint_as_float(o[q * 4 + 3]));
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 v;
+                        v.x = pack_f16x2(__uint_as_float(o[q * 8 + 0]), __uint_as_float(o[q * 8 + 1]));
+                        v.y = pack_f16x2(__uint_as_float(o[q * 8 + 2]), __uint_as_float(o[q * 8 + 3]));
+                        v.z = pack_f16x2(__uint_as_float(o[q * 8 + 4]), __uint_as_float(o[q * 8 + 5]));
+                        v.w = pack_f16x2(__uint_as_float(o[q * 8 + 6]), __uint_as_float(o[q * 8 + 7]));
+                        dst_w[(size_t)(c * 4 + q) * kM] = v;
+                    }
                 }
             }
             if (merge_slots) {
@@ -828,7 +833,7 @@ __device__ long long sched_prefix(const Sched &s, int b_end, int lane)
 
 struct MergeParams {
     const int32_t *prefix_lens;
-    const float *ws_o;
+    const uint4 *ws_o;
     const float *ws_lse;
     uint16_t *o;
     float *lse;
@@ -856,6 +861,7 @@ __global__ void __launch_bounds__(kMergeThreads) tree_attn_merge_kernel(const Me
     const int lane = threadIdx.x & 31, q = threadIdx.x >> 5;
     const Sched sch{mp.prefix_lens, mp.nb, mp.B, mp.Hkv, mp.NT, mp.MT, mp.max_pages * kPage};
 
+    pdl_launch_dependents();  // the next kernel (its own wait keeps it ordered) may start launching
     if (q == 0) {  // prefix_lens is an input of both kernels: safe to read before the dependency wait
         const long long total = sched_total(sch, lane);
         const long long C = active_ctas(total, mp.attn_grid);
@@ -896,16 +902,16 @@ __global__ void __launch_bounds__(kMergeThreads) tree_attn_merge_kernel(const Me
     for (int k = 0; k < 8; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int cb = c0; cb <= c1; cb += 4) {
         float l[4];
-        float4 v[4][8];
+        uint4 v[4][4];  // 8 fp16 columns each: this thread's 32 columns of 4 pieces
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int c = cb + u;
             const bool in = c <= c1;
             const size_t slot = slot_of(in ? c : c0);
             l[u] = in ? __ldcg(mp.ws_lse + slot * kM + r) : -INFINITY;
-            const float4 *src = reinterpret_cast<const float4 *>(mp.ws_o) + (slot * 32 + q * 8) * kM + r;
+            const uint4 *src = mp.ws_o + (slot * (kHeadDim / 8) + q * 4) * kM + r;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) v[u][k] = in ? __ldcg(src + (size_t)k * kM) : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int k = 0; k < 4; ++k) v[u][k] = in ? __ldcg(src + (size_t)k * kM) : make_uint4(0u, 0u, 0u, 0u);
         }
         const float mb = fmaxf(fmaxf(m, fmaxf(l[0], l[1])), fmaxf(l[2], l[3]));
         if (mb == -INFINITY) continue;  // no piece with a visible key yet
@@ -923,11 +929,17 @@ __global__ void __launch_bounds__(kMergeThreads) tree_attn_merge_kernel(const Me
             const float w = expf(l[u] - mb);  // 0 for an empty piece
             wsum += w;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                acc[k].x = fmaf(w, v[u][k].x, acc[k].x);
-                acc[k].y = fmaf(w, v[u][k].y, acc[k].y);
-                acc[k].z = fmaf(w, v[u][k].z, acc[k].z);
-                acc[k].w = fmaf(w, v[u][k].w, acc[k].w);
+            for (int k = 0; k < 4; ++k) {
+                const float2 a = unpack_f16x2(v[u][k].x), b = unpack_f16x2(v[u][k].y);
+                const float2 c = unpack_f16x2(v[u][k].z), d = unpack_f16x2(v[u][k].w);
+                acc[2 * k].x = fmaf(w, a.x, acc[2 * k].x);
+                acc[2 * k].y = fmaf(w, a.y, acc[2 * k].y);
+                acc[2 * k].z = fmaf(w, b.x, acc[2 * k].z);
+                acc[2 * k].w = fmaf(w, b.y, acc[2 * k].w);
+                acc[2 * k + 1].x = fmaf(w, c.x, acc[2 * k + 1].x);
+                acc[2 * k + 1].y = fmaf(w, c.y, acc[2 * k + 1].y);
+                acc[2 * k + 1].z = fmaf(w, d.x, acc[2 * k + 1].z);
+                acc[2 * k + 1].w = fmaf(w, d.y, acc[2 * k + 1].w);
             }
         }
         m = mb;
@@ -977,7 +989,7 @@ static EncodeTiledFn encode_fn()
 size_t attn_workspace_bytes(int ctas, int row_tiles)
 {
     (void)row_tiles;
-    return (size_t)4 * ctas * kM * (kHeadDim + 1) * sizeof(float);
+    return (size_t)4 * ctas * kM * (kHeadDim * 2 + sizeof(float));  // fp16 O + fp32 LSE per row
 }
 
 int attn_row_tiles(const tv_attn_args *a)
@@ -1047,8 +1059,8 @@ int32_t launch_attn(const tv_attn_args *a, int ctas, void *workspace, cudaStream
     p.o = static_cast<uint16_t *>(a->o_d);
     p.lse = a->lse_d;
     p.status = a->dev_status_d;
-    p.ws_o = static_cast<float *>(workspace);
-    p.ws_lse = p.ws_o + (size_t)4 * ctas * kM * kHeadDim;
+    p.ws_o = static_cast<uint4 *>(workspace);
+    p.ws_lse = reinterpret_cast<float *>(p.ws_o + (size_t)4 * ctas * kM * (kHeadDim / 8));
     p.nb = a->nb;
     p.B = a->B;
     p.Hq = a->Hq;
