@@ -657,21 +657,23 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                 const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
 
                 // P = exp2(s * scale * log2 e - m) as bf16 pairs, packed in place (pair e of
-                // block c lands in s[c][e], e < 16) and stored over the first 64 columns of S
+                // block c lands in s[c][e], e < 16) and stored over the first 64 columns of S.
+                // The scale and the row sum use packed f32x2 math: these warps share each SM
+                // sub-partition with the MMA and TMA warps, and every issue slot they leave free
+                // lets those keep the tensor pipe and the K/V ring fed.
                 float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
 #pragma unroll
                     for (int e2 = 0; e2 < 16; ++e2) {
-                        const float a = ex2_approx(fmaf(__uint_as_float(s[c][2 * e2]), sl2, neg_m));
-                        const float b = ex2_approx(fmaf(__uint_as_float(s[c][2 * e2 + 1]), sl2, neg_m));
-                        if (e2 & 1) {
-                            l2 += a;
-                            l3 += b;
-                        } else {
-                            l0 += a;
-                            l1 += b;
-                        }
+                        float a = __uint_as_float(s[c][2 * e2]), b = __uint_as_float(s[c][2 * e2 + 1]);
+                        ffma2(a, b, sl2, neg_m);
+                        a = ex2_approx(a);
+                        b = ex2_approx(b);
+                        if (e2 & 1)
+                            fadd2(l2, l3, a, b);
+                        else
+                            fadd2(l0, l1, a, b);
                         s[c][e2] = pack_bf16x2(a, b);
                     }
                     if (c & 1) tmem_st16x2(lane_addr + col_s + (c >> 1) * 32, s[c - 1], s[c]);
