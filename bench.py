@@ -143,7 +143,7 @@ class ClockSampler:
         reasons = sorted({names[k] for r in sel for k in range(4) if r[2][k].lower().startswith("active")})
         return {"sm_mhz": float(np.median([r[0] for r in sel])), "sm_max_mhz": max(r[1] for r in sel),
                 "reasons": reasons, "samples": len(sel),
-                "window": "a 0.4 s load window of the same steps plus the timed steps" if inside else "whole run"}
+                "window": "a load window of the same steps plus the timed steps" if inside else "whole run"}
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -256,9 +256,10 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         raise RuntimeError(f"device status {st.status.item()} during warm-up")
 
     # The timed steps last milliseconds, shorter than one nvidia-smi sample, so the clocks
-    # are sampled over a load window of the same steps (~0.4 s) that ends where they start.
+    # are sampled over a load window of the same steps (--clock-window seconds) that ends
+    # where they start.
     t_begin = time.time()
-    while time.time() - t_begin < 0.4:
+    while time.time() - t_begin < args.clock_window:
         for _ in range(20):
             flush.zero_()
             st.run()
@@ -444,6 +445,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--ref-heads", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-window", type=float, default=0.4,
+                    help="seconds of untimed steps, sampled for clocks, before the timed steps (0 under a profiler)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
