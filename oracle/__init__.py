@@ -11,6 +11,8 @@ Functions (numpy in, numpy out):
   lse_merge(O_parts, lse_parts)              -> (O, LSE)
   argmax(logits_bf16)                        -> int32 [rows]
   accept(logits, draft, parent)              -> (argmax, n_acc, path, bonus)
+  kv_commit(k_cache, v_cache, block_table, prefix_lens, n_acc, path)
+                                             -> (k_cache', v_cache', new prefix_lens)  (copies)
 Every pinned property of these functions is listed in ``tests/test_oracle_pins.py``.
 """
 from __future__ import annotations
@@ -55,7 +57,10 @@ def _load():
         lib.tvo_lse_merge.argtypes = [C.c_int, C.c_long, C.c_int, P, P, P, P]
         lib.tvo_argmax.argtypes = [P, C.c_long, C.c_long, P]
         lib.tvo_accept.argtypes = [P, C.c_long, P, P, C.c_int, C.c_int, P, P, P, P]
-        for f in (lib.tvo_build_mask, lib.tvo_attn, lib.tvo_lse_merge, lib.tvo_argmax, lib.tvo_accept):
+        lib.tvo_kv_commit.argtypes = [P, P, P, P, P, P, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
+                                      C.c_int, P]
+        for f in (lib.tvo_build_mask, lib.tvo_attn, lib.tvo_lse_merge, lib.tvo_argmax, lib.tvo_accept,
+                  lib.tvo_kv_commit):
             f.restype = C.c_int
         _lib = lib
     return _lib
@@ -158,3 +163,19 @@ def accept(logits, draft, parent):
     _check(_load().tvo_accept(_ptr(logits), V, _ptr(draft), _ptr(parent), B, nb, _ptr(am), _ptr(n_acc),
                               _ptr(path), _ptr(bonus)), "accept")
     return am, n_acc, path, bonus
+
+
+def kv_commit(k_cache, v_cache, block_table, prefix_lens, n_acc, path):
+    """Commit of the accepted branch on copies of the caches; returns (k, v, new prefix_lens)."""
+    k = np.array(k_cache, dtype=np.uint16, copy=True, order="C")
+    v = np.array(v_cache, dtype=np.uint16, copy=True, order="C")
+    block_table = _c(block_table, np.int32)
+    prefix_lens = _c(prefix_lens, np.int32).reshape(-1)
+    n_acc = _c(n_acc, np.int32).reshape(-1)
+    path = _c(path, np.int32)
+    nb, B = path.shape
+    num_blocks, Hkv, page, D = k.shape
+    new_pl = np.zeros(nb, dtype=np.int32)
+    _check(_load().tvo_kv_commit(_ptr(k), _ptr(v), _ptr(block_table), _ptr(prefix_lens), _ptr(n_acc), _ptr(path),
+                                 nb, B, Hkv, D, page, block_table.shape[1], num_blocks, _ptr(new_pl)), "kv_commit")
+    return k, v, new_pl

@@ -327,3 +327,64 @@ int tvo_accept(const uint16_t *logits, long V, const int32_t *draft, const int32
     free(acc); free(dep);
     return rc;
 }
+
+/* ------------------------------------------------------------ KV commit */
+
+/* Commit of the accepted branch (DFlash-TfM summary, §3 "Solución": the state is
+ * committed once the accepted branch is known, so nothing is rolled back).  For
+ * attention the state is the paged K/V cache.  Sequence b holds its committed
+ * tokens at logical positions [0, P) (P = prefix_lens[b]) and tree node t at
+ * P + t.  The commit keeps the root and the accepted nodes, in path order:
+ * afterwards position P + k holds what position P + path[b][k] held before, for
+ * k = 0 .. n_acc[b] (path[b][0] = 0, so the root stays), and the committed
+ * length becomes P + n_acc[b] + 1.  No other position changes.  All sources are
+ * read before any destination is written (a source may be another row's
+ * destination).  Logical position x of sequence b lives in physical page
+ * block_table[b][x / page], slot x % page; caches are [num_blocks][Hkv][page][D]. */
+int tvo_kv_commit(uint16_t *k_cache, uint16_t *v_cache, const int32_t *block_table, const int32_t *prefix_lens,
+                  const int32_t *n_acc, const int32_t *path, int nb, int B, int Hkv, int D, int page, int max_pages,
+                  int num_blocks, int32_t *new_prefix_lens)
+{
+    if (!k_cache || !v_cache || !block_table || !prefix_lens || !n_acc || !path || !new_prefix_lens) return TVO_ERR_ARG;
+    if (nb < 0 || B < 1 || Hkv < 1 || D < 1 || page < 1 || max_pages < 1 || num_blocks < 1) return TVO_ERR_ARG;
+    const size_t row = (size_t)D;                 /* elements of one (position, kv head) row */
+    uint16_t *tmp = malloc(sizeof(uint16_t) * 2 * (size_t)B * Hkv * row);
+    if (!tmp) return TVO_ERR_ARG;
+    int rc = TVO_OK;
+    for (int b = 0; b < nb && rc == TVO_OK; b++) {
+        const int P = prefix_lens[b], n = n_acc[b];
+        const int32_t *pr = path + (size_t)b * B;
+        const int32_t *bt = block_table + (size_t)b * max_pages;
+        if (P < 0 || n < 0 || n >= B || pr[0] != 0) { rc = TVO_ERR_ARG; break; }
+        for (int k = 1; k <= n; k++)
+            if (pr[k] <= pr[k - 1] || pr[k] >= B) rc = TVO_ERR_ARG;
+        if ((long)P + B > (long)max_pages * page) rc = TVO_ERR_ARG;
+        if (rc != TVO_OK) break;
+        /* read every source row first */
+        for (int k = 0; k <= n; k++) {
+            const long x = (long)P + pr[k];
+            const int blk = bt[x / page];
+            if (blk < 0 || blk >= num_blocks) { rc = TVO_ERR_ARG; break; }
+            for (int g = 0; g < Hkv; g++) {
+                const size_t src = (((size_t)blk * Hkv + g) * page + (size_t)(x % page)) * row;
+                memcpy(tmp + ((size_t)(2 * k) * Hkv + g) * row, k_cache + src, sizeof(uint16_t) * row);
+                memcpy(tmp + ((size_t)(2 * k + 1) * Hkv + g) * row, v_cache + src, sizeof(uint16_t) * row);
+            }
+        }
+        if (rc != TVO_OK) break;
+        /* then write position P + k */
+        for (int k = 0; k <= n; k++) {
+            const long x = (long)P + k;
+            const int blk = bt[x / page];
+            if (blk < 0 || blk >= num_blocks) { rc = TVO_ERR_ARG; break; }
+            for (int g = 0; g < Hkv; g++) {
+                const size_t dst = (((size_t)blk * Hkv + g) * page + (size_t)(x % page)) * row;
+                memcpy(k_cache + dst, tmp + ((size_t)(2 * k) * Hkv + g) * row, sizeof(uint16_t) * row);
+                memcpy(v_cache + dst, tmp + ((size_t)(2 * k + 1) * Hkv + g) * row, sizeof(uint16_t) * row);
+            }
+        }
+        new_prefix_lens[b] = P + n + 1;
+    }
+    free(tmp);
+    return rc;
+}

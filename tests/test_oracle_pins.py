@@ -382,3 +382,95 @@ def test_accept_closed_forms():
 def test_accept_rejects_non_topological():
     with pytest.raises(oracle.OracleError):
         oracle.accept(np.zeros((3, 4), np.uint16), np.zeros(3, np.int32), np.array([-1, 2, 0], np.int32))
+
+
+# ------------------------------------------------------------------ KV commit
+
+def _root_path(parent, v):
+    out = []
+    while v != -1:
+        out.append(int(v))
+        v = int(parent[v])
+    return out[::-1]
+
+
+def _commit_inputs(rng, parent):
+    """A random acceptance outcome: the root path of a random node, as tv_accept returns it."""
+    nb, B = parent.shape
+    n_acc = np.zeros(nb, np.int32)
+    path = np.full((nb, B), -1, np.int32)
+    for b in range(nb):
+        p = _root_path(parent[b], int(rng.integers(0, B)))
+        n_acc[b] = len(p) - 1
+        path[b, :len(p)] = p
+    return n_acc, path
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_kv_commit_keeps_what_each_accepted_node_attended_to(seed):
+    """Before the commit, node path[k] attends to the prefix and its root path path[0..k]
+    (JETFLOW §2 mask).  After it, those keys are exactly positions [0, P + k], so a chain
+    tree over the committed cache queried with the path nodes' queries gives the same rows:
+    the same keys in the same order, hence bit-identical fp64 results."""
+    rng = np.random.default_rng(100 + seed)
+    w = _small_workload(seed, nb=3, B=12, Hq=4, Hkv=2, D=16, prefix=[0, 5, 37])
+    n_acc, path = _commit_inputs(rng, w.parent)
+    O_tree, L_tree = oracle.attn_workload(w)
+    k2, v2, new_pl = oracle.kv_commit(w.k_cache, w.v_cache, w.block_table, w.prefix_lens, n_acc, path)
+    assert np.array_equal(new_pl, w.prefix_lens + n_acc + 1)
+    chain = np.tile(np.arange(-1, w.B - 1, dtype=np.int32), (w.nb, 1))
+    q_chain = np.zeros_like(w.q)
+    for b in range(w.nb):
+        for k in range(n_acc[b] + 1):
+            q_chain[b * w.B + k] = w.q[b * w.B + path[b, k]]
+    O_ch, L_ch = oracle.attn(q_chain, k2, v2, w.block_table, w.prefix_lens, chain, w.Hq, w.Hkv)
+    for b in range(w.nb):
+        for k in range(n_acc[b] + 1):
+            assert np.array_equal(O_ch[b * w.B + k], O_tree[b * w.B + path[b, k]])
+            assert np.array_equal(L_ch[b * w.B + k], L_tree[b * w.B + path[b, k]])
+
+
+def test_kv_commit_moves_only_the_accepted_rows():
+    rng = np.random.default_rng(7)
+    w = _small_workload(7, nb=4, B=20, Hq=4, Hkv=2, D=8, prefix=[3, 0, 16, 50])
+    n_acc, path = _commit_inputs(rng, w.parent)
+    k2, v2, new_pl = oracle.kv_commit(w.k_cache, w.v_cache, w.block_table, w.prefix_lens, n_acc, path)
+    w2 = wl.Workload(**{**w.__dict__, "k_cache": k2, "v_cache": v2})
+    for b in range(w.nb):
+        P, n = int(w.prefix_lens[b]), int(n_acc[b])
+        for which in ("k", "v"):
+            before, after = wl.logical_kv(w, b, which), wl.logical_kv(w2, b, which)
+            assert np.array_equal(after[:P + 1], before[:P + 1])              # prefix and root
+            assert np.array_equal(after[P + n + 1:], before[P + n + 1:])      # everything past the path
+            for k in range(1, n + 1):
+                assert np.array_equal(after[P + k], before[P + path[b, k]])
+    # physical pages no block table points at are untouched
+    used = set(int(x) for x in w.block_table.reshape(-1) if x >= 0)
+    for blk in range(w.num_blocks):
+        if blk not in used:
+            assert np.array_equal(k2[blk], w.k_cache[blk]) and np.array_equal(v2[blk], w.v_cache[blk])
+
+
+def test_kv_commit_closed_forms():
+    w = _small_workload(8, nb=2, B=9, Hq=2, Hkv=1, D=8, prefix=[4, 30],
+                        trees=[np.arange(-1, 8, dtype=np.int32)] * 2)
+    # nothing accepted: only the root is committed, no row moves
+    path = np.full((2, 9), -1, np.int32)
+    path[:, 0] = 0
+    k2, v2, pl = oracle.kv_commit(w.k_cache, w.v_cache, w.block_table, w.prefix_lens, np.zeros(2, np.int32), path)
+    assert np.array_equal(k2, w.k_cache) and np.array_equal(v2, w.v_cache)
+    assert pl.tolist() == [5, 31]
+    # a chain accepted in full is already in place
+    full = np.tile(np.arange(9, dtype=np.int32), (2, 1))
+    k2, v2, pl = oracle.kv_commit(w.k_cache, w.v_cache, w.block_table, w.prefix_lens, np.full(2, 8, np.int32), full)
+    assert np.array_equal(k2, w.k_cache) and np.array_equal(v2, w.v_cache)
+    assert pl.tolist() == [13, 39]
+
+
+@pytest.mark.parametrize("bad", [[0, 2, 2], [1, 2, 3], [0, 5, 3], [0, 1, 9]])
+def test_kv_commit_rejects_a_path_that_is_not_a_root_path(bad):
+    w = _small_workload(9, nb=1, B=9, Hq=2, Hkv=1, D=8, prefix=[4])
+    path = np.full((1, 9), -1, np.int32)
+    path[0, :3] = bad
+    with pytest.raises(oracle.OracleError):
+        oracle.kv_commit(w.k_cache, w.v_cache, w.block_table, w.prefix_lens, np.array([2], np.int32), path)
