@@ -224,6 +224,29 @@ class Step:
         if ev is not None:
             ev[1].record()
 
+    def time_commit(self, flush, steps):
+        """Mean ms of tv_kv_commit (commit of the accepted branch found by the step) replayed from
+        its own graph with the same flush, and the bytes it moves.  Run last: it rewrites the
+        caches' tree positions."""
+        torch, tv = self.torch, self.tv
+        n_acc, path = self.acc_out[1], self.acc_out[2]
+        self.new_pl = torch.empty_like(self.pl)
+        kv = (self.k.view(torch.int16), self.v.view(torch.int16))
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            tv.kv_commit(*kv, self.bt, self.pl, n_acc, path, new_prefix_lens=self.new_pl, status=self.status)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            tv.kv_commit(*kv, self.bt, self.pl, n_acc, path, new_prefix_lens=self.new_pl, status=self.status)
+        ms = self.time_stage(g, flush, steps)
+        # rows that move (path[k] != k), K and V, read and written
+        nacc, pth = n_acc.cpu().numpy(), path.cpu().numpy()
+        moved = sum(int(np.sum(pth[b, 1:nacc[b] + 1] != np.arange(1, nacc[b] + 1))) for b in range(self.w.nb))
+        return ms, moved * self.w.Hkv * 2 * self.w.D * 2 * 2
+
     def time_stage(self, graph, flush, steps):
         """Mean ms of one stage graph replay, L2 flushed before each (CUDA events, current stream)."""
         torch = self.torch
@@ -355,6 +378,9 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     e2e_ms = e0.elapsed_time(e1)
     if any(x.status.item() != 0 for x in sets):
         raise RuntimeError("device status set in the end-to-end run")
+    commit_ms, commit_bytes = st.time_commit(flush, args.steps)
+    if st.status.item() != 0:
+        raise RuntimeError(f"device status {st.status.item()} in the commit stage")
     if world > 1:
         t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -400,6 +426,9 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
             "stage_timing": "each stage's own graph replayed K times with the same L2 flush, after the timed steps",
             "attention_nodes_per_s": nodes / t_attn, "attention_roofline": attn_roof, "accept_roofline": acc_roof,
             "attention_bytes": ab, "attention_flops": af, "accept_bytes": lb,
+            "kv_commit_ms": commit_ms, "kv_commit_bytes": commit_bytes,
+            "kv_commit_note": "tv_kv_commit of the accepted branch, its own graph after the timed steps; not part "
+                              "of the step (it rewrites the caches); latency-bound (a few KB moved)",
         },
         "clocks": clocks,
         "gpu_launches": st.launches_per_step * args.steps,

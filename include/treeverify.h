@@ -182,6 +182,36 @@ TV_API int32_t tv_accept(const uint16_t *logits_d, int32_t V, const int32_t *dra
                          int32_t *dev_status_d, void *workspace_d, size_t workspace_bytes, void *stream);
 
 /*
+ * Commit of the accepted branch  [TfM-3] (the pages commit state once the
+ * accepted branch is known; for a paged K/V cache this library reads that as
+ * compaction in path order)
+ *
+ *   For sequence b with committed length P = prefix_lens[b] (tree node t at
+ *   position P + t, as tv_attn reads it): position P + k of both caches takes
+ *   what position P + path[b][k] held, for k = 1 .. n_acc[b] (the root stays at
+ *   P; all rows are read before any is written), and
+ *   new_prefix_lens[b] = P + n_acc[b] + 1.  No other position changes.
+ *
+ *   k_cache_d, v_cache_d   bf16 [num_blocks][Hkv][page_size][D] (in/out), 16-byte aligned
+ *   block_table_d          int32 [nb][max_pages]; must cover P + B positions
+ *   prefix_lens_d          int32 [nb]
+ *   n_acc_d, path_d        int32 [nb] and [nb][B] as tv_accept returns them
+ *   new_prefix_lens_d      int32 [nb] (out); must not be prefix_lens_d
+ *   Shapes as tv_attn: 1 <= B <= 256, D = 128, page_size = 16.
+ * Ordering: launched as a programmatic dependent of the previous kernel on the
+ * stream, it waits for that kernel to finish before reading anything, so it can
+ * directly follow tv_accept.
+ * Returns TV_OK, TV_ERR_INVALID_ARG, TV_ERR_UNSUPPORTED_SHAPE or TV_ERR_CUDA.
+ * A path that is not a root path of at most B nodes, an n_acc outside [0, B) or a
+ * touched position the block table does not cover writes TV_ERR_INVALID_ARG to
+ * dev_status_d and leaves that sequence uncommitted (new_prefix_lens_d[b] = P).
+ */
+TV_API int32_t tv_kv_commit(void *k_cache_d, void *v_cache_d, const int32_t *block_table_d,
+                            const int32_t *prefix_lens_d, const int32_t *n_acc_d, const int32_t *path_d,
+                            int32_t nb, int32_t B, int32_t Hkv, int32_t D, int32_t page_size, int32_t num_blocks,
+                            int32_t max_pages, int32_t *new_prefix_lens_d, int32_t *dev_status_d, void *stream);
+
+/*
  * tv_accept_noalloc — tv_accept for callers that cannot allocate device memory.
  * (The pages have no counterpart: this is an integration aid, not part of the
  * method.)

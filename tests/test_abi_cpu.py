@@ -110,6 +110,25 @@ def test_accept_argument_checks(L):
     assert L.tv_accept_workspace_size(0, 16, 1) == 0 and L.tv_accept_workspace_size(10, 300, 1) == 0
 
 
+def test_kv_commit_argument_checks(L):
+    P = C.c_void_p
+    base = dict(k=P(FAKE), v=P(FAKE), bt=P(FAKE), pl=P(FAKE), n=P(FAKE), path=P(FAKE), nb=2, B=16, Hkv=8, D=128,
+                page=16, blocks=64, pages=8, out=P(FAKE + 4096))
+
+    def call(**kw):
+        d = dict(base)
+        d.update(kw)
+        return L.tv_kv_commit(d["k"], d["v"], d["bt"], d["pl"], d["n"], d["path"], d["nb"], d["B"], d["Hkv"], d["D"],
+                              d["page"], d["blocks"], d["pages"], d["out"], None, None)
+
+    assert call(nb=0) == 0                                    # nothing to do, nothing enqueued
+    assert call(nb=-1) == 1 and call(Hkv=0) == 1 and call(blocks=0) == 1
+    assert call(B=0) == 3 and call(B=257) == 3 and call(D=64) == 3 and call(page=32) == 3
+    assert call(k=None) == 1 and call(path=None) == 1 and call(out=None) == 1
+    assert call(out=P(FAKE)) == 1                             # new prefix lengths may not overwrite the old
+    assert call(k=P(FAKE + 8)) == 1 and call(n=P(FAKE + 2)) == 1
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "_lib", None)
     monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "missing.so"))

@@ -7,7 +7,9 @@ attention output is compared element by element on sampled (sequence, kv head) u
 each of which the fp64 oracle recomputes from a slice of the inputs (that unit's query
 heads and kv-head slice of the paged cache); every other row is checked for finiteness
 and for the LSE lower bound that holds at any size (a row sees at least one key, so
-LSE >= the largest scaled score, which is >= the score of the row's own tree key).
+LSE >= the largest scaled score, which is >= the score of the row's own tree key).  The
+commit of the accepted branch (tv_kv_commit) runs last, on the device's own acceptance
+outputs, and both whole caches are compared bit-exactly with the oracle's commit.
 """
 import numpy as np
 import pytest
@@ -67,6 +69,17 @@ def test_config_full_size(config):
         O_u = O_all[b, :, g * G:(g + 1) * G].reshape(w.B, G, w.D)
         L_u = L_all[b, :, g * G:(g + 1) * G].reshape(w.B, G)
         assert_attn_close(O_u, L_u, O_ref, L_ref, w)
+
+    # commit of the accepted branch, fed by the device's own acceptance: bit-exact caches and lengths
+    import tree_speculative_decoding_tv_gb300 as tv
+    new_pl = tv.kv_commit(d.k.view(torch.int16), d.v.view(torch.int16), d.bt, d.pl, n_acc, path, status=d.status)
+    torch.cuda.synchronize()
+    assert d.status.item() == 0
+    k_ref, v_ref, pl_ref = oracle.kv_commit(w.k_cache, w.v_cache, w.block_table, w.prefix_lens, r_n, r_path)
+    assert np.array_equal(new_pl.cpu().numpy(), pl_ref)
+    assert np.array_equal(d.k.view(torch.int16).cpu().numpy().view(np.uint16), k_ref)
+    assert np.array_equal(d.v.view(torch.int16).cpu().numpy().view(np.uint16), v_ref)
+    del k_ref, v_ref
 
     # any size: finite outputs, and LSE >= the scaled score of the row's own key (its tree slot)
     assert torch.isfinite(O).all() and torch.isfinite(L).all()

@@ -4,8 +4,8 @@ The product is libtreeverify.so (C ABI in include/treeverify.h, CUDA kernels
 for sm_103a in csrc/).  This package builds it (build.py) and exposes a thin
 ctypes binding (binding.py) that the tests and the benchmark call.
 """
-from .binding import (EXPORTED, AttnArgs, TVError, accept, accept_noalloc, accept_workspace_size, attn, attn_args, attn_workspace_size, build_mask, lib,
-                      status_str)
+from .binding import (EXPORTED, AttnArgs, TVError, accept, accept_noalloc, accept_workspace_size, attn, attn_args,
+                      attn_workspace_size, build_mask, kv_commit, lib, status_str)
 
-__all__ = ["EXPORTED", "AttnArgs", "TVError", "accept", "accept_noalloc", "accept_workspace_size", "attn", "attn_args", "attn_workspace_size", "build_mask",
-           "lib", "status_str"]
+__all__ = ["EXPORTED", "AttnArgs", "TVError", "accept", "accept_noalloc", "accept_workspace_size", "attn", "attn_args",
+           "attn_workspace_size", "build_mask", "kv_commit", "lib", "status_str"]

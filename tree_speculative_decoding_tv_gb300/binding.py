@@ -24,7 +24,7 @@ TV_ERR_TIMEOUT = 5
 TV_ERR_UNIMPLEMENTED = 6
 
 EXPORTED = ("tv_status_str", "tv_version", "tv_build_mask", "tv_attn_workspace_size", "tv_attn",
-            "tv_accept_workspace_size", "tv_accept", "tv_accept_noalloc")
+            "tv_accept_workspace_size", "tv_accept", "tv_accept_noalloc", "tv_kv_commit")
 NOALLOC_MAX_ROWS = 8192  # TV_ACCEPT_NOALLOC_MAX_ROWS
 
 
@@ -73,6 +73,8 @@ def lib() -> C.CDLL:
         L.tv_accept.restype = I
         L.tv_accept_noalloc.argtypes = [P, I, P, P, P, I, I, P, P, P, P, P, P]
         L.tv_accept_noalloc.restype = I
+        L.tv_kv_commit.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P]
+        L.tv_kv_commit.restype = I
         _lib = L
     return _lib
 
@@ -188,3 +190,18 @@ def accept_noalloc(logits, draft, parent, mask, status=None, out=None, stream=No
                                  _p(bonus), _p(status), _stream(stream))
     _check(rc, "tv_accept_noalloc")
     return am, n_acc, path, bonus
+
+
+def kv_commit(k_cache, v_cache, block_table, prefix_lens, n_acc, path, new_prefix_lens=None, status=None,
+              stream=None):
+    """tv_kv_commit: moves the accepted path's K/V into place (caches updated in place);
+    returns new_prefix_lens int32 [nb]."""
+    num_blocks, Hkv, page, D = k_cache.shape
+    nb, B = path.shape
+    if new_prefix_lens is None:
+        new_prefix_lens = torch.empty(nb, dtype=torch.int32, device=k_cache.device)
+    rc = lib().tv_kv_commit(_p(k_cache), _p(v_cache), _p(block_table), _p(prefix_lens), _p(n_acc), _p(path), nb, B,
+                            Hkv, D, page, num_blocks, block_table.shape[1], _p(new_prefix_lens), _p(status),
+                            _stream(stream))
+    _check(rc, "tv_kv_commit")
+    return new_prefix_lens

@@ -167,4 +167,27 @@ int32_t tv_accept_noalloc(const uint16_t *logits_d, int32_t V, const int32_t *dr
     return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
 
+int32_t tv_kv_commit(void *k_cache_d, void *v_cache_d, const int32_t *block_table_d, const int32_t *prefix_lens_d,
+                     const int32_t *n_acc_d, const int32_t *path_d, int32_t nb, int32_t B, int32_t Hkv, int32_t D,
+                     int32_t page_size, int32_t num_blocks, int32_t max_pages, int32_t *new_prefix_lens_d,
+                     int32_t *dev_status_d, void *stream)
+{
+    if (nb < 0 || Hkv < 1 || num_blocks < 1 || max_pages < 1) return TV_ERR_INVALID_ARG;
+    if (B < 1 || B > kMaxB || D != kHeadDim || page_size != kPageSize) return TV_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)nb * Hkv >= (1ll << 31) || (long long)num_blocks * Hkv * kPageSize >= (1ll << 31))
+        return TV_ERR_UNSUPPORTED_SHAPE;
+    if (!k_cache_d || !v_cache_d || !block_table_d || !prefix_lens_d || !n_acc_d || !path_d || !new_prefix_lens_d)
+        return TV_ERR_INVALID_ARG;
+    if (new_prefix_lens_d == prefix_lens_d) return TV_ERR_INVALID_ARG;
+    if (!aligned(k_cache_d, 16) || !aligned(v_cache_d, 16) || !aligned(block_table_d, 4) ||
+        !aligned(prefix_lens_d, 4) || !aligned(n_acc_d, 4) || !aligned(path_d, 4) || !aligned(new_prefix_lens_d, 4) ||
+        !aligned(dev_status_d, 4))
+        return TV_ERR_INVALID_ARG;
+    if (nb == 0) return TV_OK;
+    cudaError_t e = tv::launch_kv_commit(static_cast<uint16_t *>(k_cache_d), static_cast<uint16_t *>(v_cache_d),
+                                         block_table_d, prefix_lens_d, n_acc_d, path_d, nb, B, Hkv, D, num_blocks,
+                                         max_pages, new_prefix_lens_d, dev_status_d, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
 }  // extern "C"

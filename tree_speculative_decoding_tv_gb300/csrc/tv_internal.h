@@ -45,6 +45,12 @@ cudaError_t launch_accept_noalloc(const uint16_t *logits, int V, const int32_t *
                                   const uint32_t *mask, int B, int nb, int32_t *am, int32_t *n_acc, int32_t *path,
                                   int32_t *bonus, int32_t *status, int num_sms, cudaStream_t stream);
 
+// Commit of the accepted branch's K/V (one CTA per (sequence, kv head)).
+cudaError_t launch_kv_commit(uint16_t *k_cache, uint16_t *v_cache, const int32_t *block_table,
+                             const int32_t *prefix_lens, const int32_t *n_acc, const int32_t *path, int nb, int B,
+                             int Hkv, int D, int num_blocks, int max_pages, int32_t *new_prefix_lens, int32_t *status,
+                             cudaStream_t stream);
+
 // Workspace bytes the attention needs with `ctas` CTAs over `row_tiles`
 // (sequence, kv head, 128-row tile) units, and that unit count for `a`.
 size_t attn_workspace_bytes(int ctas, int row_tiles);
