@@ -11,6 +11,7 @@ Functions (numpy in, numpy out):
   lse_merge(O_parts, lse_parts)              -> (O, LSE)
   argmax(logits_bf16)                        -> int32 [rows]
   accept(logits, draft, parent)              -> (argmax, n_acc, path, bonus)
+  build_tree(logp, tokens, B, w)              -> (parent, token, score)   best-first, top-w rounds
   kv_commit(k_cache, v_cache, block_table, prefix_lens, n_acc, path)
                                              -> (k_cache', v_cache', new prefix_lens)  (copies)
 Every pinned property of these functions is listed in ``tests/test_oracle_pins.py``.
@@ -59,8 +60,9 @@ def _load():
         lib.tvo_accept.argtypes = [P, C.c_long, P, P, C.c_int, C.c_int, P, P, P, P]
         lib.tvo_kv_commit.argtypes = [P, P, P, P, P, P, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
                                       C.c_int, P]
+        lib.tvo_build_tree.argtypes = [P, P, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, P, P, P]
         for f in (lib.tvo_build_mask, lib.tvo_attn, lib.tvo_lse_merge, lib.tvo_argmax, lib.tvo_accept,
-                  lib.tvo_kv_commit):
+                  lib.tvo_kv_commit, lib.tvo_build_tree):
             f.restype = C.c_int
         _lib = lib
     return _lib
@@ -179,3 +181,17 @@ def kv_commit(k_cache, v_cache, block_table, prefix_lens, n_acc, path):
     _check(_load().tvo_kv_commit(_ptr(k), _ptr(v), _ptr(block_table), _ptr(prefix_lens), _ptr(n_acc), _ptr(path),
                                  nb, B, Hkv, D, page, block_table.shape[1], num_blocks, _ptr(new_pl)), "kv_commit")
     return k, v, new_pl
+
+
+def build_tree(logp, tokens, B, w=1):
+    """Best-first tree (top-w rounds) from per-depth candidates logp/tokens [nb][Dmax][K].
+    Returns parent, token int32 [nb][B] and score float32 [nb][B]; node 0 is the root."""
+    logp = _c(logp, np.float32)
+    tokens = _c(tokens, np.int32)
+    nb, Dmax, K = logp.shape
+    parent = np.zeros((nb, B), np.int32)
+    token = np.zeros((nb, B), np.int32)
+    score = np.zeros((nb, B), np.float32)
+    _check(_load().tvo_build_tree(_ptr(logp), _ptr(tokens), nb, Dmax, K, B, w, _ptr(parent), _ptr(token),
+                                  _ptr(score)), "build_tree")
+    return parent, token, score

@@ -388,3 +388,85 @@ int tvo_kv_commit(uint16_t *k_cache, uint16_t *v_cache, const int32_t *block_tab
     free(tmp);
     return rc;
 }
+
+/* ---------------------------------------------------------- tree building */
+
+/* Best-first draft-tree construction with top-w rounds.
+ * JETFLOW summary, §2 "Estrategia de Entrenamiento" / tree construction: the
+ * draft head emits logits for every tree depth at once, a branch score (by
+ * default the cumulative draft log-probability) ranks the nodes and best-first
+ * expansion builds the tree up to a budget.  DFlash-TfM summary, §2
+ * "Construcción de Árboles": the top w candidates are taken from the candidate
+ * heap and expanded together, so B nodes take ceil(B/w) rounds.
+ * Reading: depth d's candidates are the K tokens tok[d][c] with log-probs
+ * logp[d][c] (c = 0..K-1, per sequence), the same for every node at depth d-1;
+ * a candidate child (node u, rank c) at depth d scores score[u] + logp[d][c] in
+ * fp32 (the rounding the GPU uses); node 0 is the root (score 0, depth 0).
+ * Each round takes the w best candidates in the heap (larger score first; ties to
+ * the smaller parent index, then the smaller rank), numbers them in that order
+ * and only then pushes their K children (depth < Dmax).  Outputs per sequence:
+ * parent[b][i] (-1 for the root), token[b][i] (-1 for the root), score[b][i].
+ * logp/tok are [nb][Dmax][K] (depth d at index d-1). */
+typedef struct { float s; int u, c; } tvo_cand;
+
+static int cand_better(const tvo_cand *a, const tvo_cand *b)
+{
+    if (a->s != b->s) return a->s > b->s;
+    if (a->u != b->u) return a->u < b->u;
+    return a->c < b->c;
+}
+
+int tvo_build_tree(const float *logp, const int32_t *tok, int nb, int Dmax, int K, int B, int w, int32_t *parent,
+                   int32_t *token, float *score)
+{
+    if (!logp || !tok || !parent || !token || !score || nb < 0 || Dmax < 1 || K < 1 || B < 1 || w < 1)
+        return TVO_ERR_ARG;
+    {   /* the full tree of depth Dmax must hold B nodes */
+        long total = 1, level = 1;
+        for (int d = 1; d <= Dmax && total < B; d++) { level *= K; total += level; if (level > B) level = B; }
+        if (total < B) return TVO_ERR_ARG;
+    }
+    /* a plain array of candidates; each round scans it w times (slow and obvious) */
+    const long cap = (long)B * K + 1;
+    tvo_cand *pool = malloc(sizeof(tvo_cand) * (size_t)cap);
+    int *dep = malloc(sizeof(int) * (size_t)B);
+    tvo_cand *round_sel = malloc(sizeof(tvo_cand) * (size_t)w);
+    if (!pool || !dep || !round_sel) { free(pool); free(dep); free(round_sel); return TVO_ERR_ARG; }
+    for (int b = 0; b < nb; b++) {
+        const float *lp = logp + (size_t)b * Dmax * K;
+        const int32_t *tk = tok + (size_t)b * Dmax * K;
+        int32_t *par = parent + (size_t)b * B, *tkn = token + (size_t)b * B;
+        float *sc = score + (size_t)b * B;
+        par[0] = -1; tkn[0] = -1; sc[0] = 0.f; dep[0] = 0;
+        long np = 0;
+        for (int c = 0; c < K; c++) { pool[np].s = 0.f + lp[c]; pool[np].u = 0; pool[np].c = c; np++; }
+        int made = 1;
+        while (made < B && np > 0) {
+            int take = w < B - made ? w : B - made;
+            int got = 0;
+            for (int t = 0; t < take && np > 0; t++) {
+                long best = 0;
+                for (long j = 1; j < np; j++)
+                    if (cand_better(&pool[j], &pool[best])) best = j;
+                round_sel[got++] = pool[best];
+                pool[best] = pool[--np];
+            }
+            int first = made;
+            for (int t = 0; t < got; t++) {
+                const int i = made++;
+                par[i] = round_sel[t].u;
+                dep[i] = dep[round_sel[t].u] + 1;
+                tkn[i] = tk[(size_t)(dep[i] - 1) * K + round_sel[t].c];
+                sc[i] = round_sel[t].s;
+            }
+            for (int i = first; i < made; i++)
+                if (dep[i] < Dmax)
+                    for (int c = 0; c < K; c++) {
+                        pool[np].s = sc[i] + lp[(size_t)dep[i] * K + c];
+                        pool[np].u = i; pool[np].c = c; np++;
+                    }
+        }
+    }
+    free(pool); free(dep); free(round_sel);
+    return TVO_OK;
+}

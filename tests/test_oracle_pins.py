@@ -474,3 +474,92 @@ def test_kv_commit_rejects_a_path_that_is_not_a_root_path(bad):
     path[0, :3] = bad
     with pytest.raises(oracle.OracleError):
         oracle.kv_commit(w.k_cache, w.v_cache, w.block_table, w.prefix_lens, np.array([2], np.int32), path)
+
+
+# --------------------------------------------------------------- tree building
+
+def _tree_inputs(seed, nb, Dmax, K):
+    """Distinct random log-probs, sorted best first per depth; token = 1000 * depth + rank."""
+    rng = np.random.default_rng(seed)
+    lp = np.log(rng.dirichlet([0.3] * K, size=(nb, Dmax)) + 1e-9).astype(np.float32)
+    lp = -np.sort(-lp, axis=-1)
+    tok = np.broadcast_to((1000 * np.arange(1, Dmax + 1)[:, None] + np.arange(K)[None, :]).astype(np.int32),
+                          (nb, Dmax, K)).copy()
+    return lp, tok
+
+
+def _all_paths(lp, Dmax, K):
+    """Every node of the full K-ary tree as (rank path, fp32 score accumulated root to leaf)."""
+    out = [((), np.float32(0.0))]
+    frontier = [((), np.float32(0.0))]
+    for d in range(Dmax):
+        nxt = []
+        for path, s in frontier:
+            for c in range(K):
+                nxt.append((path + (c,), np.float32(s + lp[d, c])))
+        out += nxt
+        frontier = nxt
+    return out
+
+
+def _rank_paths(parent, token):
+    """Rank path of every node, read off the tokens (token % 1000 = rank)."""
+    paths = [()]
+    for i in range(1, len(parent)):
+        paths.append(paths[parent[i]] + (int(token[i]) % 1000,))
+    return paths
+
+
+@pytest.mark.parametrize("Dmax,K,B", [(3, 4, 20), (4, 3, 60), (2, 5, 31), (6, 2, 64)])
+def test_build_tree_best_first_is_the_top_B_nodes_by_score(Dmax, K, B):
+    """w = 1: the nodes are the B best-scoring nodes of the full tree (log-probs <= 0, so the
+    set is closed under taking parents), created in decreasing score order (brute force)."""
+    lp, tok = _tree_inputs(Dmax * 10 + K, 2, Dmax, K)
+    parent, token, score = oracle.build_tree(lp, tok, B, 1)
+    for b in range(2):
+        every = sorted(_all_paths(lp[b], Dmax, K), key=lambda t: -t[1])
+        want = [p for p, _ in every[:B]]
+        assert _rank_paths(parent[b], token[b]) == want
+        assert np.all(np.diff(score[b]) <= 0)
+        for i in range(1, B):
+            assert score[b, i] == np.float32(score[b, parent[b, i]] + lp[b, len(want[i]) - 1, want[i][-1]])
+
+
+@pytest.mark.parametrize("w", [2, 3, 8, 64])
+def test_build_tree_top_w_rounds(w):
+    """Each round takes the w best candidates available when it starts (children of nodes made
+    in earlier rounds), in order, recomputed here from the output tree alone."""
+    Dmax, K, B = 5, 4, 100
+    lp, tok = _tree_inputs(w, 1, Dmax, K)
+    parent, token, score = oracle.build_tree(lp, tok, B, w)
+    par, paths = parent[0], _rank_paths(parent[0], token[0])
+    made = 1
+    while made < B:
+        have = set(paths[:made])
+        avail = []
+        for u in range(made):
+            if len(paths[u]) < Dmax:
+                for c in range(K):
+                    if paths[u] + (c,) not in have:
+                        avail.append((-np.float32(score[0, u] + lp[0, len(paths[u]), c]), u, c))
+        avail.sort()
+        take = min(w, B - made, len(avail))  # a round takes fewer when fewer are available
+        for t in range(take):
+            i = made + t
+            assert (par[i], paths[i][-1]) == (avail[t][1], avail[t][2])
+            assert score[0, i] == -avail[t][0]
+        made += take
+
+
+def test_build_tree_closed_forms():
+    lp, tok = _tree_inputs(5, 1, 6, 3)
+    # one candidate per depth: a chain whose scores are the running sums
+    p1, t1, s1 = oracle.build_tree(lp[:, :, :1].copy(), tok[:, :, :1].copy(), 7, 3)
+    assert p1[0].tolist() == [-1, 0, 1, 2, 3, 4, 5]
+    assert np.array_equal(s1[0, 1:], np.cumsum(lp[0, :, 0], dtype=np.float32))
+    # depth 1 only: a star of the best candidates in rank order
+    p2, t2, s2 = oracle.build_tree(lp[:, :1].copy(), tok[:, :1].copy(), 4, 1)
+    assert p2[0].tolist() == [-1, 0, 0, 0] and t2[0].tolist() == [-1, 1000, 1001, 1002]
+    # a budget larger than the full tree is an argument error
+    with pytest.raises(oracle.OracleError):
+        oracle.build_tree(lp[:, :1].copy(), tok[:, :1].copy(), 5, 1)
