@@ -247,6 +247,28 @@ class Step:
         moved = sum(int(np.sum(pth[b, 1:nacc[b] + 1] != np.arange(1, nacc[b] + 1))) for b in range(self.w.nb))
         return ms, moved * self.w.Hkv * 2 * self.w.D * 2 * 2
 
+    # Per-depth candidate tables for tv_build_tree on the best-first workloads: K candidates
+    # per depth (the recipe's child cap) drawn as the top K of Dirichlet(0.3) over 8, depth cap.
+    TREE_SHAPES = {2: (16, 4), 3: (12, 3), 5: (24, 4)}
+
+    def time_tree(self, config, flush, steps, w=1):
+        """Mean ms of tv_build_tree for this workload's budget (its own graph, same flush), or None."""
+        if config not in self.TREE_SHAPES:
+            return None
+        torch, tv = self.torch, self.tv
+        Dmax, K = self.TREE_SHAPES[config]
+        rng = np.random.default_rng(99)
+        p = rng.dirichlet([0.3] * 8, size=(self.w.nb, Dmax))
+        lp = np.log(-np.sort(-p, axis=-1)[..., :K] + 1e-12).astype(np.float32)
+        tok = rng.integers(0, self.w.V, size=(self.w.nb, Dmax, K)).astype(np.int32)
+        d_lp, d_tok = torch.from_numpy(lp).to(self.q.device), torch.from_numpy(tok).to(self.q.device)
+        out = tv.build_tree(d_lp, d_tok, self.w.B, w, status=self.status)  # warm (outside the graph)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            tv.build_tree(d_lp, d_tok, self.w.B, w, out=out, status=self.status)
+        return self.time_stage(g, flush, steps)
+
     def time_stage(self, graph, flush, steps):
         """Mean ms of one stage graph replay, L2 flushed before each (CUDA events, current stream)."""
         torch = self.torch
@@ -379,6 +401,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     if any(x.status.item() != 0 for x in sets):
         raise RuntimeError("device status set in the end-to-end run")
     commit_ms, commit_bytes = st.time_commit(flush, args.steps)
+    tree_ms = st.time_tree(args.config, flush, args.steps)
     if st.status.item() != 0:
         raise RuntimeError(f"device status {st.status.item()} in the commit stage")
     if world > 1:
@@ -427,6 +450,9 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
             "attention_nodes_per_s": nodes / t_attn, "attention_roofline": attn_roof, "accept_roofline": acc_roof,
             "attention_bytes": ab, "attention_flops": af, "accept_bytes": lb,
             "kv_commit_ms": commit_ms, "kv_commit_bytes": commit_bytes,
+            "build_tree_ms": tree_ms,
+            "build_tree_note": "tv_build_tree (best-first, w = 1) of this workload's budget from per-depth candidate "
+                               "tables, its own graph; not part of the step (it precedes verification)",
             "kv_commit_note": "tv_kv_commit of the accepted branch, its own graph after the timed steps; not part "
                               "of the step (it rewrites the caches); latency-bound (a few KB moved)",
         },

@@ -16,6 +16,11 @@
  *           masking.
  *   [TfM-3] DFlash-TfM summary, §3 "Solución": the tree is topologically
  *           ordered (parents before children).
+ *   [JF-2t] JETFLOW summary, §2 "Estrategia de Entrenamiento", tree
+ *           construction: logits for every depth at once, cumulative draft
+ *           log-probability as the branch score, best-first expansion to a budget.
+ *   [TfM-2t] DFlash-TfM summary, §2 "Construcción de Árboles": the top w
+ *           candidates of the heap are expanded together (ceil(B/w) rounds).
  *   [JF-4]  JETFLOW summary, §3 item 2 and §4: accepted tokens (tau) and
  *           longer accepted prefixes; the pages give no acceptance rule, so
  *           the greedy rule below is this library's reading.
@@ -180,6 +185,35 @@ TV_API int32_t tv_accept(const uint16_t *logits_d, int32_t V, const int32_t *dra
                          const int32_t *parent_d, const uint32_t *mask_d, int32_t B, int32_t nb,
                          int32_t *argmax_d, int32_t *n_acc_d, int32_t *path_d, int32_t *bonus_d,
                          int32_t *dev_status_d, void *workspace_d, size_t workspace_bytes, void *stream);
+
+/*
+ * Best-first draft-tree construction with top-w rounds  [JF-2t] [TfM-2t]
+ *
+ *   Per sequence: depth d (1..Dmax) offers K candidates, token tokens[b][d-1][c]
+ *   with draft log-probability logp[b][d-1][c], sorted best first (c = 0 best);
+ *   the same candidates hang under every node at depth d-1 (the draft head emits
+ *   logits for every depth at once).  A candidate child (u, c) at depth d scores
+ *   score[u] + logp[d-1][c] (fp32, cumulative draft log-probability); node 0 is
+ *   the root (score 0).  Each round takes the min(w, B - made) best candidates
+ *   (larger score, then smaller parent index, then smaller rank), numbers them in
+ *   that order (so the tree is topologically ordered) and only then adds their
+ *   children; w = 1 is plain best-first expansion, B nodes take ceil(B/w)
+ *   rounds once the heap holds w candidates.
+ *
+ *   logp_d    fp32 [nb][Dmax][K], finite, non-increasing along c
+ *   tokens_d  int32 [nb][Dmax][K]
+ *   parent_d  int32 [nb][B] (out): -1 for the root; feeds tv_build_mask / tv_accept
+ *   token_d   int32 [nb][B] (out): the draft token of each node, -1 for the root
+ *   score_d   fp32 [nb][B] (out): cumulative log-probability, 0 for the root
+ *   Limits: 1 <= B <= 256, 1 <= K <= 32767, 1 <= Dmax <= 32767, w >= 1, and the
+ *   full tree of depth Dmax must hold B nodes (else TV_ERR_INVALID_ARG).
+ * Ordering: a programmatic dependent of the previous kernel; waits for it before
+ * reading anything.  Log-probs that are not finite or not sorted write
+ * TV_ERR_INVALID_ARG to dev_status_d (outputs unspecified).
+ */
+TV_API int32_t tv_build_tree(const float *logp_d, const int32_t *tokens_d, int32_t nb, int32_t Dmax, int32_t K,
+                             int32_t B, int32_t w, int32_t *parent_d, int32_t *token_d, float *score_d,
+                             int32_t *dev_status_d, void *stream);
 
 /*
  * Commit of the accepted branch  [TfM-3] (the pages commit state once the

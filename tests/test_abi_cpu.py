@@ -129,6 +129,24 @@ def test_kv_commit_argument_checks(L):
     assert call(k=P(FAKE + 8)) == 1 and call(n=P(FAKE + 2)) == 1
 
 
+def test_build_tree_argument_checks(L):
+    P = C.c_void_p
+    base = dict(lp=P(FAKE), tk=P(FAKE), nb=2, D=16, K=8, B=256, w=1, par=P(FAKE), tok=P(FAKE), sc=P(FAKE))
+
+    def call(**kw):
+        d = dict(base)
+        d.update(kw)
+        return L.tv_build_tree(d["lp"], d["tk"], d["nb"], d["D"], d["K"], d["B"], d["w"], d["par"], d["tok"], d["sc"],
+                               None, None)
+
+    assert call(nb=0) == 0
+    assert call(nb=-1) == 1 and call(D=0) == 1 and call(K=0) == 1 and call(w=0) == 1
+    assert call(B=0) == 3 and call(B=257) == 3 and call(K=40000) == 3
+    assert call(lp=None) == 1 and call(sc=None) == 1 and call(tk=P(FAKE + 2)) == 1
+    assert call(D=1, K=8, B=10) == 1          # the full tree of depth 1 holds 9 nodes
+    assert call(D=1, K=8, B=9, nb=0) == 0 and call(D=2, K=2, B=8, nb=0) == 1
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "_lib", None)
     monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "missing.so"))

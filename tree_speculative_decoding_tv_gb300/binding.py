@@ -24,7 +24,7 @@ TV_ERR_TIMEOUT = 5
 TV_ERR_UNIMPLEMENTED = 6
 
 EXPORTED = ("tv_status_str", "tv_version", "tv_build_mask", "tv_attn_workspace_size", "tv_attn",
-            "tv_accept_workspace_size", "tv_accept", "tv_accept_noalloc", "tv_kv_commit")
+            "tv_accept_workspace_size", "tv_accept", "tv_accept_noalloc", "tv_kv_commit", "tv_build_tree")
 NOALLOC_MAX_ROWS = 8192  # TV_ACCEPT_NOALLOC_MAX_ROWS
 
 
@@ -75,6 +75,8 @@ def lib() -> C.CDLL:
         L.tv_accept_noalloc.restype = I
         L.tv_kv_commit.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P]
         L.tv_kv_commit.restype = I
+        L.tv_build_tree.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P]
+        L.tv_build_tree.restype = I
         _lib = L
     return _lib
 
@@ -205,3 +207,18 @@ def kv_commit(k_cache, v_cache, block_table, prefix_lens, n_acc, path, new_prefi
                             _stream(stream))
     _check(rc, "tv_kv_commit")
     return new_prefix_lens
+
+
+def build_tree(logp, tokens, B, w=1, out=None, status=None, stream=None):
+    """tv_build_tree: logp fp32 / tokens int32 [nb][Dmax][K] (cuda) -> (parent, token int32 [nb][B],
+    score fp32 [nb][B])."""
+    nb, Dmax, K = logp.shape
+    dev = logp.device
+    if out is None:
+        out = (torch.empty((nb, B), dtype=torch.int32, device=dev), torch.empty((nb, B), dtype=torch.int32, device=dev),
+               torch.empty((nb, B), dtype=torch.float32, device=dev))
+    parent, token, score = out
+    rc = lib().tv_build_tree(_p(logp), _p(tokens), nb, Dmax, K, B, w, _p(parent), _p(token), _p(score), _p(status),
+                             _stream(stream))
+    _check(rc, "tv_build_tree")
+    return parent, token, score

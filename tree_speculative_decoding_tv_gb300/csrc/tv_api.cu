@@ -167,6 +167,32 @@ int32_t tv_accept_noalloc(const uint16_t *logits_d, int32_t V, const int32_t *dr
     return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
 
+int32_t tv_build_tree(const float *logp_d, const int32_t *tokens_d, int32_t nb, int32_t Dmax, int32_t K, int32_t B,
+                      int32_t w, int32_t *parent_d, int32_t *token_d, float *score_d, int32_t *dev_status_d,
+                      void *stream)
+{
+    if (nb < 0 || Dmax < 1 || K < 1 || w < 1) return TV_ERR_INVALID_ARG;
+    if (B < 1 || B > kMaxB || K > 32767 || Dmax > 32767) return TV_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)nb * Dmax * K >= (1ll << 31)) return TV_ERR_UNSUPPORTED_SHAPE;
+    {  // the full tree of depth Dmax must hold B nodes
+        long long total = 1, level = 1;
+        for (int d = 1; d <= Dmax && total < B; ++d) {
+            level *= K;
+            total += level;
+            if (level > B) level = B;
+        }
+        if (total < B) return TV_ERR_INVALID_ARG;
+    }
+    if (!logp_d || !tokens_d || !parent_d || !token_d || !score_d) return TV_ERR_INVALID_ARG;
+    if (!aligned(logp_d, 4) || !aligned(tokens_d, 4) || !aligned(parent_d, 4) || !aligned(token_d, 4) ||
+        !aligned(score_d, 4) || !aligned(dev_status_d, 4))
+        return TV_ERR_INVALID_ARG;
+    if (nb == 0) return TV_OK;
+    cudaError_t e = tv::launch_build_tree(logp_d, tokens_d, nb, Dmax, K, B, w, parent_d, token_d, score_d,
+                                          dev_status_d, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
 int32_t tv_kv_commit(void *k_cache_d, void *v_cache_d, const int32_t *block_table_d, const int32_t *prefix_lens_d,
                      const int32_t *n_acc_d, const int32_t *path_d, int32_t nb, int32_t B, int32_t Hkv, int32_t D,
                      int32_t page_size, int32_t num_blocks, int32_t max_pages, int32_t *new_prefix_lens_d,

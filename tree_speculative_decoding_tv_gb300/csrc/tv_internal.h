@@ -45,6 +45,10 @@ cudaError_t launch_accept_noalloc(const uint16_t *logits, int V, const int32_t *
                                   const uint32_t *mask, int B, int nb, int32_t *am, int32_t *n_acc, int32_t *path,
                                   int32_t *bonus, int32_t *status, int num_sms, cudaStream_t stream);
 
+// Best-first draft-tree construction with top-w rounds (one warp per sequence).
+cudaError_t launch_build_tree(const float *logp, const int32_t *tok, int nb, int Dmax, int K, int B, int w,
+                              int32_t *parent, int32_t *token, float *score, int32_t *status, cudaStream_t stream);
+
 // Commit of the accepted branch's K/V (one CTA per (sequence, kv head)).
 cudaError_t launch_kv_commit(uint16_t *k_cache, uint16_t *v_cache, const int32_t *block_table,
                              const int32_t *prefix_lens, const int32_t *n_acc, const int32_t *path, int nb, int B,
