@@ -12,6 +12,7 @@ Functions (numpy in, numpy out):
   argmax(logits_bf16)                        -> int32 [rows]
   accept(logits, draft, parent)              -> (argmax, n_acc, path, bonus)
   build_tree(logp, tokens, B, w)              -> (parent, token, score)   best-first, top-w rounds
+  gdn_tree(q, k, v, alpha, beta, S0, parent)  -> O float64 [nb*B][H][D]  (Gated DeltaNet state per root path)
   kv_commit(k_cache, v_cache, block_table, prefix_lens, n_acc, path)
                                              -> (k_cache', v_cache', new prefix_lens)  (copies)
 Every pinned property of these functions is listed in ``tests/test_oracle_pins.py``.
@@ -61,8 +62,9 @@ def _load():
         lib.tvo_kv_commit.argtypes = [P, P, P, P, P, P, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
                                       C.c_int, P]
         lib.tvo_build_tree.argtypes = [P, P, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, P, P, P]
+        lib.tvo_gdn_tree.argtypes = [P, P, P, P, P, P, P, C.c_int, C.c_int, C.c_int, C.c_int, P]
         for f in (lib.tvo_build_mask, lib.tvo_attn, lib.tvo_lse_merge, lib.tvo_argmax, lib.tvo_accept,
-                  lib.tvo_kv_commit, lib.tvo_build_tree):
+                  lib.tvo_kv_commit, lib.tvo_build_tree, lib.tvo_gdn_tree):
             f.restype = C.c_int
         _lib = lib
     return _lib
@@ -195,3 +197,17 @@ def build_tree(logp, tokens, B, w=1):
     _check(_load().tvo_build_tree(_ptr(logp), _ptr(tokens), nb, Dmax, K, B, w, _ptr(parent), _ptr(token),
                                   _ptr(score)), "build_tree")
     return parent, token, score
+
+
+def gdn_tree(q, k, v, alpha, beta, S0, parent):
+    """Gated DeltaNet outputs of every tree node (fp64), each from its own root path's state."""
+    q, k, v = _c(q, np.uint16), _c(k, np.uint16), _c(v, np.uint16)
+    alpha, beta, S0 = _c(alpha, np.float32), _c(beta, np.float32), _c(S0, np.float32)
+    parent = _c(parent, np.int32)
+    nb, B = parent.shape
+    H, D = q.shape[1], q.shape[2]
+    assert q.shape == (nb * B, H, D) and S0.shape == (nb, H, D, D) and alpha.shape == (nb * B, H)
+    O = np.zeros((nb * B, H, D), np.float64)
+    _check(_load().tvo_gdn_tree(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0), _ptr(parent),
+                                nb, B, H, D, _ptr(O)), "gdn_tree")
+    return O

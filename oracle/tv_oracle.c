@@ -470,3 +470,63 @@ int tvo_build_tree(const float *logp, const int32_t *tok, int nb, int Dmax, int 
     free(pool); free(dep); free(round_sel);
     return TVO_OK;
 }
+
+/* ------------------------------------------------- Gated DeltaNet over a tree */
+
+/* Tree verification through a Gated DeltaNet layer (DFlash-TfM summary, §3
+ * "Verificación de Árboles sin Rollback"): the recurrent state follows
+ *   S_t = alpha_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T
+ * (S is D x D: rows indexed by the key dimension, columns by the value
+ * dimension), and every tree node must see the state its own root path would
+ * have built from the committed state S0, without touching S0 (no rollback).
+ * Reading: node i's state is the recurrence applied along root ... i starting
+ * from S0 (parent[i] = -1 for the root, which is itself a tree node), and its
+ * output is o_i = S_i^T q_i.  This is the plain definition, applied by brute force
+ * per node and head, in fp64.
+ *   q, k, v: bf16 [nb*B][H][D]; alpha, beta: fp32 [nb*B][H]; S0: fp32 [nb][H][D][D];
+ *   parent: int32 [nb][B] topologically ordered; O: fp64 [nb*B][H][D]. */
+int tvo_gdn_tree(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha, const float *beta,
+                 const float *S0, const int32_t *parent, int nb, int B, int H, int D, double *O)
+{
+    if (!q || !k || !v || !alpha || !beta || !S0 || !parent || !O || nb < 0 || B < 1 || H < 1 || D < 1)
+        return TVO_ERR_ARG;
+    double *S = malloc(sizeof(double) * (size_t)D * D);
+    double *kv = malloc(sizeof(double) * (size_t)D * 3);
+    int *path = malloc(sizeof(int) * (size_t)B);
+    if (!S || !kv || !path) { free(S); free(kv); free(path); return TVO_ERR_ARG; }
+    int rc = TVO_OK;
+    for (int b = 0; b < nb && rc == TVO_OK; b++) {
+        const int32_t *p = parent + (size_t)b * B;
+        if (!parent_is_valid(p, B)) { rc = TVO_ERR_NOT_TOPOLOGICAL; break; }
+        for (int h = 0; h < H; h++) {
+            for (int i = 0; i < B; i++) {
+                int len = 0;
+                for (int j = i; j != -1; j = p[j]) path[len++] = j;
+                const float *s0 = S0 + ((size_t)b * H + h) * D * D;
+                for (int x = 0; x < D * D; x++) S[x] = s0[x];
+                for (int t = len - 1; t >= 0; t--) {          /* root first */
+                    const size_t row = ((size_t)b * B + path[t]) * H + h;
+                    const double a = alpha[row], be = beta[row];
+                    double *kk = kv, *vv = kv + D, *ks = kv + 2 * D;
+                    for (int d = 0; d < D; d++) { kk[d] = bf16_value(k[row * D + d]); vv[d] = bf16_value(v[row * D + d]); }
+                    for (int c = 0; c < D; c++) {                /* ks = k^T S (one entry per value column) */
+                        double acc = 0.0;
+                        for (int r = 0; r < D; r++) acc += kk[r] * S[(size_t)r * D + c];
+                        ks[c] = acc;
+                    }
+                    for (int r = 0; r < D; r++)
+                        for (int c = 0; c < D; c++)
+                            S[(size_t)r * D + c] = a * (S[(size_t)r * D + c] - be * kk[r] * ks[c]) + be * kk[r] * vv[c];
+                }
+                const size_t row = ((size_t)b * B + i) * H + h;
+                for (int c = 0; c < D; c++) {
+                    double acc = 0.0;
+                    for (int r = 0; r < D; r++) acc += S[(size_t)r * D + c] * bf16_value(q[row * D + r]);
+                    O[row * D + c] = acc;
+                }
+            }
+        }
+    }
+    free(S); free(kv); free(path);
+    return rc;
+}

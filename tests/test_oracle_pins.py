@@ -563,3 +563,92 @@ def test_build_tree_closed_forms():
     # a budget larger than the full tree is an argument error
     with pytest.raises(oracle.OracleError):
         oracle.build_tree(lp[:, :1].copy(), tok[:, :1].copy(), 5, 1)
+
+
+# ------------------------------------------------------ Gated DeltaNet over a tree
+
+def _gdn_path(parent, i):
+    out = []
+    while i != -1:
+        out.append(i)
+        i = int(parent[i])
+    return out[::-1]
+
+
+def _gdn_small(seed, nb=2, B=12, H=2, D=16, trees=None):
+    rng = np.random.default_rng(seed)
+    if trees is None:
+        trees = _random_trees(rng, B, nb)
+    return wl.make_gdn_workload("pin", nb, B, H, D, trees, seed)
+
+
+def test_gdn_zero_write_strength_closed_form():
+    """beta = 0: the state only decays, o_i = (prod of alpha on i's root path) S0^T q_i."""
+    w = _gdn_small(1)
+    beta = np.zeros_like(w.beta)
+    O = oracle.gdn_tree(w.q, w.k, w.v, w.alpha, beta, w.S0, w.parent)
+    for b in range(w.nb):
+        for i in range(w.B):
+            g = np.prod([np.float64(w.alpha[b * w.B + j]) for j in _gdn_path(w.parent[b], i)], axis=0)  # [H]
+            for h in range(w.H):
+                want = g[h] * (w.S0[b, h].astype(np.float64).T @ _f64(w.q[b * w.B + i, h]))
+                assert np.allclose(O[b * w.B + i, h], want, rtol=1e-12, atol=1e-14)
+
+
+def test_gdn_unit_keys_overwrite_rows():
+    """alpha = beta = 1 and unit keys e_r: each step replaces row r of the state by v, so node i's
+    state is S0 with the rows of its path's keys replaced (a key met twice keeps the later v)."""
+    B, D = 10, 16
+    rng = np.random.default_rng(3)
+    w = _gdn_small(3, nb=1, B=B, H=1, D=D)
+    rows = rng.integers(0, D, size=B)
+    k = np.zeros((B, 1, D), np.float32)
+    k[np.arange(B), 0, rows] = 1.0
+    kb = wl.f32_to_bf16(k)
+    ones = np.ones_like(w.alpha)
+    O = oracle.gdn_tree(w.q, kb, w.v, ones, ones, w.S0, w.parent)
+    for i in range(B):
+        S = w.S0[0, 0].astype(np.float64).copy()
+        for j in _gdn_path(w.parent[0], i):
+            S[rows[j]] = _f64(w.v[j, 0])
+        assert np.allclose(O[i, 0], S.T @ _f64(w.q[i, 0]), rtol=1e-12, atol=1e-14)
+
+
+def test_gdn_matches_the_masked_triangular_solve():
+    """The chunked form the pages sketch (DFlash-TfM §3): with gamma_i the product of alpha on
+    i's root path, (I + X) U = beta (V - gamma K S0), X_ij = beta_i (gamma_i / gamma_j) k_i.k_j
+    for j a strict ancestor of i, and O = gamma Q S0 + Y U, Y_ij = (gamma_i / gamma_j) q_i.k_j
+    for j an ancestor of i or i itself.  Solved densely by numpy, it must equal the per-path
+    recurrence."""
+    w = _gdn_small(5, nb=2, B=14, H=3, D=16)
+    O = oracle.gdn_tree(w.q, w.k, w.v, w.alpha, w.beta, w.S0, w.parent)
+    for b in range(w.nb):
+        anc = [set(_gdn_path(w.parent[b], i)) for i in range(w.B)]
+        for h in range(w.H):
+            r = slice(b * w.B, (b + 1) * w.B)
+            Q, Kk, Vv = _f64(w.q[r, h]), _f64(w.k[r, h]), _f64(w.v[r, h])
+            al, be = w.alpha[r, h].astype(np.float64), w.beta[r, h].astype(np.float64)
+            S0 = w.S0[b, h].astype(np.float64)
+            gam = np.array([np.prod([al[j] for j in anc[i]]) for i in range(w.B)])
+            X = np.zeros((w.B, w.B))
+            Y = np.zeros((w.B, w.B))
+            for i in range(w.B):
+                for j in anc[i]:
+                    Y[i, j] = gam[i] / gam[j] * (Q[i] @ Kk[j])
+                    if j != i:
+                        X[i, j] = be[i] * gam[i] / gam[j] * (Kk[i] @ Kk[j])
+            U = np.linalg.solve(np.eye(w.B) + X, be[:, None] * (Vv - gam[:, None] * (Kk @ S0)))
+            want = gam[:, None] * (Q @ S0) + Y @ U
+            assert np.allclose(O[r, h], want, rtol=1e-9, atol=1e-11)
+
+
+def test_gdn_invariant_under_sibling_relabelling():
+    rng = np.random.default_rng(8)
+    w = _gdn_small(8, nb=1, B=12, H=2, D=16)
+    parent = w.parent[0]
+    new_of_old, new_parent = _random_topological_relabel(rng, parent)
+    old_of_new = np.argsort(new_of_old)
+    O = oracle.gdn_tree(w.q, w.k, w.v, w.alpha, w.beta, w.S0, w.parent)
+    O2 = oracle.gdn_tree(w.q[old_of_new], w.k[old_of_new], w.v[old_of_new], w.alpha[old_of_new],
+                         w.beta[old_of_new], w.S0, new_parent[None])
+    assert np.allclose(O2[new_of_old], O, rtol=1e-12, atol=1e-14)

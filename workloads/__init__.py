@@ -34,7 +34,7 @@ PAGE = 16
 
 __all__ = [
     "PAGE", "Workload", "f32_to_bf16", "bf16_to_f32", "tree_window", "tree_best_first",
-    "make_workload", "config", "CONFIG_NAMES", "logical_kv",
+    "make_workload", "config", "CONFIG_NAMES", "logical_kv", "GdnWorkload", "make_gdn_workload", "gdn_config",
 ]
 
 
@@ -253,3 +253,62 @@ def logical_kv(w: Workload, b: int, which: str = "k") -> np.ndarray:
     pos = np.arange(n)
     pages = w.block_table[b, pos // PAGE]
     return cache[pages, :, pos % PAGE, :]
+
+
+# --------------------------------------------------------------------- Gated DeltaNet
+
+@dataclass
+class GdnWorkload:
+    """Inputs of one Gated DeltaNet tree-verification step (one layer).
+
+    q, k, v  uint16 (bf16 bits) [nb*B][H][D]   q and k L2-normalised per head before rounding
+    alpha    float32 [nb*B][H]                 gate in [0.85, 1)
+    beta     float32 [nb*B][H]                 write strength in [0.1, 0.9)
+    S0       float32 [nb][H][D][D]             committed state (rows: key dim, columns: value dim)
+    parent   int32 [nb][B]                     topologically ordered tree, parent[b][0] = -1
+    """
+    name: str
+    nb: int
+    B: int
+    H: int
+    D: int
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    alpha: np.ndarray
+    beta: np.ndarray
+    S0: np.ndarray
+    parent: np.ndarray
+
+
+def _unit_bf16(rng, shape):
+    x = rng.standard_normal(shape, dtype=np.float32)
+    x /= np.linalg.norm(x, axis=-1, keepdims=True)
+    return f32_to_bf16(x)
+
+
+def make_gdn_workload(name: str, nb: int, B: int, H: int, D: int, trees, seed: int,
+                      s0_sigma: float = 0.1) -> GdnWorkload:
+    """Seeded GDN inputs: normalised q/k, N(0,1)*0.5 v, gates, write strengths, a random state."""
+    ss = np.random.SeedSequence(seed)
+    r_tree, r_q, r_k, r_v, r_a, r_s = [np.random.default_rng(x) for x in ss.spawn(6)]
+    if callable(trees):
+        parents = [np.asarray(trees(r_tree), dtype=np.int32) for _ in range(nb)]
+    else:
+        parents = [np.asarray(t, dtype=np.int32) for t in trees]
+    parent = np.stack(parents).astype(np.int32).reshape(nb, B)
+    q = _unit_bf16(r_q, (nb * B, H, D))
+    k = _unit_bf16(r_k, (nb * B, H, D))
+    v = _normal_bf16(r_v, (nb * B, H, D), 0.5)
+    alpha = r_a.uniform(0.85, 1.0, size=(nb * B, H)).astype(np.float32)
+    beta = r_a.uniform(0.1, 0.9, size=(nb * B, H)).astype(np.float32)
+    S0 = (r_s.standard_normal((nb, H, D, D), dtype=np.float32) * np.float32(s0_sigma)).astype(np.float32)
+    return GdnWorkload(name=name, nb=nb, B=B, H=H, D=D, q=q, k=k, v=v, alpha=alpha, beta=beta, S0=S0, parent=parent)
+
+
+def gdn_config(seed: int = 0) -> GdnWorkload:
+    """The GDN workload: one sequence, a 128-node best-first tree (the DFlash-TfM summary's
+    tree size for its fused-kernel figure), 32 heads of dimension 128 (the head shape of the
+    Qwen3.6-27B GDN layers the summary evaluates is not printed; 32 x 128 is this recipe's)."""
+    return make_gdn_workload("gdn nb=1 B=128 H=32 D=128 best-first", 1, 128, 32, 128,
+                             lambda r: tree_best_first(r, 128, child_cap=4, max_depth=16), seed)
