@@ -269,6 +269,27 @@ class Step:
             tv.build_tree(d_lp, d_tok, self.w.B, w, out=out, status=self.status)
         return self.time_stage(g, flush, steps)
 
+    def time_gdn(self, flush, steps):
+        """Mean ms of tv_gdn_tree on the Gated DeltaNet tree workload (its own graph, same flush),
+        and that call's algorithmic bytes (q, k, v, gates, S0 in; O out)."""
+        torch, tv = self.torch, self.tv
+        g_w = wl.gdn_config(seed=5)
+        dev = self.q.device
+        f = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        bf = lambda a: f(a.view(np.int16)).view(torch.bfloat16)
+        q, k, v = bf(g_w.q), bf(g_w.k), bf(g_w.v)
+        a, b, S0, par = f(g_w.alpha), f(g_w.beta), f(g_w.S0), f(g_w.parent)
+        out = tv.gdn_tree(q, k, v, a, b, S0, par, status=self.status)  # warm (outside the graph)
+        ws = torch.empty(tv.lib().tv_gdn_tree_workspace_size(g_w.nb, g_w.B, g_w.H, g_w.D), dtype=torch.uint8,
+                         device=dev)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            tv.gdn_tree(q, k, v, a, b, S0, par, out=out, workspace=ws, status=self.status)
+        rows = g_w.nb * g_w.B * g_w.H
+        nbytes = rows * g_w.D * (3 * 2 + 4) + rows * 8 + g_w.S0.nbytes + g_w.parent.nbytes
+        return self.time_stage(g, flush, steps), nbytes, g_w.name
+
     def time_stage(self, graph, flush, steps):
         """Mean ms of one stage graph replay, L2 flushed before each (CUDA events, current stream)."""
         torch = self.torch
@@ -402,6 +423,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         raise RuntimeError("device status set in the end-to-end run")
     commit_ms, commit_bytes = st.time_commit(flush, args.steps)
     tree_ms = st.time_tree(args.config, flush, args.steps)
+    gdn_ms, gdn_bytes, gdn_name = st.time_gdn(flush, args.steps)
     if st.status.item() != 0:
         raise RuntimeError(f"device status {st.status.item()} in the commit stage")
     if world > 1:
@@ -453,6 +475,11 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
             "build_tree_ms": tree_ms,
             "build_tree_note": "tv_build_tree (best-first, w = 1) of this workload's budget from per-depth candidate "
                                "tables, its own graph; not part of the step (it precedes verification)",
+            "gdn_tree_ms": gdn_ms, "gdn_tree_bytes": gdn_bytes, "gdn_tree_workload": gdn_name,
+            "gdn_tree_hbm_frac": gdn_bytes / (gdn_ms * 1e-3) / (peaks["hbm_gbs"] * 1e9),
+            "gdn_tree_note": "tv_gdn_tree (Gated DeltaNet layer verified over the tree without rollback), its own "
+                             "graph; a layer of the hybrid model's verification pass, not part of this attention "
+                             "step; the dependent chain along each root path bounds it, not HBM",
             "kv_commit_note": "tv_kv_commit of the accepted branch, its own graph after the timed steps; not part "
                               "of the step (it rewrites the caches); latency-bound (a few KB moved)",
         },

@@ -21,6 +21,10 @@
  *           log-probability as the branch score, best-first expansion to a budget.
  *   [TfM-2t] DFlash-TfM summary, §2 "Construcción de Árboles": the top w
  *           candidates of the heap are expanded together (ceil(B/w) rounds).
+ *   [TfM-3g] DFlash-TfM summary, §3 "Verificación de Árboles sin Rollback": the
+ *           Gated DeltaNet state update, the masked triangular solve
+ *           (I + X) U = beta V over the topologically ordered tree, and the state
+ *           committed only once the accepted branch is known.
  *   [JF-4]  JETFLOW summary, §3 item 2 and §4: accepted tokens (tau) and
  *           longer accepted prefixes; the pages give no acceptance rule, so
  *           the greedy rule below is this library's reading.
@@ -214,6 +218,43 @@ TV_API int32_t tv_accept(const uint16_t *logits_d, int32_t V, const int32_t *dra
 TV_API int32_t tv_build_tree(const float *logp_d, const int32_t *tokens_d, int32_t nb, int32_t Dmax, int32_t K,
                              int32_t B, int32_t w, int32_t *parent_d, int32_t *token_d, float *score_d,
                              int32_t *dev_status_d, void *stream);
+
+/*
+ * Rollback-free tree verification through a Gated DeltaNet layer  [TfM-3g]
+ *
+ *   Per sequence b and head h, with the committed state S0[b][h] (D x D: rows
+ *   indexed by the key dimension, columns by the value dimension), every tree
+ *   node i gets the output of the state its own root path builds, without
+ *   touching S0:
+ *     S_i = alpha_i (I - beta_i k_i k_i^T) S_parent(i) + beta_i k_i v_i^T
+ *     (S_parent(root) = S0),      o_i = S_i^T q_i.
+ *   Computed as the masked triangular solve over the tree: with gamma_i the
+ *   product of alpha on i's root path, (I + X) U = beta (V - gamma K S0) with
+ *   X_ij = beta_i (gamma_i/gamma_j) k_i.k_j for j a strict ancestor of i, and
+ *   O = gamma Q S0 + Y U with Y_ij = (gamma_i/gamma_j) q_i.k_j for j an ancestor
+ *   of i or i itself.
+ *
+ *   q_d, k_d, v_d   bf16 [nb*B][H][D], 16-byte aligned (GDN layers normalise q, k)
+ *   alpha_d, beta_d fp32 [nb*B][H]
+ *   S0_d            fp32 [nb][H][D][D], 16-byte aligned
+ *   parent_d        int32 [nb][B], topologically ordered (as tv_build_mask takes it)
+ *   O_d             fp32 [nb*B][H][D] (out), 16-byte aligned
+ *   workspace_d     >= tv_gdn_tree_workspace_size(nb, B, H, D) bytes, 16-byte
+ *                   aligned: K S0 and Q S0 (fp32); concurrent calls need their own
+ *   Shapes: D = 128, 1 <= B <= 256.
+ * Two kernel launches, the first a programmatic dependent of the previous kernel
+ * on the stream (it waits for it before reading anything).  A parent array that is
+ * not topological writes TV_ERR_NOT_TOPOLOGICAL to dev_status_d (outputs
+ * unspecified); an internal wait that runs out writes TV_ERR_TIMEOUT.
+ * Returns TV_OK (nb == 0 launches nothing), TV_ERR_INVALID_ARG (null or misaligned
+ * pointer, nb or H < 1, workspace too small), TV_ERR_UNSUPPORTED_SHAPE or TV_ERR_CUDA.
+ * tv_gdn_tree_workspace_size returns 0 for an unsupported shape.
+ */
+TV_API size_t tv_gdn_tree_workspace_size(int32_t nb, int32_t B, int32_t H, int32_t D);
+TV_API int32_t tv_gdn_tree(const uint16_t *q_d, const uint16_t *k_d, const uint16_t *v_d, const float *alpha_d,
+                           const float *beta_d, const float *S0_d, const int32_t *parent_d, int32_t nb, int32_t B,
+                           int32_t H, int32_t D, float *O_d, void *workspace_d, size_t workspace_bytes,
+                           int32_t *dev_status_d, void *stream);
 
 /*
  * Commit of the accepted branch  [TfM-3] (the pages commit state once the

@@ -147,6 +147,27 @@ def test_build_tree_argument_checks(L):
     assert call(D=1, K=8, B=9, nb=0) == 0 and call(D=2, K=2, B=8, nb=0) == 1
 
 
+def test_gdn_tree_argument_checks(L):
+    P = C.c_void_p
+    base = dict(q=P(FAKE), k=P(FAKE), v=P(FAKE), a=P(FAKE), b=P(FAKE), s=P(FAKE), par=P(FAKE), nb=1, B=128, H=32, D=128,
+                o=P(FAKE), ws=P(FAKE), wsb=1 << 30)
+
+    def call(**kw):
+        d = dict(base)
+        d.update(kw)
+        return L.tv_gdn_tree(d["q"], d["k"], d["v"], d["a"], d["b"], d["s"], d["par"], d["nb"], d["B"], d["H"], d["D"],
+                             d["o"], d["ws"], d["wsb"], None, None)
+
+    assert call(nb=0) == 0
+    assert call(nb=-1) == 1 and call(H=0) == 1
+    assert call(B=0) == 3 and call(B=257) == 3 and call(D=64) == 3
+    assert call(q=None) == 1 and call(s=None) == 1 and call(o=None) == 1
+    assert call(k=P(FAKE + 8)) == 1 and call(s=P(FAKE + 4)) == 1 and call(a=P(FAKE + 2)) == 1
+    assert call(ws=None) == 1 and call(wsb=16) == 1
+    assert L.tv_gdn_tree_workspace_size(1, 128, 32, 128) == 2 * 128 * 32 * 128 * 4
+    assert L.tv_gdn_tree_workspace_size(1, 128, 32, 64) == 0
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "_lib", None)
     monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "missing.so"))

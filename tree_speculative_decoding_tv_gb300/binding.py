@@ -24,7 +24,7 @@ TV_ERR_TIMEOUT = 5
 TV_ERR_UNIMPLEMENTED = 6
 
 EXPORTED = ("tv_status_str", "tv_version", "tv_build_mask", "tv_attn_workspace_size", "tv_attn",
-            "tv_accept_workspace_size", "tv_accept", "tv_accept_noalloc", "tv_kv_commit", "tv_build_tree")
+            "tv_accept_workspace_size", "tv_accept", "tv_accept_noalloc", "tv_kv_commit", "tv_build_tree", "tv_gdn_tree_workspace_size", "tv_gdn_tree")
 NOALLOC_MAX_ROWS = 8192  # TV_ACCEPT_NOALLOC_MAX_ROWS
 
 
@@ -77,6 +77,10 @@ def lib() -> C.CDLL:
         L.tv_kv_commit.restype = I
         L.tv_build_tree.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P]
         L.tv_build_tree.restype = I
+        L.tv_gdn_tree_workspace_size.argtypes = [I, I, I, I]
+        L.tv_gdn_tree_workspace_size.restype = C.c_size_t
+        L.tv_gdn_tree.argtypes = [P, P, P, P, P, P, P, I, I, I, I, P, P, C.c_size_t, P, P]
+        L.tv_gdn_tree.restype = I
         _lib = L
     return _lib
 
@@ -222,3 +226,19 @@ def build_tree(logp, tokens, B, w=1, out=None, status=None, stream=None):
                              _stream(stream))
     _check(rc, "tv_build_tree")
     return parent, token, score
+
+
+def gdn_tree(q, k, v, alpha, beta, S0, parent, out=None, workspace=None, status=None, stream=None):
+    """tv_gdn_tree: q/k/v bf16 [nb*B][H][D], alpha/beta fp32 [nb*B][H], S0 fp32 [nb][H][D][D],
+    parent int32 [nb][B] (cuda) -> O fp32 [nb*B][H][D]."""
+    nb, B = parent.shape
+    H, D = q.shape[1], q.shape[2]
+    if out is None:
+        out = torch.empty((nb * B, H, D), dtype=torch.float32, device=q.device)
+    need = int(lib().tv_gdn_tree_workspace_size(nb, B, H, D))
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    rc = lib().tv_gdn_tree(_p(q), _p(k), _p(v), _p(alpha), _p(beta), _p(S0), _p(parent), nb, B, H, D, _p(out),
+                           _p(workspace), workspace.numel() * workspace.element_size(), _p(status), _stream(stream))
+    _check(rc, "tv_gdn_tree")
+    return out

@@ -49,6 +49,13 @@ cudaError_t launch_accept_noalloc(const uint16_t *logits, int V, const int32_t *
 cudaError_t launch_build_tree(const float *logp, const int32_t *tok, int nb, int Dmax, int K, int B, int w,
                               int32_t *parent, int32_t *token, float *score, int32_t *status, cudaStream_t stream);
 
+// Gated DeltaNet tree verification: dense K S0 / Q S0 products, then the sparse
+// masked solve and outputs (one CTA per (sequence, head)).
+size_t gdn_workspace_bytes(int nb, int B, int H);
+cudaError_t launch_gdn_tree(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
+                            const float *beta, const float *S0, const int32_t *parent, int nb, int B, int H, float *O,
+                            void *workspace, int32_t *status, cudaStream_t stream);
+
 // Commit of the accepted branch's K/V (one CTA per (sequence, kv head)).
 cudaError_t launch_kv_commit(uint16_t *k_cache, uint16_t *v_cache, const int32_t *block_table,
                              const int32_t *prefix_lens, const int32_t *n_acc, const int32_t *path, int nb, int B,
