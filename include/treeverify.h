@@ -240,9 +240,12 @@ TV_API int32_t tv_build_tree(const float *logp_d, const int32_t *tokens_d, int32
  *   parent_d        int32 [nb][B], topologically ordered (as tv_build_mask takes it)
  *   O_d             fp32 [nb*B][H][D] (out), 16-byte aligned
  *   workspace_d     >= tv_gdn_tree_workspace_size(nb, B, H, D) bytes, 16-byte
- *                   aligned: K S0 and Q S0 (fp32); concurrent calls need their own
+ *                   aligned: per (sequence, head) a B x B table of 16-byte ancestor
+ *                   records, plus (B > 128) two fp32 [B][D] row blocks; concurrent
+ *                   calls need their own
  *   Shapes: D = 128, 1 <= B <= 256.
- * Two kernel launches, the first a programmatic dependent of the previous kernel
+ * One kernel launch per call (one CTA per (sequence, head); tensor cores form
+ * K S0, Q S0 and the Gram blocks), a programmatic dependent of the previous kernel
  * on the stream (it waits for it before reading anything).  A parent array that is
  * not topological writes TV_ERR_NOT_TOPOLOGICAL to dev_status_d (outputs
  * unspecified); an internal wait that runs out writes TV_ERR_TIMEOUT.

@@ -8,22 +8,35 @@
 // With gamma_i the product of alpha over i's root path (i included) and
 // r_ij = gamma_i / gamma_j, that state is S_i = gamma_i S0 + sum_{j in path(i)}
 // r_ij k_j u_j^T, where
-//   u_i = beta_i (v_i - gamma_i S0^T k_i - sum_{j strict ancestor} r_ij (k_i . k_j) u_j)
+//   u_i = beta_i (v_i - gamma_i S0^T k_i) - sum_{j strict ancestor} beta_i r_ij (k_i . k_j) u_j
 //   o_i = gamma_i S0^T q_i + sum_{j in path(i)} r_ij (q_i . k_j) u_j.
 // (X_ij = beta_i r_ij k_i.k_j and Y_ij = r_ij q_i.k_j are the pages' interaction
 // matrices, restricted to ancestors by the tree mask.)
 //
-// GPU form, two kernels on the caller's stream:
-//   1. gdn_state_products_kernel: the dense part, K S0 and Q S0 (B x D x D each),
-//      one CTA per 32 tree rows of a (sequence, head): S0 staged in shared memory,
-//      a 4 x 4 register tile per thread, fp32 into the workspace.
-//   2. gdn_tree_solve_kernel: the sparse part, one CTA per (sequence, head), one
-//      warp per node in dataflow order: node i waits (bounded) for its parent's
-//      done flag, walks up its ancestors forming k_i.k_j and q_i.k_j with warp
-//      reductions and the decay ratio r_ij as a running product of alphas (no
-//      division), keeps u_i in shared memory for its descendants and writes o_i.
-//      Warps take nodes in index order, so the smallest unfinished node can always
-//      run: the wait always ends.
+// GPU form: one fused kernel, one CTA per (sequence, head), 16 warps.
+//   1. Stage, with every global load issued at once: the K and Q rows (cp.async)
+//      as K-major 128-byte-swizzled bf16 tiles, the v rows (B <= 128), S0 (through
+//      registers, split into bf16 hi + lo parts, S0 = hi + lo to ~2^-17, as MN-major
+//      swizzled tiles), the parent array (validated), and a walk up each node's root
+//      path that sets its ancestor bits and writes, per ancestor j (slot = distance
+//      to i - 1), the record (j, r_ij): r_ij is the running product of the alphas
+//      passed, and gamma_i the product over the whole path.
+//   2. Tensor cores (tcgen05, fp32 accumulators in TMEM): the Gram blocks K K^T and
+//      Q K^T (committed first, so the epilogue starts on them early), then K S0 and
+//      Q S0 (each as K hi + K lo, so fp32-accurate), 128 nodes per M tile (two tiles
+//      and three passes for B > 128, so a pass never needs more than the 512 TMEM
+//      columns).
+//   3. Epilogue, all warps (warp w reads TMEM lanes 32 (w % 4).. and columns
+//      32 (w / 4)..): r_i = beta_i (v_i - gamma_i (K S0)_i) and o0_i = gamma_i (Q S0)_i
+//      per node, and, for each ancestor j of i (its bit in i's mask; its slot is the
+//      count of mask bits above it), the pair (k_i.k_j, q_i.k_j) into j's record
+//      (the first 24 records of a node in shared memory when B <= 128, the rest in
+//      the workspace).
+//   4. Solve, warp per node in dataflow order: node i's r_i and o0_i rows are loaded
+//      (the warp's next node's while this one runs), node i waits (bounded, asleep on
+//      an mbarrier) until its parent's u row is written, then each ancestor costs one broadcast record load, one
+//      u-row load and a few fused multiply-adds (four ancestors in flight at a time).  Warps take nodes in index order, so the
+//      smallest unfinished node can always run: every wait ends.
 #include <cuda_runtime.h>
 
 #include "tv_device.cuh"
@@ -33,195 +46,445 @@ namespace tv {
 
 constexpr int kGdnD = 128;
 constexpr int kGdnMaxB = 256;
-constexpr int kGdnRows = 32;      // tree rows per CTA in the dense kernel
-constexpr int kGdnThreads = 256;  // both kernels
+constexpr int kGdnThreads = 512;
+constexpr int kGdnWarps = kGdnThreads / 32;
+constexpr uint32_t kGdnTile = 128 * 128 * 2;  // one 128 x 128 bf16 operand tile
+constexpr uint32_t kGdnHalf = kGdnTile / 2;   // one 64-column (128-byte) swizzle block of it
+constexpr int kGdnMaskWords = kGdnMaxB / 32;
+constexpr uint32_t kGdnRowBytes = kGdnD * 4;  // an fp32 row (r, u, o0)
+constexpr int kGdnSmemSlots = 24;             // records per node kept in shared memory (B <= 128)
+constexpr uint32_t kGdnTmemCols = 512;
+// TMEM columns of one pass: K S0, Q S0, then the K K^T and Q K^T blocks
+constexpr uint32_t kColKS = 0, kColQS = 128, kColKK = 256, kColQK = 384;
+constexpr uint32_t kIdescS = umma_idesc_bf16(128, 128, 1);  // B = S0 part, MN-major
+constexpr uint32_t kIdescG = umma_idesc_bf16(128, 128, 0);  // B = K tile, K-major
 
-__device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+// One ancestor j of a node i: its index, the decay ratio r_ij (written by the root
+// walk) and the two Gram entries k_i.k_j, q_i.k_j (written by the epilogue).
+struct __align__(16) GdnRec {
+    int32_t j;
+    float r, kk, qk;
+};
 
-// KS0[i][c] = sum_r k_i[r] S0[r][c], QS0 likewise, for kGdnRows rows of one (b, h).
-__global__ void __launch_bounds__(kGdnThreads) gdn_state_products_kernel(const uint16_t *__restrict__ q,
-                                                                         const uint16_t *__restrict__ k,
-                                                                         const float *__restrict__ S0, int B, int H,
-                                                                         float *__restrict__ ks0,
-                                                                         float *__restrict__ qs0)
+struct GdnSmem {
+    uint32_t k, q, s_hi, s_lo, tiles_end;
+    uint32_t recs, v;  // B <= 128 only: records [128][kGdnSmemSlots], v rows [128][D] bf16
+    uint32_t done, parent, alpha, beta, gamma, depth, yii, mask, total;
+};
+
+__host__ __device__ inline GdnSmem gdn_smem_layout(int B)
 {
-    extern __shared__ float4 gdn_smem[];
-    float *s_S = reinterpret_cast<float *>(gdn_smem);   // [D][D]
-    float *s_kq = s_S + kGdnD * kGdnD;                  // [2][kGdnRows][D] (k rows, then q rows)
-    const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
-    const int row0 = blk * kGdnRows;
-    pdl_wait_primary();
-    pdl_launch_dependents();
-    const float4 *src = reinterpret_cast<const float4 *>(S0 + ((size_t)b * H + h) * kGdnD * kGdnD);
-    for (int t = tid; t < kGdnD * kGdnD / 4; t += kGdnThreads) reinterpret_cast<float4 *>(s_S)[t] = src[t];
-    for (int t = tid; t < 2 * kGdnRows * kGdnD; t += kGdnThreads) {
-        const int which = t / (kGdnRows * kGdnD), rem = t - which * kGdnRows * kGdnD;
-        const int r = rem / kGdnD, d = rem - r * kGdnD;
-        const int i = row0 + r;
-        float x = 0.f;
-        if (i < B) x = bf16_to_f32((which ? q : k)[(((size_t)b * B + i) * H + h) * kGdnD + d]);
-        s_kq[t] = x;
+    GdnSmem L;
+    const uint32_t T = (uint32_t)(B + 127) / 128;
+    L.k = 0;
+    L.q = T * kGdnTile;
+    L.s_hi = 2 * T * kGdnTile;
+    L.s_lo = L.s_hi + kGdnTile;
+    L.tiles_end = L.s_lo + kGdnTile;
+    uint32_t o = L.tiles_end;
+    L.recs = L.v = 0;
+    if (B <= 128) {
+        L.recs = o;
+        o += 128u * kGdnSmemSlots * 16u;
+        L.v = o;
+        o += 128u * kGdnD * 2u;
     }
-    __syncthreads();
-    // thread: columns 4*(tid % 32) .. +3, rows 4*(tid / 32) .. +3 of both products
-    const int c0 = 4 * (tid & 31), r0 = 4 * (tid >> 5);
-    float acc[2][4][4];
-#pragma unroll
-    for (int m = 0; m < 2; ++m)
-#pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) acc[m][a][c] = 0.f;
-#pragma unroll 4
-    for (int r = 0; r < kGdnD; ++r) {
-        const float4 s = reinterpret_cast<const float4 *>(s_S + r * kGdnD)[c0 / 4];
-#pragma unroll
-        for (int m = 0; m < 2; ++m)
-#pragma unroll
-            for (int a = 0; a < 4; ++a) {
-                const float x = s_kq[(m * kGdnRows + r0 + a) * kGdnD + r];
-                acc[m][a][0] = fmaf(x, s.x, acc[m][a][0]);
-                acc[m][a][1] = fmaf(x, s.y, acc[m][a][1]);
-                acc[m][a][2] = fmaf(x, s.z, acc[m][a][2]);
-                acc[m][a][3] = fmaf(x, s.w, acc[m][a][3]);
-            }
-    }
-#pragma unroll
-    for (int m = 0; m < 2; ++m)
-#pragma unroll
-        for (int a = 0; a < 4; ++a) {
-            const int i = row0 + r0 + a;
-            if (i < B) {
-                float *dst = (m ? qs0 : ks0) + (((size_t)b * B + i) * H + h) * kGdnD + c0;
-                *reinterpret_cast<float4 *>(dst) = make_float4(acc[m][a][0], acc[m][a][1], acc[m][a][2], acc[m][a][3]);
-            }
-        }
+    const uint32_t a = 4u * (uint32_t)B;
+    L.done = o; o += 2 * a;  // one mbarrier per node
+    L.parent = o; o += a;
+    L.alpha = o; o += a;
+    L.beta = o; o += a;
+    L.gamma = o; o += a;
+    L.depth = o; o += a;
+    L.yii = o; o += a;
+    L.mask = o; o += 4u * kGdnMaskWords * (uint32_t)B;
+    L.total = o;
+    return L;
 }
 
-__device__ __forceinline__ float warp_sum(float v)
+// byte offset of logical 16-byte chunk c (0..31) of fp32 row i: chunks swizzled by (i & 7)
+__device__ __forceinline__ uint32_t row_chunk(int i, int c) { return (uint32_t)i * kGdnRowBytes + ((c ^ (i & 7)) << 4); }
+
+// round-to-nearest bf16 bits of x
+__device__ __forceinline__ uint32_t bf16_bits(float x)
 {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
+    uint16_t r;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(x));
+    return r;
 }
 
-__global__ void __launch_bounds__(kGdnThreads) gdn_tree_solve_kernel(
+__device__ __forceinline__ void st_shared_v2(uint32_t addr, uint32_t a, uint32_t b)
+{
+    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+
+// 16-byte global -> shared copy, zero-filled when !valid (nothing is read then)
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ void fma_row(float4 &u, float4 &o, float x, float y, const float4 &uj)
+{
+    u.x -= x * uj.x; u.y -= x * uj.y; u.z -= x * uj.z; u.w -= x * uj.w;
+    o.x += y * uj.x; o.y += y * uj.y; o.z += y * uj.z; o.w += y * uj.w;
+}
+
+// record slot `slot` of node i: the first kGdnSmemSlots in shared memory when B <= 128
+__device__ __forceinline__ GdnRec *rec_at(GdnRec *s_recs, GdnRec *g_recs, bool small, int B, int i, int slot)
+{
+    return (small && slot < kGdnSmemSlots) ? s_recs + i * kGdnSmemSlots + slot : g_recs + (size_t)i * B + slot;
+}
+
+__global__ void __launch_bounds__(kGdnThreads, 1) gdn_tree_kernel(
     const uint16_t *__restrict__ q, const uint16_t *__restrict__ k, const uint16_t *__restrict__ v,
-    const float *__restrict__ alpha, const float *__restrict__ beta, const int32_t *__restrict__ parent,
-    const float *__restrict__ ks0, const float *__restrict__ qs0, int B, int H, float *__restrict__ O,
-    int32_t *status)
+    const float *__restrict__ alpha, const float *__restrict__ beta, const float *__restrict__ S0,
+    const int32_t *__restrict__ parent, int B, int H, float *__restrict__ O, void *__restrict__ ws, int32_t *status)
 {
-    extern __shared__ float4 gdn_smem[];
-    float *s_u = reinterpret_cast<float *>(gdn_smem);                 // [B][D] u_i
-    uint16_t *s_k = reinterpret_cast<uint16_t *>(s_u + (size_t)B * kGdnD);  // [B][D] k_i (bf16)
-    float *s_gamma = reinterpret_cast<float *>(s_k + (size_t)B * kGdnD);    // [B]
-    float *s_alpha = s_gamma + B;                                            // [B]
-    int *s_parent = reinterpret_cast<int *>(s_alpha + B);                   // [B]
-    volatile int *s_done = s_parent + B;                                     // [B]
+    extern __shared__ uint8_t gdn_raw[];
+    __shared__ __align__(8) uint64_t s_bar[2];  // Gram MMAs done, S0 MMAs done
+    __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
-    const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const int nwarps = kGdnThreads / 32;
+    const uint32_t raw = smem_u32(gdn_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gb = gdn_raw + (base - raw);
+    const GdnSmem L = gdn_smem_layout(B);
+    int *s_parent = reinterpret_cast<int *>(gb + L.parent);
+    float *s_alpha = reinterpret_cast<float *>(gb + L.alpha);
+    float *s_beta = reinterpret_cast<float *>(gb + L.beta);
+    float *s_gamma = reinterpret_cast<float *>(gb + L.gamma);
+    int *s_depth = reinterpret_cast<int *>(gb + L.depth);
+    float *s_yii = reinterpret_cast<float *>(gb + L.yii);
+    const uint32_t done_bar = base + L.done;  // node i's mbarrier at done_bar + 8 i: phase 0 completes when u_i is written
+    uint32_t *s_mask = reinterpret_cast<uint32_t *>(gb + L.mask);
 
-    // inputs that do not come from the dense kernel
+    const int h = blockIdx.x, b = blockIdx.y, nb = gridDim.y;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int T = (B + 127) >> 7;
+    const bool small = B <= 128;  // one M tile: r / u and o0 rows, records and v rows fit in shared memory
+    const size_t bh = (size_t)b * H + h;
+    // workspace: records [nb][H][B][B]; for B > 128 also r and o0 rows [nb][H][B][D] each
+    GdnRec *g_recs = reinterpret_cast<GdnRec *>(ws) + bh * B * B;
+    GdnRec *s_recs = reinterpret_cast<GdnRec *>(gb + L.recs);
+    float *g_rows = reinterpret_cast<float *>(reinterpret_cast<GdnRec *>(ws) + (size_t)nb * H * B * B);
+    uint8_t *r_rows = small ? gb : reinterpret_cast<uint8_t *>(g_rows + bh * B * kGdnD);
+    uint8_t *o0_rows = small ? gb + 128 * kGdnRowBytes
+                             : reinterpret_cast<uint8_t *>(g_rows + ((size_t)nb * H + bh) * B * kGdnD);
+    const uint32_t bar_g = smem_u32(&s_bar[0]), bar_s = smem_u32(&s_bar[1]);
+
+    pdl_wait_primary();  // every input may come from the previous kernel
+    pdl_launch_dependents();
+
+    // ---- every global load at once: the tree first, then K, Q (and v) rows by cp.async
+    // and S0 into registers
+    int pv[2] = {0, 0};
+    float av[2] = {0.f, 0.f}, bv[2] = {0.f, 0.f};
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int i = tid + e * kGdnThreads;
+        if (i < B) {
+            const size_t row = ((size_t)b * B + i) * H + h;
+            pv[e] = parent[(size_t)b * B + i];
+            av[e] = alpha[row];
+            bv[e] = beta[row];
+        }
+    }
+    const int n16 = T * 128 * 16;  // 16-byte chunks per operand tile set
+    for (int idx = tid; idx < 2 * n16; idx += kGdnThreads) {
+        const int which = idx >= n16, r = idx - which * n16, i = r >> 4, c = r & 15;
+        const uint32_t dst = base + (which ? L.q : L.k) + (uint32_t)(i >> 7) * kGdnTile + (uint32_t)(c >> 3) * kGdnHalf +
+                             (uint32_t)(i & 127) * 128 + ((uint32_t)((c & 7) ^ (i & 7)) << 4);
+        const uint16_t *src = (which ? q : k) + (((size_t)b * B + min(i, B - 1)) * H + h) * kGdnD + c * 8;
+        cp_async16(dst, src, i < B);
+    }
+    if (small) {  // v rows [i][16 chunks], chunks swizzled by (i & 7)
+        for (int idx = tid; idx < B * 16; idx += kGdnThreads) {
+            const int i = idx >> 4, c = idx & 15;
+            cp_async16(base + L.v + (uint32_t)i * 256 + ((uint32_t)(c ^ (i & 7)) << 4),
+                       v + (((size_t)b * B + i) * H + h) * kGdnD + c * 8, true);
+        }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    constexpr int kPer = kGdnD * kGdnD / 4 / kGdnThreads;  // S0: 8 float4 per thread
+    float4 sv[kPer];
+    {
+        const float4 *src = reinterpret_cast<const float4 *>(S0 + bh * kGdnD * kGdnD);
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) sv[u] = src[tid + u * kGdnThreads];
+    }
+
     bool bad = false;
-    for (int i = tid; i < B; i += kGdnThreads) {
-        const int p = parent[(size_t)b * B + i];
-        bad |= (i == 0) ? (p != -1) : (p < 0 || p >= i);
-        s_parent[i] = p;
-        s_alpha[i] = alpha[((size_t)b * B + i) * H + h];
-        s_done[i] = 0;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int i = tid + e * kGdnThreads;
+        if (i < B) {
+            bad |= (i == 0) ? (pv[e] != -1) : (pv[e] < 0 || pv[e] >= i);
+            s_parent[i] = pv[e];
+            s_alpha[i] = av[e];
+            s_beta[i] = bv[e];
+            mbar_init(done_bar + 8u * (uint32_t)i, 1);
+        }
     }
-    for (int t = tid; t < B * kGdnD / 8; t += kGdnThreads) {
-        const int i = t / (kGdnD / 8), d8 = t - i * (kGdnD / 8);
-        reinterpret_cast<uint4 *>(s_k)[t] =
-            reinterpret_cast<const uint4 *>(k + (((size_t)b * B + i) * H + h) * kGdnD)[d8];
+    if (tid == 0) {
+        s_abort = 0;
+        mbar_init(bar_g, 1);
+        mbar_init(bar_s, 1);
     }
-    if (tid == 0) s_abort = 0;
-    const bool any_bad = __syncthreads_or(bad);
-    pdl_wait_primary();  // K S0 and Q S0 come from the dense kernel (waited even on bad input)
-    if (any_bad) {
+    fence_mbar_init();
+    if (__syncthreads_or(bad)) {
+        cp_async_wait_all();
         if (tid == 0) report_status(status, TV_ERR_NOT_TOPOLOGICAL);
         return;
     }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(&s_tmem), kGdnTmemCols);
+        tmem_relinquish();
+    }
 
-    for (int i = wid; i < B; i += nwarps) {
-        const int p = s_parent[i];
-        // wait (bounded) until the parent is done: then all ancestors are
-        if (p >= 0) {
-            const uint64_t t0 = global_timer_ns();
-            bool ok = true;
-            for (uint32_t it = 0; s_done[p] == 0; ++it) {
-                if ((it & 63) == 63 && (s_abort || global_timer_ns() - t0 > kWaitLimitNs)) {
-                    ok = false;
-                    break;
-                }
-            }
-            if (!__all_sync(0xffffffffu, ok)) {
-                if (lane == 0) {
-                    s_abort = 1;
-                    report_status(status, TV_ERR_TIMEOUT);
-                }
-                break;
-            }
-            __threadfence_block();  // the ancestors' u rows are visible from here
-        }
-        const size_t row = ((size_t)b * B + i) * H + h;
-        const float ai = s_alpha[i], bi = beta[row];
-        const float gi = (p >= 0 ? s_gamma[p] : 1.f) * ai;
-        // lane l holds columns 4l .. 4l+3 of this node's vectors
-        float ki[4], qi[4], acc_u[4] = {0.f, 0.f, 0.f, 0.f}, acc_o[4] = {0.f, 0.f, 0.f, 0.f};
-        {
-            const uint2 kk = reinterpret_cast<const uint2 *>(s_k + (size_t)i * kGdnD)[lane];
-            const uint2 qq = reinterpret_cast<const uint2 *>(q + row * kGdnD)[lane];
-            ki[0] = bf16_to_f32(kk.x & 0xFFFFu); ki[1] = bf16_to_f32(kk.x >> 16);
-            ki[2] = bf16_to_f32(kk.y & 0xFFFFu); ki[3] = bf16_to_f32(kk.y >> 16);
-            qi[0] = bf16_to_f32(qq.x & 0xFFFFu); qi[1] = bf16_to_f32(qq.x >> 16);
-            qi[2] = bf16_to_f32(qq.y & 0xFFFFu); qi[3] = bf16_to_f32(qq.y >> 16);
-        }
-        // strict ancestors j = p, parent(p), ...: r = gamma_i / gamma_j as a running product
-        float r = ai;
-        for (int j = p; j >= 0; j = s_parent[j]) {
-            const uint2 kk = reinterpret_cast<const uint2 *>(s_k + (size_t)j * kGdnD)[lane];
-            const float k0 = bf16_to_f32(kk.x & 0xFFFFu), k1 = bf16_to_f32(kk.x >> 16);
-            const float k2 = bf16_to_f32(kk.y & 0xFFFFu), k3 = bf16_to_f32(kk.y >> 16);
-            const float g = warp_sum(ki[0] * k0 + ki[1] * k1 + ki[2] * k2 + ki[3] * k3) * r;
-            const float a = warp_sum(qi[0] * k0 + qi[1] * k1 + qi[2] * k2 + qi[3] * k3) * r;
-            const float4 uj = reinterpret_cast<const float4 *>(s_u + (size_t)j * kGdnD)[lane];
-            acc_u[0] = fmaf(g, uj.x, acc_u[0]); acc_u[1] = fmaf(g, uj.y, acc_u[1]);
-            acc_u[2] = fmaf(g, uj.z, acc_u[2]); acc_u[3] = fmaf(g, uj.w, acc_u[3]);
-            acc_o[0] = fmaf(a, uj.x, acc_o[0]); acc_o[1] = fmaf(a, uj.y, acc_o[1]);
-            acc_o[2] = fmaf(a, uj.z, acc_o[2]); acc_o[3] = fmaf(a, uj.w, acc_o[3]);
+    // root paths: ancestor bits, records (j, r_ij) in slot order, depth and gamma
+    for (int i = tid; i < B; i += kGdnThreads) {
+        uint32_t *m = s_mask + i * kGdnMaskWords;
+#pragma unroll
+        for (int w = 0; w < kGdnMaskWords; ++w) m[w] = 0;
+        m[i >> 5] = 1u << (i & 31);
+        float r = s_alpha[i];
+        int slot = 0;
+        for (int j = s_parent[i]; j >= 0; j = s_parent[j], ++slot) {
+            m[j >> 5] |= 1u << (j & 31);
+            GdnRec *rc = rec_at(s_recs, g_recs, small, B, i, slot);
+            rc->j = j;
+            rc->r = r;
             r *= s_alpha[j];
         }
-        const float4 ks = reinterpret_cast<const float4 *>(ks0 + row * kGdnD)[lane];
-        const float4 qs = reinterpret_cast<const float4 *>(qs0 + row * kGdnD)[lane];
-        const uint2 vv = reinterpret_cast<const uint2 *>(v + row * kGdnD)[lane];
-        const float vi[4] = {bf16_to_f32(vv.x & 0xFFFFu), bf16_to_f32(vv.x >> 16), bf16_to_f32(vv.y & 0xFFFFu),
-                             bf16_to_f32(vv.y >> 16)};
-        const float ksv[4] = {ks.x, ks.y, ks.z, ks.w}, qsv[4] = {qs.x, qs.y, qs.z, qs.w};
-        float ui[4];
+        s_depth[i] = slot;
+        s_gamma[i] = r;
+    }
+    // S0 [key r][value c] -> hi and lo bf16 parts, MN-major 128B-swizzled (key rows of 64 values)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) ui[c] = bi * (vi[c] - gi * ksv[c] - acc_u[c]);
-        const float aii = warp_sum(qi[0] * ki[0] + qi[1] * ki[1] + qi[2] * ki[2] + qi[3] * ki[3]);
-        reinterpret_cast<float4 *>(s_u + (size_t)i * kGdnD)[lane] = make_float4(ui[0], ui[1], ui[2], ui[3]);
-        if (lane == 0) s_gamma[i] = gi;
-        float4 o;
-        o.x = gi * qsv[0] + acc_o[0] + aii * ui[0];
-        o.y = gi * qsv[1] + acc_o[1] + aii * ui[1];
-        o.z = gi * qsv[2] + acc_o[2] + aii * ui[2];
-        o.w = gi * qsv[3] + acc_o[3] + aii * ui[3];
-        reinterpret_cast<float4 *>(O + row * kGdnD)[lane] = o;
-        __threadfence_block();  // every lane's u_i (and gamma_i) before the done flag
+    for (int u = 0; u < kPer; ++u) {
+        const int idx = tid + u * kGdnThreads, r = idx >> 5, c = (idx & 31) * 4;
+        const float x[4] = {sv[u].x, sv[u].y, sv[u].z, sv[u].w};
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            hi[e] = bf16_bits(x[e]);
+            lo[e] = bf16_bits(x[e] - __uint_as_float(hi[e] << 16));
+        }
+        const uint32_t off = (uint32_t)(c >> 6) * kGdnHalf + (uint32_t)r * 128 +
+                             ((uint32_t)(((c & 63) >> 3) ^ (r & 7)) << 4) + (uint32_t)(c & 7) * 2;
+        st_shared_v2(base + L.s_hi + off, hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16));
+        st_shared_v2(base + L.s_lo + off, lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
+    }
+    cp_async_wait_all();
+    fence_proxy_async_smem();  // the tensor core reads what these threads wrote
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    // ---- passes: (M tile m, with K S0 / Q S0?, Gram column block n)
+    const int npass = T == 1 ? 1 : 3;
+    const int quarter = warp & 3, chunk = warp >> 2;
+    const uint32_t t_lane = tmem + ((uint32_t)(32 * quarter) << 16);
+    for (int p = 0; p < npass; ++p) {
+        const int m = p == 0 ? 0 : 1, n = p == 2 ? 1 : 0;
+        const bool has_s = p < 2;
+        if (tid == 0) {
+            const uint32_t kA = base + L.k + (uint32_t)m * kGdnTile, qA = base + L.q + (uint32_t)m * kGdnTile;
+            const uint32_t kB = base + L.k + (uint32_t)n * kGdnTile;
+#pragma unroll
+            for (int kk = 0; kk < kGdnD / 16; ++kk) {
+                const uint32_t off = (uint32_t)(kk >> 2) * kGdnHalf + (uint32_t)(kk & 3) * 32;
+                const uint32_t acc = kk > 0 ? 1u : 0u;
+                umma_bf16_ss(tmem + kColKK, sdesc_kmajor_sw128(kA + off), sdesc_kmajor_sw128(kB + off), kIdescG, acc);
+                umma_bf16_ss(tmem + kColQK, sdesc_kmajor_sw128(qA + off), sdesc_kmajor_sw128(kB + off), kIdescG, acc);
+            }
+            umma_commit(bar_g);
+            if (has_s) {
+#pragma unroll
+                for (int kk = 0; kk < kGdnD / 16; ++kk) {
+                    const uint32_t off = (uint32_t)(kk >> 2) * kGdnHalf + (uint32_t)(kk & 3) * 32;
+                    const uint32_t acc = kk > 0 ? 1u : 0u;
+                    const uint64_t sh = sdesc_mnmajor_sw128(base + L.s_hi + kk * 2048, kGdnHalf);
+                    const uint64_t sl = sdesc_mnmajor_sw128(base + L.s_lo + kk * 2048, kGdnHalf);
+                    umma_bf16_ss(tmem + kColKS, sdesc_kmajor_sw128(kA + off), sh, kIdescS, acc);
+                    umma_bf16_ss(tmem + kColKS, sdesc_kmajor_sw128(kA + off), sl, kIdescS, 1u);
+                    umma_bf16_ss(tmem + kColQS, sdesc_kmajor_sw128(qA + off), sh, kIdescS, acc);
+                    umma_bf16_ss(tmem + kColQS, sdesc_kmajor_sw128(qA + off), sl, kIdescS, 1u);
+                }
+                umma_commit(bar_s);
+            }
+        }
+        const int i = 128 * m + 32 * quarter + lane;  // this thread's TMEM lane = node
+        const bool live = i < B;
+        uint4 vv[4];
+        if (has_s && live) {
+            if (small) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    vv[e] = *reinterpret_cast<const uint4 *>(gb + L.v + i * 256 + (((4 * chunk + e) ^ (i & 7)) << 4));
+            } else {
+                const uint4 *vr =
+                    reinterpret_cast<const uint4 *>(v + (((size_t)b * B + i) * H + h) * kGdnD + 32 * chunk);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) vv[e] = vr[e];
+            }
+        }
+        // Gram entries of node i's ancestors j = 128 n + 32 chunk + t (and of i itself)
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar_g, (uint32_t)(p & 1), &s_abort, status));
+        if (ok) {
+            tc_fence_after();
+            uint32_t x[32], y[32];
+            tmem_ld32(t_lane + kColKK + 32 * chunk, x);
+            tmem_ld32(t_lane + kColQK + 32 * chunk, y);
+            tmem_ld_wait(x);
+            reg_order(y);
+            if (live) {
+                // node i's bits are its ancestors and itself (its highest bit), so ancestor j's
+                // slot (0 = the parent) is the number of bits above j, minus one
+                const int w = 4 * n + chunk;
+                const uint32_t bits = s_mask[i * kGdnMaskWords + w];
+                int above = -1;
+#pragma unroll
+                for (int ww = 0; ww < kGdnMaskWords; ++ww)
+                    if (ww > w) above += __popc(s_mask[i * kGdnMaskWords + ww]);
+#pragma unroll
+                for (int t = 0; t < 32; ++t) {
+                    if ((bits >> t) & 1u) {
+                        const int j = 32 * w + t;
+                        if (j == i) {
+                            s_yii[i] = __uint_as_float(y[t]);
+                        } else {
+                            const int slot = above + __popc(t == 31 ? 0u : bits >> (t + 1));
+                            GdnRec *rc = rec_at(s_recs, g_recs, small, B, i, slot);
+                            rc->kk = __uint_as_float(x[t]);
+                            rc->qk = __uint_as_float(y[t]);
+                        }
+                    }
+                }
+            }
+        }
+        if (ok && has_s) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar_s, (uint32_t)(p & 1), &s_abort, status));
+            if (ok) {
+                tc_fence_after();
+                uint32_t x[32], y[32];
+                tmem_ld32(t_lane + kColKS + 32 * chunk, x);
+                tmem_ld32(t_lane + kColQS + 32 * chunk, y);
+                tmem_ld_wait(x);
+                reg_order(y);
+                if (live) {
+                    const float bi = s_beta[i], gi = s_gamma[i];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {  // 16-byte chunk 8 chunk + e: columns 32 chunk + 4 e ..
+                        const uint4 w = vv[e >> 1];
+                        const uint32_t w0 = (e & 1) ? w.z : w.x, w1 = (e & 1) ? w.w : w.y;
+                        const float vx[4] = {bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1)};
+                        float4 r4, o4;
+                        r4.x = bi * (vx[0] - gi * __uint_as_float(x[4 * e + 0]));
+                        r4.y = bi * (vx[1] - gi * __uint_as_float(x[4 * e + 1]));
+                        r4.z = bi * (vx[2] - gi * __uint_as_float(x[4 * e + 2]));
+                        r4.w = bi * (vx[3] - gi * __uint_as_float(x[4 * e + 3]));
+                        o4.x = gi * __uint_as_float(y[4 * e + 0]);
+                        o4.y = gi * __uint_as_float(y[4 * e + 1]);
+                        o4.z = gi * __uint_as_float(y[4 * e + 2]);
+                        o4.w = gi * __uint_as_float(y[4 * e + 3]);
+                        const uint32_t off = row_chunk(i, 8 * chunk + e);
+                        *reinterpret_cast<float4 *>(r_rows + off) = r4;  // over the finished tiles when small
+                        *reinterpret_cast<float4 *>(o0_rows + off) = o4;
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (s_abort) break;
+    }
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kGdnTmemCols);
+    }
+    if (s_abort) return;
+
+    // ---- solve: warp per node, in index order; the next node's rows load during this one
+    uint8_t *s_u = gb;  // u rows (fp32, swizzled 16-byte chunks) over the finished operand tiles
+    float4 r_n = make_float4(0.f, 0.f, 0.f, 0.f), o_n = r_n;
+    if (warp < B) {
+        r_n = *reinterpret_cast<const float4 *>(r_rows + row_chunk(warp, lane));
+        o_n = *reinterpret_cast<const float4 *>(o0_rows + row_chunk(warp, lane));
+    }
+    for (int i = warp; i < B; i += kGdnWarps) {
+        const int p = s_parent[i], di = s_depth[i];
+        const float bi = s_beta[i], yii = s_yii[i];
+        float4 u = r_n, o = o_n;
+        if (i + kGdnWarps < B) {
+            r_n = *reinterpret_cast<const float4 *>(r_rows + row_chunk(i + kGdnWarps, lane));
+            o_n = *reinterpret_cast<const float4 *>(o0_rows + row_chunk(i + kGdnWarps, lane));
+        }
+        // wait (bounded; the hardware suspends the warp) until the parent's u row is
+        // written: then every ancestor's is, and the acquire makes them visible
+        if (p >= 0 && !__all_sync(0xffffffffu, mbar_wait(done_bar + 8u * (uint32_t)p, 0, &s_abort, status))) break;
+        auto accumulate = [&](const GdnRec *recs_i) {
+            for (int l0 = 0; l0 < di; l0 += 4) {  // four ancestors in flight
+                GdnRec rc[4];
+                float4 uj[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (l0 + e < di) rc[e] = recs_i[l0 + e];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (l0 + e < di) uj[e] = *reinterpret_cast<const float4 *>(s_u + row_chunk(rc[e].j, lane));
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (l0 + e < di) fma_row(u, o, bi * rc[e].r * rc[e].kk, rc[e].r * rc[e].qk, uj[e]);
+            }
+        };
+        if (small && di <= kGdnSmemSlots) {
+            accumulate(s_recs + i * kGdnSmemSlots);
+        } else {  // deep paths: 32 records at a time, one per lane, then broadcast
+            for (int l0 = 0; l0 < di; l0 += 32) {
+                const int n = min(di - l0, 32);
+                GdnRec mine = {0, 0.f, 0.f, 0.f};
+                if (lane < n) mine = *rec_at(s_recs, g_recs, small, B, i, l0 + lane);
+                const float xm = bi * mine.r * mine.kk, ym = mine.r * mine.qk;
+                for (int e0 = 0; e0 < n; e0 += 4) {
+                    int jj[4];
+                    float xx[4], yy[4];
+                    float4 uj[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        jj[e] = __shfl_sync(0xffffffffu, mine.j, e0 + e);
+                        xx[e] = __shfl_sync(0xffffffffu, xm, e0 + e);
+                        yy[e] = __shfl_sync(0xffffffffu, ym, e0 + e);
+                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (e0 + e < n) uj[e] = *reinterpret_cast<const float4 *>(s_u + row_chunk(jj[e], lane));
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (e0 + e < n) fma_row(u, o, xx[e], yy[e], uj[e]);
+                }
+            }
+        }
+        *reinterpret_cast<float4 *>(s_u + row_chunk(i, lane)) = u;
+        __threadfence_block();  // every lane's u_i before the arrival
         __syncwarp();
-        if (lane == 0) s_done[i] = 1;
+        if (lane == 0) mbar_arrive(done_bar + 8u * (uint32_t)i);
+        o.x += yii * u.x; o.y += yii * u.y; o.z += yii * u.z; o.w += yii * u.w;
+        reinterpret_cast<float4 *>(O + (((size_t)b * B + i) * H + h) * kGdnD)[lane] = o;
     }
 }
 
-size_t gdn_workspace_bytes(int nb, int B, int H) { return (size_t)2 * nb * B * H * kGdnD * sizeof(float); }
-
-static size_t gdn_solve_smem(int B)
+size_t gdn_workspace_bytes(int nb, int B, int H)
 {
-    return (size_t)B * kGdnD * (sizeof(float) + sizeof(uint16_t)) + (size_t)B * (2 * sizeof(float) + 2 * sizeof(int));
+    size_t bytes = (size_t)nb * H * B * B * sizeof(GdnRec);
+    if (B > 128) bytes += (size_t)2 * nb * H * B * kGdnD * sizeof(float);
+    return bytes;
 }
 
 cudaError_t launch_gdn_tree(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
@@ -232,24 +495,17 @@ cudaError_t launch_gdn_tree(const uint16_t *q, const uint16_t *k, const uint16_t
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const size_t smem1 = (size_t)kGdnD * kGdnD * sizeof(float) + (size_t)2 * kGdnRows * kGdnD * sizeof(float);
     if (!(dev >= 0 && dev < 64 && opted_in[dev])) {
-        e = cudaFuncSetAttribute(gdn_state_products_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(gdn_tree_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)gdn_solve_smem(kGdnMaxB));
+        const uint32_t most = gdn_smem_layout(128).total > gdn_smem_layout(kGdnMaxB).total
+                                  ? gdn_smem_layout(128).total
+                                  : gdn_smem_layout(kGdnMaxB).total;  // the largest layout over 1 <= B <= 256
+        e = cudaFuncSetAttribute(gdn_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(most + 1024));
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) opted_in[dev] = 1;
     }
-    float *ks0 = static_cast<float *>(workspace);
-    float *qs0 = ks0 + (size_t)nb * B * H * kGdnD;
-    e = launch_dependent(gdn_state_products_kernel, dim3((unsigned)((B + kGdnRows - 1) / kGdnRows), (unsigned)H,
-                                                         (unsigned)nb),
-                         dim3(kGdnThreads), smem1, stream, q, k, S0, B, H, ks0, qs0);
-    if (e != cudaSuccess) return e;
-    return launch_dependent(gdn_tree_solve_kernel, dim3((unsigned)H, (unsigned)nb), dim3(kGdnThreads),
-                            gdn_solve_smem(B), stream, q, k, v, alpha, beta, parent, (const float *)ks0,
-                            (const float *)qs0, B, H, O, status);
+    return launch_dependent(gdn_tree_kernel, dim3((unsigned)H, (unsigned)nb), dim3(kGdnThreads),
+                            gdn_smem_layout(B).total + 1024, stream, q, k, v, alpha, beta, S0, parent, B, H, O,
+                            workspace, status);
 }
 
 }  // namespace tv
