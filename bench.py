@@ -71,10 +71,12 @@ def source_hash(name: str) -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def profiled_traffic(kernel: str, src: str, config: int):
+def profiled_traffic(kernel: str, src: str, config):
     """DRAM bytes per launch (read + write) from the committed ncu summary of this kernel and
-    workload, or None when there is none or the kernel source changed since it was taken."""
-    path = os.path.join(ROOT, "profiles", f"{kernel}_config{config}.md")
+    workload (a config number, or a workload tag), or None when there is none or the kernel
+    source changed since it was taken."""
+    tag = f"config{config}" if isinstance(config, int) else config
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{tag}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -476,7 +478,12 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
             "build_tree_note": "tv_build_tree (best-first, w = 1) of this workload's budget from per-depth candidate "
                                "tables, its own graph; not part of the step (it precedes verification)",
             "gdn_tree_ms": gdn_ms, "gdn_tree_bytes": gdn_bytes, "gdn_tree_workload": gdn_name,
-            "gdn_tree_hbm_frac": gdn_bytes / (gdn_ms * 1e-3) / (peaks["hbm_gbs"] * 1e9),
+            "gdn_tree_roofline": {
+                "kernel": "gdn_tree_kernel (tv_gdn_tree)", "bound": "hbm",
+                "achieved": gdn_bytes / (gdn_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": gdn_bytes / (gdn_ms * 1e-3) / (peaks["hbm_gbs"] * 1e9),
+                "peak_source": peak_src + " burst", "algorithmic_bytes": gdn_bytes,
+                "traffic": profiled_traffic("gdn_tree_kernel", "tv_gdn.cu", "gdn128")},
             "gdn_tree_note": "tv_gdn_tree (Gated DeltaNet layer verified over the tree without rollback), its own "
                              "graph; a layer of the hybrid model's verification pass, not part of this attention "
                              "step; the dependent chain along each root path bounds it, not HBM",
