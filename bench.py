@@ -180,19 +180,72 @@ class Step:
                         torch.empty((w.nb, w.B), dtype=torch.int32, device=dev),
                         torch.empty(w.nb, dtype=torch.int32, device=dev))
         self.acc_ws = torch.empty(tv.accept_workspace_size(w.V, w.B, w.nb), dtype=torch.uint8, device=dev)
-        self.launches_per_step = 5  # mask, attention, merge, argmax, acceptance
+        self.launches_per_step = 4  # attention, merge, argmax, acceptance (the masks are folded in)
         self.g_step = self.g_attn = self.g_acc = None
 
-    def _mask_stage(self):
-        self.tv.build_mask(self.parent, status=self.status, mask=self.mask, depth=self.depth)
-
+    # The step is the folded form: the attention and the acceptance walk derive the ancestor
+    # bits from the parent array, so no mask kernel runs (the fastest form measured; the
+    # breakdown times the others).
     def _attn_stage(self):
-        self.tv.attn(self.q, self.k, self.v, self.bt, self.pl, self.mask, status=self.status, o=self.o, lse=self.lse,
-                     workspace=self.ws)
+        self.tv.attn(self.q, self.k, self.v, self.bt, self.pl, None, status=self.status, o=self.o, lse=self.lse,
+                     workspace=self.ws, parent=self.parent)
 
     def _accept_stage(self):
-        self.tv.accept(self.logits, self.draft, self.parent, self.mask, status=self.status, out=self.acc_out,
+        self.tv.accept(self.logits, self.draft, self.parent, None, status=self.status, out=self.acc_out,
                        workspace=self.acc_ws)
+
+    def time_step_form(self, flush, steps, form):
+        """Mean ms of one form of the whole step (its own graph, same flush, own outputs):
+        "mask": tv_build_mask + attention + merge + argmax + walk (5 launches);
+        "folded": attention and walk build the ancestor bits from the parent array (4 launches);
+        "fused": folded, with argmax and walk in one kernel, tv_accept_fused (3 launches)."""
+        torch, tv = self.torch, self.tv
+        dev = self.q.device
+        ws = torch.zeros(tv.accept_fused_workspace_size(self.w.V, self.w.B, self.w.nb), dtype=torch.uint8, device=dev)
+        o, lse = torch.empty_like(self.o), torch.empty_like(self.lse)
+        out = tuple(torch.empty_like(t) for t in self.acc_out)
+        mask = torch.empty_like(self.mask)
+
+        def step():
+            if form == "mask":
+                tv.build_mask(self.parent, status=self.status, mask=mask)
+                tv.attn(self.q, self.k, self.v, self.bt, self.pl, mask, status=self.status, o=o, lse=lse,
+                        workspace=self.ws)
+                tv.accept(self.logits, self.draft, self.parent, mask, status=self.status, out=out, workspace=ws)
+            else:
+                tv.attn(self.q, self.k, self.v, self.bt, self.pl, None, status=self.status, o=o, lse=lse,
+                        workspace=self.ws, parent=self.parent)
+                if form == "folded":
+                    tv.accept(self.logits, self.draft, self.parent, None, status=self.status, out=out, workspace=ws)
+                else:
+                    tv.accept_fused(self.logits, self.draft, self.parent, None, status=self.status, out=out,
+                                    workspace=ws)
+
+        step()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        return self.time_stage(g, flush, steps)
+
+    def time_accept_fused(self, flush, steps, with_mask=True):
+        """Mean ms of tv_accept_fused (argmax and walk in one kernel) on the same inputs, with the
+        step's mask or building it from the parent array, for comparison with the two-kernel
+        tv_accept the step uses (its own graph, same flush)."""
+        torch, tv = self.torch, self.tv
+        ws = torch.zeros(tv.accept_fused_workspace_size(self.w.V, self.w.B, self.w.nb), dtype=torch.uint8,
+                         device=self.q.device)
+        out = tuple(torch.empty_like(t) for t in self.acc_out)
+        mask = None
+        if with_mask:  # the step itself builds no mask array
+            tv.build_mask(self.parent, status=self.status, mask=self.mask)
+            mask = self.mask
+        tv.accept_fused(self.logits, self.draft, self.parent, mask, status=self.status, out=out, workspace=ws)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            tv.accept_fused(self.logits, self.draft, self.parent, mask, status=self.status, out=out, workspace=ws)
+        return self.time_stage(g, flush, steps)
 
     def capture(self):
         """Record the step into one CUDA graph (and each stage into its own graph, for the
@@ -201,18 +254,15 @@ class Step:
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
-            self._mask_stage()
             self._attn_stage()
             self._accept_stage()
         torch.cuda.current_stream().wait_stream(side)
         torch.cuda.synchronize()
         self.g_step, self.g_attn, self.g_acc = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.g_step):
-            self._mask_stage()
             self._attn_stage()
             self._accept_stage()
         with torch.cuda.graph(self.g_attn):
-            self._mask_stage()
             self._attn_stage()
         with torch.cuda.graph(self.g_acc):
             self._accept_stage()
@@ -426,6 +476,9 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     commit_ms, commit_bytes = st.time_commit(flush, args.steps)
     tree_ms = st.time_tree(args.config, flush, args.steps)
     gdn_ms, gdn_bytes, gdn_name = st.time_gdn(flush, args.steps)
+    acc_fused_ms = st.time_accept_fused(flush, args.steps)
+    acc_fused_nomask_ms = st.time_accept_fused(flush, args.steps, with_mask=False)
+    forms_ms = {f: st.time_step_form(flush, args.steps, f) for f in ("mask", "folded", "fused")}
     if st.status.item() != 0:
         raise RuntimeError(f"device status {st.status.item()} in the commit stage")
     if world > 1:
@@ -444,10 +497,10 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     attn_tc = af / (peaks["bf16_tflops"] * 1e12)
     attn_hbm = ab / (peaks["hbm_gbs"] * 1e9)
     if attn_tc >= attn_hbm:
-        attn_roof = {"kernel": "attention stage: build_mask_kernel + tree_attn_kernel + tree_attn_merge_kernel", "bound": "tensor",
+        attn_roof = {"kernel": "attention stage: tree_attn_kernel (ancestor bits from the parent array) + tree_attn_merge_kernel", "bound": "tensor",
                      "achieved": af / t_attn / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
     else:
-        attn_roof = {"kernel": "attention stage: build_mask_kernel + tree_attn_kernel + tree_attn_merge_kernel", "bound": "hbm",
+        attn_roof = {"kernel": "attention stage: tree_attn_kernel (ancestor bits from the parent array) + tree_attn_merge_kernel", "bound": "hbm",
                      "achieved": ab / t_attn / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     acc_roof = {"kernel": "argmax_rows_kernel + accept_kernel (tv_accept)", "bound": "hbm",
                 "achieved": lb / t_acc / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
@@ -466,10 +519,19 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         "config": {"workload": wl.CONFIG_NAMES[args.config], "nb": w.nb, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
                    "D": w.D, "prefix_lens": [int(x) for x in w.prefix_lens][:8], "V": w.V,
                    "l2": "flushed before every timed step (512 MB write)", "parallelism": f"replicas x{world}",
-                   "launch": "one CUDA graph per step (mask, attention, merge, argmax, acceptance), captured once"},
+                   "launch": "one CUDA graph per step (attention with the ancestor bits from the parent array, merge, "
+                             "argmax, acceptance walk), captured once"},
         "roofline": roof,
         "breakdown": {
-            "attention_stage_ms": attn_stage_ms, "accept_ms": acc_stage_ms,
+            "attention_stage_ms": attn_stage_ms, "accept_ms": acc_stage_ms, "accept_fused_ms": acc_fused_ms,
+            "accept_fused_nomask_ms": acc_fused_nomask_ms, "step_forms_ms": forms_ms,
+            "step_forms_note": "each form of the whole step from its own graph with the same flush: mask = "
+                               "tv_build_mask + attention + merge + argmax + walk (5 launches); folded = the "
+                               "attention and the walk derive the ancestor bits from the parent array (4); fused = "
+                               "folded with tv_accept_fused (3)",
+            "accept_note": "the step's acceptance is the two-kernel tv_accept (argmax, then the walk as a programmatic "
+                           "dependent); accept_fused_ms is tv_accept_fused (one kernel) on the same inputs with the "
+                           "step's mask, accept_fused_nomask_ms the same building the mask from the parent array",
             "stage_timing": "each stage's own graph replayed K times with the same L2 flush, after the timed steps",
             "attention_nodes_per_s": nodes / t_attn, "attention_roofline": attn_roof, "accept_roofline": acc_roof,
             "attention_bytes": ab, "attention_flops": af, "accept_bytes": lb,

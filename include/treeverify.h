@@ -125,13 +125,17 @@ typedef struct tv_attn_args {
     const void *v_cache_d;       /* same layout as k_cache_d */
     const int32_t *block_table_d;/* int32 [nb][max_pages]; must cover P_b + B positions */
     const int32_t *prefix_lens_d;/* int32 [nb], P_b >= 0 (committed prefix, tree excluded) */
-    const uint32_t *mask_d;      /* uint32 [nb][B][ceil(B/32)] from tv_build_mask */
+    const uint32_t *mask_d;      /* uint32 [nb][B][ceil(B/32)] from tv_build_mask, or NULL */
     void *o_d;                   /* bf16 [nb*B][Hq][D] (out), 16-byte aligned */
     float *lse_d;                /* fp32 [nb*B][Hq] (out), natural log */
     int32_t *dev_status_d;       /* device status word, may be NULL */
     int32_t nb, B, Hq, Hkv, D, page_size, num_blocks, max_pages;
     float scale;                 /* <= 0 selects 1/sqrt(D) */
     int32_t num_ctas;            /* 0 = one CTA per SM; otherwise the CTA count to use */
+    const int32_t *parent_d;     /* int32 [nb][B], read only when mask_d is NULL: then each query
+                                    row's ancestor bits come from a walk up its node's root path
+                                    (the mask build folded into the attention; a parent array
+                                    that is not topological writes TV_ERR_NOT_TOPOLOGICAL) */
 } tv_attn_args;
 
 /* Bytes of device workspace tv_attn needs for these arguments (depends on
@@ -149,7 +153,7 @@ TV_API size_t tv_attn_workspace_size(const tv_attn_args *args);
  * Ordering: the attention kernel is launched as a programmatic dependent of the
  * previous kernel on the stream and reads q, the caches, block_table and
  * prefix_lens before waiting for that kernel to finish (it waits only before
- * reading mask_d).  So that previous kernel must not be one that writes those
+ * reading mask_d or parent_d).  So that previous kernel must not be one that writes those
  * inputs after signalling its dependents early.  Kernels launched without
  * programmatic dependent launch never signal early, and tv_build_mask (the
  * natural predecessor) writes only the masks and depths.
@@ -173,7 +177,12 @@ TV_API int32_t tv_attn(const tv_attn_args *args, void *workspace_d, size_t works
  *   logits_d       bf16 [nb*B][V], 2-byte aligned (any V >= 1)
  *   draft_tokens_d int32 [nb][B]  (entry 0 of each sequence is ignored)
  *   parent_d       int32 [nb][B]  (the array given to tv_build_mask)
- *   mask_d         uint32 [nb][B][ceil(B/32)] from tv_build_mask for the same parent
+ *   mask_d         uint32 [nb][B][ceil(B/32)] from tv_build_mask for the same parent,
+ *                  or NULL: the walk then builds each node's ancestor bits from
+ *                  parent_d itself while the argmax runs (tv_build_mask is not
+ *                  needed); a parent array that is not topological then writes
+ *                  TV_ERR_NOT_TOPOLOGICAL and gives n_acc = 0, path = {0, -1, ...},
+ *                  bonus = argmax of the root
  *   argmax_d       int32 [nb*B] (out), n_acc_d int32 [nb], path_d int32 [nb][B],
  *   bonus_d        int32 [nb] (out)
  *   workspace_d    device buffer of at least tv_accept_workspace_size(V, B, nb)
@@ -288,6 +297,32 @@ TV_API int32_t tv_kv_commit(void *k_cache_d, void *v_cache_d, const int32_t *blo
                             const int32_t *prefix_lens_d, const int32_t *n_acc_d, const int32_t *path_d,
                             int32_t nb, int32_t B, int32_t Hkv, int32_t D, int32_t page_size, int32_t num_blocks,
                             int32_t max_pages, int32_t *new_prefix_lens_d, int32_t *dev_status_d, void *stream);
+
+/*
+ * Argmax and acceptance in one kernel (the survey's fused acceptance)  [JF-4]
+ *
+ * The same results as tv_accept (argmax of every row, then the greedy walk), from
+ * one kernel launch instead of two: the argmax CTAs own whole rows, and the CTA
+ * whose keys complete a sequence's B rows (a per-sequence counter in the
+ * workspace tells) runs that sequence's walk.
+ *   mask_d     as tv_accept, or NULL: then the walk builds each node's ancestor
+ *              bits from parent_d itself (tv_build_mask is not needed), and a
+ *              parent array that is not topological writes TV_ERR_NOT_TOPOLOGICAL
+ *              and gives n_acc = 0, path = {0, -1, ...}, bonus = argmax of the root
+ *   workspace_d >= tv_accept_fused_workspace_size(V, B, nb) bytes, 8-byte aligned:
+ *              nb*B 8-byte keys, then nb 32-bit counters.  The counters must be zero
+ *              before the first call on a workspace (cudaMemset once); every call
+ *              leaves them zero.  Concurrent calls need their own workspace.
+ *   Other arguments as tv_accept.
+ * Ordering: a programmatic dependent of the previous kernel on the stream; it
+ * waits for it before reading anything.
+ * Returns TV_OK, TV_ERR_INVALID_ARG, TV_ERR_UNSUPPORTED_SHAPE or TV_ERR_CUDA.
+ */
+TV_API size_t tv_accept_fused_workspace_size(int32_t V, int32_t B, int32_t nb);
+TV_API int32_t tv_accept_fused(const uint16_t *logits_d, int32_t V, const int32_t *draft_tokens_d,
+                               const int32_t *parent_d, const uint32_t *mask_d, int32_t B, int32_t nb,
+                               int32_t *argmax_d, int32_t *n_acc_d, int32_t *path_d, int32_t *bonus_d,
+                               int32_t *dev_status_d, void *workspace_d, size_t workspace_bytes, void *stream);
 
 /*
  * tv_accept_noalloc — tv_accept for callers that cannot allocate device memory.

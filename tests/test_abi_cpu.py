@@ -100,7 +100,7 @@ def test_accept_argument_checks(L):
     assert call(nb=0) == 0
     assert call(V=0) == 1
     assert call(B=0) == 3 and call(B=300) == 3
-    assert call(logits=None) == 1 and call(mask=None) == 1
+    assert call(logits=None) == 1 and call(parent=None) == 1 and call(mask=P(FAKE + 2)) == 1
     assert call(logits=P(FAKE + 1)) == 1
     assert call(draft=P(FAKE + 2)) == 1
     assert call(ws=None) == 1 and call(ws_bytes=8) == 1 and call(ws=P(FAKE + 4)) == 1
@@ -108,6 +108,29 @@ def test_accept_argument_checks(L):
     assert L.tv_accept_workspace_size(151936, 256, 1) == 256 * 8
     assert L.tv_accept_workspace_size(4096, 16, 2) == 32 * 8
     assert L.tv_accept_workspace_size(0, 16, 1) == 0 and L.tv_accept_workspace_size(10, 300, 1) == 0
+
+
+def test_accept_fused_argument_checks(L):
+    P = C.c_void_p
+    ok = [P(FAKE)] * 4
+    base = dict(logits=P(FAKE), V=100, draft=P(FAKE), parent=P(FAKE), mask=P(FAKE), B=16, nb=1)
+
+    def call(**kw):
+        d = dict(base)
+        d.update(kw)
+        return L.tv_accept_fused(d["logits"], d["V"], d["draft"], d["parent"], d["mask"], d["B"], d["nb"], *ok, None,
+                                 d.get("ws", P(FAKE)), d.get("ws_bytes", 1 << 30), None)
+
+    assert call(nb=0) == 0
+    assert call(V=0) == 1
+    assert call(B=0) == 3 and call(B=300) == 3
+    assert call(logits=None) == 1 and call(parent=None) == 1
+    assert call(mask=P(FAKE + 2)) == 1 and call(logits=P(FAKE + 1)) == 1
+    assert call(ws=None) == 1 and call(ws_bytes=16 * 8) == 1 and call(ws=P(FAKE + 4)) == 1
+    # keys, then one 32-bit counter per sequence
+    assert L.tv_accept_fused_workspace_size(151936, 256, 1) == 256 * 8 + 4
+    assert L.tv_accept_fused_workspace_size(4096, 16, 3) == 48 * 8 + 12
+    assert L.tv_accept_fused_workspace_size(0, 16, 1) == 0
 
 
 def test_kv_commit_argument_checks(L):

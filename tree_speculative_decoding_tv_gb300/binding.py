@@ -24,7 +24,8 @@ TV_ERR_TIMEOUT = 5
 TV_ERR_UNIMPLEMENTED = 6
 
 EXPORTED = ("tv_status_str", "tv_version", "tv_build_mask", "tv_attn_workspace_size", "tv_attn",
-            "tv_accept_workspace_size", "tv_accept", "tv_accept_noalloc", "tv_kv_commit", "tv_build_tree", "tv_gdn_tree_workspace_size", "tv_gdn_tree")
+            "tv_accept_workspace_size", "tv_accept", "tv_accept_fused_workspace_size", "tv_accept_fused",
+            "tv_accept_noalloc", "tv_kv_commit", "tv_build_tree", "tv_gdn_tree_workspace_size", "tv_gdn_tree")
 NOALLOC_MAX_ROWS = 8192  # TV_ACCEPT_NOALLOC_MAX_ROWS
 
 
@@ -42,7 +43,7 @@ class AttnArgs(C.Structure):
         ("o_d", C.c_void_p), ("lse_d", C.c_void_p), ("dev_status_d", C.c_void_p),
         ("nb", C.c_int32), ("B", C.c_int32), ("Hq", C.c_int32), ("Hkv", C.c_int32), ("D", C.c_int32),
         ("page_size", C.c_int32), ("num_blocks", C.c_int32), ("max_pages", C.c_int32),
-        ("scale", C.c_float), ("num_ctas", C.c_int32),
+        ("scale", C.c_float), ("num_ctas", C.c_int32), ("parent_d", C.c_void_p),
     ]
 
 
@@ -71,6 +72,10 @@ def lib() -> C.CDLL:
         L.tv_accept_workspace_size.restype = C.c_size_t
         L.tv_accept.argtypes = [P, I, P, P, P, I, I, P, P, P, P, P, P, C.c_size_t, P]
         L.tv_accept.restype = I
+        L.tv_accept_fused_workspace_size.argtypes = [I, I, I]
+        L.tv_accept_fused_workspace_size.restype = C.c_size_t
+        L.tv_accept_fused.argtypes = [P, I, P, P, P, I, I, P, P, P, P, P, P, C.c_size_t, P]
+        L.tv_accept_fused.restype = I
         L.tv_accept_noalloc.argtypes = [P, I, P, P, P, I, I, P, P, P, P, P, P]
         L.tv_accept_noalloc.restype = I
         L.tv_kv_commit.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P]
@@ -119,17 +124,19 @@ def build_mask(parent: torch.Tensor, status: torch.Tensor | None = None, mask: t
 
 
 def attn_args(q, k_cache, v_cache, block_table, prefix_lens, mask, o, lse, status=None, scale: float = 0.0,
-              num_ctas: int = 0) -> AttnArgs:
+              num_ctas: int = 0, parent=None) -> AttnArgs:
+    """mask may be None when parent is given (the attention derives the ancestor bits itself)."""
     nbB, Hq, D = q.shape
     num_blocks, Hkv, page, _ = k_cache.shape
     nb = prefix_lens.shape[0]
     B = nbB // nb if nb else 0
     return AttnArgs(q_d=q.data_ptr(), k_cache_d=k_cache.data_ptr(), v_cache_d=v_cache.data_ptr(),
                     block_table_d=block_table.data_ptr(), prefix_lens_d=prefix_lens.data_ptr(),
-                    mask_d=mask.data_ptr(), o_d=o.data_ptr(), lse_d=lse.data_ptr(),
+                    mask_d=(mask.data_ptr() if mask is not None else None), o_d=o.data_ptr(), lse_d=lse.data_ptr(),
                     dev_status_d=(status.data_ptr() if status is not None else None),
                     nb=nb, B=B, Hq=Hq, Hkv=Hkv, D=D, page_size=page, num_blocks=num_blocks,
-                    max_pages=block_table.shape[1], scale=float(scale), num_ctas=int(num_ctas))
+                    max_pages=block_table.shape[1], scale=float(scale), num_ctas=int(num_ctas),
+                    parent_d=(parent.data_ptr() if parent is not None else None))
 
 
 def attn_workspace_size(args: AttnArgs) -> int:
@@ -137,13 +144,14 @@ def attn_workspace_size(args: AttnArgs) -> int:
 
 
 def attn(q, k_cache, v_cache, block_table, prefix_lens, mask, status=None, scale: float = 0.0, num_ctas: int = 0,
-         o=None, lse=None, workspace=None, stream=None):
-    """tv_attn: returns (O bf16 [nb*B][Hq][D], LSE fp32 [nb*B][Hq])."""
+         o=None, lse=None, workspace=None, stream=None, parent=None):
+    """tv_attn: returns (O bf16 [nb*B][Hq][D], LSE fp32 [nb*B][Hq]); mask=None with parent
+    given folds the mask build into the attention."""
     if o is None:
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
-    a = attn_args(q, k_cache, v_cache, block_table, prefix_lens, mask, o, lse, status, scale, num_ctas)
+    a = attn_args(q, k_cache, v_cache, block_table, prefix_lens, mask, o, lse, status, scale, num_ctas, parent)
     need = attn_workspace_size(a)
     if need == 0:  # invalid arguments: let the library say which
         _check(lib().tv_attn(C.byref(a), None, 0, _stream(stream)), "tv_attn")
@@ -175,6 +183,33 @@ def accept(logits, draft, parent, mask, status=None, out=None, workspace=None, s
                          _p(bonus), _p(status), _p(workspace), workspace.numel() * workspace.element_size(),
                          _stream(stream))
     _check(rc, "tv_accept")
+    return am, n_acc, path, bonus
+
+
+def accept_fused_workspace_size(V: int, B: int, nb: int) -> int:
+    return int(lib().tv_accept_fused_workspace_size(int(V), int(B), int(nb)))
+
+
+def accept_fused(logits, draft, parent, mask=None, status=None, out=None, workspace=None, stream=None):
+    """tv_accept_fused: tv_accept's results from one kernel; mask may be None (built from parent).
+
+    A workspace passed in must have had its counters zeroed once (the library keeps
+    them zero); without one, a zeroed workspace is allocated for this call.
+    """
+    nb, B = parent.shape
+    V = logits.shape[-1]
+    dev = logits.device
+    if out is None:
+        out = (torch.empty(nb * B, dtype=torch.int32, device=dev), torch.empty(nb, dtype=torch.int32, device=dev),
+               torch.empty((nb, B), dtype=torch.int32, device=dev), torch.empty(nb, dtype=torch.int32, device=dev))
+    am, n_acc, path, bonus = out
+    need = accept_fused_workspace_size(V, B, nb)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.zeros(max(need, 8), dtype=torch.uint8, device=dev)
+    rc = lib().tv_accept_fused(_p(logits), V, _p(draft), _p(parent), _p(mask), B, nb, _p(am), _p(n_acc), _p(path),
+                               _p(bonus), _p(status), _p(workspace), workspace.numel() * workspace.element_size(),
+                               _stream(stream))
+    _check(rc, "tv_accept_fused")
     return am, n_acc, path, bonus
 
 

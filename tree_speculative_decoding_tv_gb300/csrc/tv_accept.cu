@@ -28,6 +28,14 @@
 // ballot words, node i is accepted iff (mask[i] & ~ok) == 0 (the root counts as
 // ok), the best (depth, -index) key is a block max, and the path is read off
 // the chosen node's mask bits in ascending order.
+//
+// fused (tv_accept_fused, one kernel): the same argmax CTAs, and after a CTA
+// stores a row group's keys it adds the group's row count to a per-sequence
+// counter in the workspace; the CTA whose addition completes sequence b's B rows
+// resets the counter and runs b's acceptance walk itself (a fence orders every
+// CTA's keys before its addition, and the walking CTA's fence after it before
+// it reads them).  Nothing waits on another CTA.  Without a mask the walking CTA
+// builds node i's ancestor bits in shared memory by walking i's root path.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -104,6 +112,141 @@ __device__ __forceinline__ __nv_bfloat162 vec_max2(const uint4 &v)
     return __hmax2_nan(__hmax2_nan(as_bf2(v.x), as_bf2(v.y)), __hmax2_nan(as_bf2(v.z), as_bf2(v.w)));
 }
 
+// Shared memory of one acceptance walk (one sequence, one thread per node).
+struct AcceptSmem {
+    int am[kMaxB];
+    int16_t par[kMaxB];  // the fused walk's parent array (mask built in-kernel)
+    uint32_t mask[kMaxB * kMaxW];
+    uint32_t ok[kMaxW];
+    int best[kMaxB / 32];
+    int bad;
+};
+
+// The walk proper, once s.am (every row's argmax) and s.mask (every node's ancestor
+// bits) are in shared memory and visible: p and d are this thread's parent and draft
+// token (thread i = node i).
+__device__ __forceinline__ void accept_core(AcceptSmem &s, int b, int B, int W, int p, int d,
+                                            int32_t *__restrict__ n_acc, int32_t *__restrict__ path,
+                                            int32_t *__restrict__ bonus, int32_t *status)
+{
+    const int i = threadIdx.x;
+    const int lane = i & 31, wid = i >> 5;
+    bool ok = true;
+    if (i > 0 && i < B) {
+        if (p < 0 || p >= i) {
+            ok = false;
+            s.bad = 1;
+        } else {
+            ok = d == s.am[p];
+        }
+    }
+    const uint32_t okw = __ballot_sync(0xffffffffu, ok);
+    if (lane == 0 && wid < kMaxW) s.ok[wid] = okw;
+    __syncthreads();
+
+    int key = -1;  // depth * 512 + (511 - node) of an accepted node
+    if (i < B) {
+        bool acc = true;
+        int bits = 0;
+        for (int w = 0; w < W; ++w) {
+            const uint32_t mw = s.mask[i * W + w];
+            acc = acc && ((mw & ~s.ok[w]) == 0u);
+            bits += __popc(mw);
+        }
+        if (acc) key = (bits - 1) * 512 + (511 - i);
+    }
+    key = __reduce_max_sync(0xffffffffu, key);
+    if (lane == 0) s.best[wid] = key;
+    __syncthreads();
+    int top = s.best[0];
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) top = max(top, s.best[w]);
+    const int vstar = top >= 0 ? 511 - (top & 511) : 0;
+    const int dep = top >= 0 ? (top >> 9) : 0;
+    const uint32_t *vmask = s.mask + vstar * W;
+
+    if (i < B) {
+        const int w = i >> 5;
+        const uint32_t mw = vmask[w];
+        if ((mw >> lane) & 1u) {
+            int before = __popc(mw & ((1u << lane) - 1u));
+            for (int k = 0; k < w; ++k) before += __popc(vmask[k]);
+            path[(size_t)b * B + before] = i;
+        }
+        if (i > dep) path[(size_t)b * B + i] = -1;
+    }
+    if (i == 0) {
+        n_acc[b] = dep;
+        bonus[b] = s.am[vstar];
+        if (s.bad) report_status(status, TV_ERR_NOT_TOPOLOGICAL);
+    }
+}
+
+// Outputs for a sequence whose parent array is not topological (no mask to walk):
+// the root alone is accepted; s.am must hold the rows' argmax.
+__device__ __forceinline__ void accept_bad_tree(const AcceptSmem &s, int b, int B, int32_t *__restrict__ n_acc,
+                                                int32_t *__restrict__ path, int32_t *__restrict__ bonus,
+                                                int32_t *status)
+{
+    const int i = threadIdx.x;
+    if (i < B) path[(size_t)b * B + i] = (i == 0) ? 0 : -1;
+    if (i == 0) {
+        n_acc[b] = 0;
+        bonus[b] = s.am[0];
+        report_status(status, TV_ERR_NOT_TOPOLOGICAL);
+    }
+}
+
+// Node i's ancestor bits from a walk up its root path in shared memory (s.par must be
+// staged and topological): the mask build folded into the acceptance.
+__device__ __forceinline__ void accept_rows_from_parents(AcceptSmem &s, int B, int W)
+{
+    const int i = threadIdx.x;
+    if (i < B) {
+        uint32_t *row = s.mask + i * W;
+        for (int w = 0; w < W; ++w) row[w] = 0u;
+        for (int j = i; j >= 0; j = s.par[j]) row[j >> 5] |= 1u << (j & 31);
+    }
+}
+
+// Sequence b's acceptance inside the fused kernel, run by the CTA that completed b's
+// keys (every CTA's keys are visible to it: see the fences in the caller).  With no
+// mask, node i's ancestor bits come from a walk up its root path, after the parent
+// array has been checked (a bad one reports TV_ERR_NOT_TOPOLOGICAL and gives the
+// root alone as the accepted path).
+__device__ void fused_walk(AcceptSmem &s, int b, int B, int W, const unsigned long long *__restrict__ best,
+                           const int32_t *__restrict__ draft, const int32_t *__restrict__ parent,
+                           const uint32_t *__restrict__ mask, int32_t *__restrict__ am,
+                           int32_t *__restrict__ n_acc, int32_t *__restrict__ path, int32_t *__restrict__ bonus,
+                           int32_t *status)
+{
+    const int i = threadIdx.x;
+    int p = -1, d = 0;
+    bool bad = false;
+    if (i < B) {
+        p = parent[(size_t)b * B + i];
+        d = draft[(size_t)b * B + i];
+        bad = (i == 0) ? (p != -1) : (p < 0 || p >= i);
+        const unsigned long long top = __ldcg(best + (size_t)b * B + i);
+        const int a = (int)(0xFFFFFFFFu - (uint32_t)top);
+        s.am[i] = a;
+        am[(size_t)b * B + i] = a;
+    }
+    if (i == 0) s.bad = 0;
+    if (mask) {
+        if (i < B)
+            for (int w = 0; w < W; ++w) s.mask[i * W + w] = mask[((size_t)b * B + i) * W + w];
+    } else {
+        if (i < B) s.par[i] = (int16_t)p;
+        if (__syncthreads_or(bad)) {
+            accept_bad_tree(s, b, B, n_acc, path, bonus, status);
+            return;
+        }
+        accept_rows_from_parents(s, B, W);
+    }
+    __syncthreads();
+    accept_core(s, b, B, W, p, d, n_acc, path, bonus, status);
+}
+
 // One unit = kArgChunk logits of one row = one warp: each lane holds kArgVec
 // 16-byte vectors in registers (all loads in flight at once) and folds them as
 // a tree of bf16x2 maxima, keeping each vector's maximum; the warp agrees on the
@@ -111,9 +254,20 @@ __device__ __forceinline__ __nv_bfloat162 vec_max2(const uint4 &v)
 // it find their first position in two steps (first vector whose maximum
 // matches, then the element inside it), and one integer min-reduction picks the
 // smallest.  No block-level synchronisation; 32-bit index arithmetic.
+// What the fused kernel needs for the acceptance walks (unused by the plain argmax).
+struct FusedAccept {
+    unsigned int *counters;  // [nb] rows whose keys are stored so far; zero between calls
+    int B, W;
+    const int32_t *draft, *parent;
+    const uint32_t *mask;  // may be null
+    int32_t *am, *n_acc, *path, *bonus, *status;
+};
+
+template <bool kFused>
 __global__ void __launch_bounds__(kArgThreads) argmax_rows_kernel(const uint16_t *__restrict__ logits, int V,
                                                                   int nchunk, int R, int rows,
-                                                                  unsigned long long *__restrict__ best)
+                                                                  unsigned long long *__restrict__ best,
+                                                                  FusedAccept fa)
 {
     __shared__ unsigned long long s_key[kArgThreads / 32];  // R <= 8 rows per group
     static_assert(kArgChunk == 32 * kArgVec * 8, "one warp per unit");
@@ -122,6 +276,22 @@ __global__ void __launch_bounds__(kArgThreads) argmax_rows_kernel(const uint16_t
     const float NEG_INF = -__int_as_float(0x7f800000);
     pdl_wait_primary();  // the logits may come from the previous kernel in the stream
     pdl_launch_dependents();
+    if constexpr (kFused) {
+        // whichever CTA walks a sequence reads its tree inputs: start them towards L2 now
+        const int b0 = blockIdx.x * R / fa.B;
+        const int b1 = min(rows - 1, blockIdx.x * R + R - 1) / fa.B;
+        for (int bb = b0; bb <= b1; ++bb) {
+            const int lines_pd = (fa.B * 4 + 127) / 128, lines_m = fa.mask ? (fa.B * fa.W * 4 + 127) / 128 : 0;
+            for (int t = threadIdx.x; t < 2 * lines_pd + lines_m; t += kArgThreads) {
+                const char *a = t < lines_pd ? reinterpret_cast<const char *>(fa.parent + (size_t)bb * fa.B) + 128 * t
+                              : t < 2 * lines_pd
+                                  ? reinterpret_cast<const char *>(fa.draft + (size_t)bb * fa.B) + 128 * (t - lines_pd)
+                                  : reinterpret_cast<const char *>(fa.mask + (size_t)bb * fa.B * fa.W) +
+                                        128 * (t - 2 * lines_pd);
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+            }
+        }
+    }
 
     for (int r0 = blockIdx.x * R; r0 < rows; r0 += gridDim.x * R) {
       const int nr = min(R, rows - r0);
@@ -215,6 +385,30 @@ __global__ void __launch_bounds__(kArgThreads) argmax_rows_kernel(const uint16_t
       }
       __syncthreads();
       if (threadIdx.x < nr) best[r0 + threadIdx.x] = s_key[threadIdx.x];
+      if constexpr (kFused) {
+          __shared__ AcceptSmem s_acc;
+          __shared__ int s_walk[kArgThreads / 32], s_nwalk;
+          if ((int)threadIdx.x < nr) __threadfence();  // this CTA's keys before its counter additions
+          if (threadIdx.x == 0) s_nwalk = 0;
+          __syncthreads();
+          // the sequences this group's rows belong to (at most nr <= 8)
+          const int b0 = r0 / fa.B, bb = b0 + (int)threadIdx.x;
+          if (bb <= (r0 + nr - 1) / fa.B) {
+              const unsigned c = (unsigned)(min(r0 + nr, (bb + 1) * fa.B) - max(r0, bb * fa.B));
+              if (atomicAdd(&fa.counters[bb], c) + c == (unsigned)fa.B) {  // b's last rows: walk it
+                  fa.counters[bb] = 0u;
+                  s_walk[atomicAdd(&s_nwalk, 1)] = bb;
+              }
+          }
+          __syncthreads();
+          const int nw = s_nwalk;
+          if (nw > 0) __threadfence();  // every other CTA's keys of those sequences from here
+          for (int k = 0; k < nw; ++k) {
+              fused_walk(s_acc, s_walk[k], fa.B, fa.W, best, fa.draft, fa.parent, fa.mask, fa.am, fa.n_acc,
+                         fa.path, fa.bonus, fa.status);
+              __syncthreads();
+          }
+      }
       __syncthreads();  // s_key is reset for the next group only after it was read
     }
 }
@@ -227,91 +421,50 @@ __global__ void __launch_bounds__(kMaxB) accept_kernel(const unsigned long long 
                                                        int32_t *__restrict__ path, int32_t *__restrict__ bonus,
                                                        int32_t *status)
 {
-    __shared__ int s_am[kMaxB];
-    __shared__ uint32_t s_mask[kMaxB * kMaxW];
-    __shared__ uint32_t s_ok[kMaxW];
-    __shared__ int s_best[kMaxB / 32];
-    __shared__ int s_bad;
-
+    __shared__ AcceptSmem s;
     const int b = blockIdx.x;
     const int i = threadIdx.x;
-    const int lane = i & 31, wid = i >> 5;
 
     // The tree inputs were written before the argmax kernel began (the key memset
     // ahead of it completes only after all earlier work), so they are read while
     // the argmax is still running; only the keys wait for it.
     int p = -1, d = 0;
-    uint32_t mrow[kMaxW];
+    bool bad = false;
     if (i < B) {
         p = parent[(size_t)b * B + i];
         d = draft[(size_t)b * B + i];
+        if (mask) {
+            uint32_t mrow[kMaxW];
 #pragma unroll
-        for (int w = 0; w < kMaxW; ++w)  // all row words in flight at once
-            if (w < W) mrow[w] = mask[((size_t)b * B + i) * W + w];
+            for (int w = 0; w < kMaxW; ++w)  // all row words in flight at once
+                if (w < W) mrow[w] = mask[((size_t)b * B + i) * W + w];
 #pragma unroll
-        for (int w = 0; w < kMaxW; ++w)
-            if (w < W) s_mask[i * W + w] = mrow[w];
+            for (int w = 0; w < kMaxW; ++w)
+                if (w < W) s.mask[i * W + w] = mrow[w];
+        } else {
+            bad = (i == 0) ? (p != -1) : (p < 0 || p >= i);
+            s.par[i] = (int16_t)p;
+        }
     }
-    if (i == 0) s_bad = 0;
+    if (i == 0) s.bad = 0;
+    // without a mask array the rows are built here, while the argmax still runs
+    const bool bad_tree = !mask && __syncthreads_or(bad);
+    if (!mask && !bad_tree) accept_rows_from_parents(s, B, W);
     pdl_wait_primary();  // the argmax keys are complete from here on
 
     // every row's argmax is the low half of its key: 0xFFFFFFFF - index
     if (i < B) {
         const unsigned long long top = __ldcg(best + (size_t)b * B + i);
         const int a = (int)(0xFFFFFFFFu - (uint32_t)top);
-        s_am[i] = a;
+        s.am[i] = a;
         am[(size_t)b * B + i] = a;
     }
     __syncthreads();
-
-    bool ok = true;
-    if (i > 0 && i < B) {
-        if (p < 0 || p >= i) {
-            ok = false;
-            s_bad = 1;
-        } else {
-            ok = d == s_am[p];
-        }
+    if (bad_tree) {
+        accept_bad_tree(s, b, B, n_acc, path, bonus, status);
+        return;
     }
-    const uint32_t okw = __ballot_sync(0xffffffffu, ok);
-    if (lane == 0 && wid < kMaxW) s_ok[wid] = okw;
-    __syncthreads();
-
-    int key = -1;  // depth * 512 + (511 - node) of an accepted node
-    if (i < B) {
-        bool acc = true;
-        int bits = 0;
-        for (int w = 0; w < W; ++w) {
-            const uint32_t mw = s_mask[i * W + w];
-            acc = acc && ((mw & ~s_ok[w]) == 0u);
-            bits += __popc(mw);
-        }
-        if (acc) key = (bits - 1) * 512 + (511 - i);
-    }
-    key = __reduce_max_sync(0xffffffffu, key);
-    if (lane == 0) s_best[wid] = key;
-    __syncthreads();
-    int top = s_best[0];
-    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) top = max(top, s_best[w]);
-    const int vstar = top >= 0 ? 511 - (top & 511) : 0;
-    const int dep = top >= 0 ? (top >> 9) : 0;
-    const uint32_t *vmask = s_mask + vstar * W;
-
-    if (i < B) {
-        const int w = i >> 5;
-        const uint32_t mw = vmask[w];
-        if ((mw >> lane) & 1u) {
-            int before = __popc(mw & ((1u << lane) - 1u));
-            for (int k = 0; k < w; ++k) before += __popc(vmask[k]);
-            path[(size_t)b * B + before] = i;
-        }
-        if (i > dep) path[(size_t)b * B + i] = -1;
-    }
-    if (i == 0) {
-        n_acc[b] = dep;
-        bonus[b] = s_am[vstar];
-        if (s_bad) report_status(status, TV_ERR_NOT_TOPOLOGICAL);
-    }
+    accept_core(s, b, B, W, p, d, n_acc, path, bonus, status);
 }
 
 size_t accept_workspace_bytes(int V, int B, int nb)
@@ -333,14 +486,48 @@ cudaError_t launch_accept(const uint16_t *logits, int V, const int32_t *draft, c
     if (grid > need) grid = need;
     if (grid < 1) grid = 1;
     unsigned long long *best = static_cast<unsigned long long *>(workspace);
-    cudaError_t e = launch_dependent(argmax_rows_kernel, dim3((unsigned)grid), dim3(kArgThreads), 0, stream, logits,
-                                     V, nchunk, R, rows, best);
+    cudaError_t e = launch_dependent(argmax_rows_kernel<false>, dim3((unsigned)grid), dim3(kArgThreads), 0, stream,
+                                     logits, V, nchunk, R, rows, best, FusedAccept{});
     if (e != cudaSuccess) return e;
     const int W = (B + 31) / 32;
     // its launch overlaps the argmax tail; it waits before reading the keys
     return launch_dependent(accept_kernel, dim3((unsigned)nb), dim3(kMaxB), 0, stream,
                             (const unsigned long long *)best, draft, parent, mask, B, W, am, n_acc, path, bonus,
                             status);
+}
+
+size_t accept_fused_workspace_bytes(int V, int B, int nb)
+{
+    return accept_workspace_bytes(V, B, nb) + (size_t)nb * sizeof(unsigned int);
+}
+
+cudaError_t launch_accept_fused(const uint16_t *logits, int V, const int32_t *draft, const int32_t *parent,
+                                const uint32_t *mask, int B, int nb, int32_t *am, int32_t *n_acc, int32_t *path,
+                                int32_t *bonus, int32_t *status, void *workspace, int num_sms, cudaStream_t stream)
+{
+    const int nchunk = (V + kArgChunk - 1) / kArgChunk;
+    const int rows = nb * B;
+    const int wpc = kArgThreads / 32;
+    const int R = nchunk >= wpc ? 1 : wpc / nchunk;
+    long long grid = (long long)num_sms * kArgCtasPerSm;
+    const long long need = ((long long)rows + R - 1) / R;
+    if (grid > need) grid = need;
+    if (grid < 1) grid = 1;
+    unsigned long long *best = static_cast<unsigned long long *>(workspace);
+    FusedAccept fa;
+    fa.counters = reinterpret_cast<unsigned int *>(best + (size_t)rows);
+    fa.B = B;
+    fa.W = (B + 31) / 32;
+    fa.draft = draft;
+    fa.parent = parent;
+    fa.mask = mask;
+    fa.am = am;
+    fa.n_acc = n_acc;
+    fa.path = path;
+    fa.bonus = bonus;
+    fa.status = status;
+    return launch_dependent(argmax_rows_kernel<true>, dim3((unsigned)grid), dim3(kArgThreads), 0, stream, logits, V,
+                            nchunk, R, rows, best, fa);
 }
 
 // ------------------------------------------------------ allocation-free variant

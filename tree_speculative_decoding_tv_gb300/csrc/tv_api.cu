@@ -43,13 +43,13 @@ int32_t check_attn(const tv_attn_args *a)
     if ((long long)a->num_blocks * a->Hkv * kPageSize >= (1ll << 31)) return TV_ERR_UNSUPPORTED_SHAPE;
     if ((long long)a->nb * a->B * a->Hq >= (1ll << 31)) return TV_ERR_UNSUPPORTED_SHAPE;
     if (a->num_ctas < 0) return TV_ERR_INVALID_ARG;
-    if (!a->q_d || !a->k_cache_d || !a->v_cache_d || !a->block_table_d || !a->prefix_lens_d || !a->mask_d ||
-        !a->o_d || !a->lse_d)
+    if (!a->q_d || !a->k_cache_d || !a->v_cache_d || !a->block_table_d || !a->prefix_lens_d ||
+        (!a->mask_d && !a->parent_d) || !a->o_d || !a->lse_d)
         return TV_ERR_INVALID_ARG;
     if (!aligned(a->q_d, 16) || !aligned(a->k_cache_d, 16) || !aligned(a->v_cache_d, 16) || !aligned(a->o_d, 16))
         return TV_ERR_INVALID_ARG;
     if (!aligned(a->block_table_d, 4) || !aligned(a->prefix_lens_d, 4) || !aligned(a->mask_d, 4) ||
-        !aligned(a->lse_d, 4) || !aligned(a->dev_status_d, 4))
+        !aligned(a->parent_d, 4) || !aligned(a->lse_d, 4) || !aligned(a->dev_status_d, 4))
         return TV_ERR_INVALID_ARG;
     return TV_OK;
 }
@@ -128,7 +128,7 @@ int32_t tv_accept(const uint16_t *logits_d, int32_t V, const int32_t *draft_toke
 {
     if (nb < 0 || V < 1) return TV_ERR_INVALID_ARG;
     if (B < 1 || B > kMaxB) return TV_ERR_UNSUPPORTED_SHAPE;
-    if (!logits_d || !draft_tokens_d || !parent_d || !mask_d || !argmax_d || !n_acc_d || !path_d || !bonus_d)
+    if (!logits_d || !draft_tokens_d || !parent_d || !argmax_d || !n_acc_d || !path_d || !bonus_d)
         return TV_ERR_INVALID_ARG;
     if (!aligned(logits_d, 2) || !aligned(draft_tokens_d, 4) || !aligned(parent_d, 4) || !aligned(mask_d, 4) ||
         !aligned(argmax_d, 4) || !aligned(n_acc_d, 4) || !aligned(path_d, 4) || !aligned(bonus_d, 4) ||
@@ -146,6 +146,37 @@ int32_t tv_accept(const uint16_t *logits_d, int32_t V, const int32_t *draft_toke
     return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
 
+size_t tv_accept_fused_workspace_size(int32_t V, int32_t B, int32_t nb)
+{
+    if (V < 1 || B < 1 || B > kMaxB || nb < 0) return 0;
+    return tv::accept_fused_workspace_bytes(V, B, nb);
+}
+
+int32_t tv_accept_fused(const uint16_t *logits_d, int32_t V, const int32_t *draft_tokens_d, const int32_t *parent_d,
+                        const uint32_t *mask_d, int32_t B, int32_t nb, int32_t *argmax_d, int32_t *n_acc_d,
+                        int32_t *path_d, int32_t *bonus_d, int32_t *dev_status_d, void *workspace_d,
+                        size_t workspace_bytes, void *stream)
+{
+    if (nb < 0 || V < 1) return TV_ERR_INVALID_ARG;
+    if (B < 1 || B > kMaxB) return TV_ERR_UNSUPPORTED_SHAPE;
+    if (!logits_d || !draft_tokens_d || !parent_d || !argmax_d || !n_acc_d || !path_d || !bonus_d)
+        return TV_ERR_INVALID_ARG;
+    if (!aligned(logits_d, 2) || !aligned(draft_tokens_d, 4) || !aligned(parent_d, 4) || !aligned(mask_d, 4) ||
+        !aligned(argmax_d, 4) || !aligned(n_acc_d, 4) || !aligned(path_d, 4) || !aligned(bonus_d, 4) ||
+        !aligned(dev_status_d, 4))
+        return TV_ERR_INVALID_ARG;
+    if ((long long)nb * B * (((long long)V + 4095) / 4096) >= (1ll << 31)) return TV_ERR_UNSUPPORTED_SHAPE;
+    if (nb == 0) return TV_OK;
+    if (!workspace_d || !aligned(workspace_d, 8) || workspace_bytes < tv::accept_fused_workspace_bytes(V, B, nb))
+        return TV_ERR_INVALID_ARG;
+    const int sms = sm_count();
+    if (sms < 1) return TV_ERR_CUDA;
+    cudaError_t e = tv::launch_accept_fused(logits_d, V, draft_tokens_d, parent_d, mask_d, B, nb, argmax_d, n_acc_d,
+                                            path_d, bonus_d, dev_status_d, workspace_d, sms,
+                                            static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
 int32_t tv_accept_noalloc(const uint16_t *logits_d, int32_t V, const int32_t *draft_tokens_d, const int32_t *parent_d,
                           const uint32_t *mask_d, int32_t B, int32_t nb, int32_t *argmax_d, int32_t *n_acc_d,
                           int32_t *path_d, int32_t *bonus_d, int32_t *dev_status_d, void *stream)
@@ -153,7 +184,7 @@ int32_t tv_accept_noalloc(const uint16_t *logits_d, int32_t V, const int32_t *dr
     if (nb < 0 || V < 1) return TV_ERR_INVALID_ARG;
     if (B < 1 || B > kMaxB) return TV_ERR_UNSUPPORTED_SHAPE;
     if ((long long)nb * B > TV_ACCEPT_NOALLOC_MAX_ROWS) return TV_ERR_UNSUPPORTED_SHAPE;
-    if (!logits_d || !draft_tokens_d || !parent_d || !mask_d || !argmax_d || !n_acc_d || !path_d || !bonus_d)
+    if (!logits_d || !draft_tokens_d || !parent_d || !argmax_d || !n_acc_d || !path_d || !bonus_d)
         return TV_ERR_INVALID_ARG;
     if (!aligned(logits_d, 2) || !aligned(draft_tokens_d, 4) || !aligned(parent_d, 4) || !aligned(mask_d, 4) ||
         !aligned(argmax_d, 4) || !aligned(n_acc_d, 4) || !aligned(path_d, 4) || !aligned(bonus_d, 4) ||

@@ -110,7 +110,8 @@ struct AttnParams {
     CUtensorMap tm_v;
     const int32_t *block_table;
     const int32_t *prefix_lens;
-    const uint32_t *mask;
+    const uint32_t *mask;   // null: ancestor bits from parent
+    const int32_t *parent;
     uint16_t *o;
     float *lse;
     int32_t *status;
@@ -249,6 +250,62 @@ __device__ __forceinline__ bool next_seg(const Sched &s, Cursor &c, Seg &sg)
         return true;
     }
     return false;
+}
+
+constexpr int kMaxMaskWords = 8;  // ceil(256 / 32)
+
+// Node i's ancestor bits (i included) from a walk up its root path, into registers
+// (word w of the row in m[w]).  Indices must fall strictly along the walk and end at
+// the root (parent -1); otherwise the walk stops and TV_ERR_NOT_TOPOLOGICAL is reported.
+__device__ __forceinline__ void row_mask_from_parents(const int32_t *__restrict__ par, int i,
+                                                      uint32_t (&m)[kMaxMaskWords], int32_t *status)
+{
+#pragma unroll
+    for (int w = 0; w < kMaxMaskWords; ++w) m[w] = 0u;
+    for (int j = i;;) {
+        const int wj = j >> 5;
+        const uint32_t bit = 1u << (j & 31);
+#pragma unroll
+        for (int w = 0; w < kMaxMaskWords; ++w)
+            if (w == wj) m[w] |= bit;
+        const int pj = __ldg(par + j);
+        if (pj < 0 || pj >= j) {
+            if (j != 0 || pj != -1) report_status(status, TV_ERR_NOT_TOPOLOGICAL);
+            return;
+        }
+        j = pj;
+    }
+}
+
+__device__ __forceinline__ uint32_t word_at(const uint32_t (&m)[kMaxMaskWords], int w)
+{
+    uint32_t r = 0u;
+#pragma unroll
+    for (int k = 0; k < kMaxMaskWords; ++k)
+        if (k == w) r = m[k];
+    return r;
+}
+
+// visible_bits (below) with the row's words in registers
+__device__ __forceinline__ uint32_t visible_bits_reg(int kstart, int P, int B, const uint32_t (&m)[kMaxMaskWords],
+                                                     int W)
+{
+    if (kstart + 32 <= P) return 0xffffffffu;
+    uint32_t v = (kstart >= P) ? 0u : ((1u << (P - kstart)) - 1u);
+    const int t0 = kstart - P;
+    if (t0 + 32 > 0 && t0 < B) {
+        uint32_t bits;
+        if (t0 >= 0) {
+            const int w = t0 >> 5, sh = t0 & 31;
+            const uint32_t lo = word_at(m, w);
+            const uint32_t hi = (w + 1 < W) ? word_at(m, w + 1) : 0u;
+            bits = sh ? ((lo >> sh) | (hi << (32 - sh))) : lo;
+        } else {
+            bits = word_at(m, 0) << (-t0);
+        }
+        v |= bits;
+    }
+    return v;
 }
 
 // 32 visibility bits for the keys kstart .. kstart+31 of one query row:
@@ -601,7 +658,9 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
             }
             const int i = (2 * sg.mp + (pair ? x : 0)) * p.NT + node_local;
             const bool valid = i < p.B;
-            const uint32_t *mrow = p.mask + ((size_t)sg.b * p.B + (valid ? i : 0)) * p.W;
+            const uint32_t *mrow = p.mask ? p.mask + ((size_t)sg.b * p.B + (valid ? i : 0)) * p.W : nullptr;
+            uint32_t mreg[kMaxMaskWords];  // the row's ancestor bits when there is no mask array
+            bool mreg_built = false;
             float m_run = -INFINITY, l_run = 0.f;  // m_run in log2 units of the scaled score
             for (int lx = 0; lx < nx; ++lx) {
                 const int t = pair ? lx : 2 * lx + x;
@@ -622,13 +681,19 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
 
                 // tree / tail mask (prefix-only tiles skip it), then the row max of the raw scores
                 if (!(valid && k0 + kN <= sg.P)) {
-                    if (!mask_ready) {  // the masks may come from the previous kernel
+                    if (!mask_ready) {  // the masks (or parents) may come from the previous kernel
                         pdl_wait_primary();
                         mask_ready = true;
                     }
+                    if (!mrow && valid && !mreg_built) {
+                        row_mask_from_parents(p.parent + (size_t)sg.b * p.B, i, mreg, p.status);
+                        mreg_built = true;
+                    }
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        const uint32_t vis = valid ? visible_bits(k0 + 32 * c, sg.P, p.B, mrow, p.W) : 0u;
+                        const uint32_t vis = !valid ? 0u
+                                             : mrow ? visible_bits(k0 + 32 * c, sg.P, p.B, mrow, p.W)
+                                                    : visible_bits_reg(k0 + 32 * c, sg.P, p.B, mreg, p.W);
 #pragma unroll
                         for (int e = 0; e < 32; ++e) s[c][e] = ((vis >> e) & 1u) ? s[c][e] : 0xff800000u;
                     }
@@ -1058,6 +1123,7 @@ int32_t launch_attn(const tv_attn_args *a, int ctas, void *workspace, cudaStream
     p.block_table = a->block_table_d;
     p.prefix_lens = a->prefix_lens_d;
     p.mask = a->mask_d;
+    p.parent = a->parent_d;
     p.o = static_cast<uint16_t *>(a->o_d);
     p.lse = a->lse_d;
     p.status = a->dev_status_d;

@@ -40,6 +40,14 @@ cudaError_t launch_accept(const uint16_t *logits, int V, const int32_t *draft, c
                           const uint32_t *mask, int B, int nb, int32_t *am, int32_t *n_acc, int32_t *path,
                           int32_t *bonus, int32_t *status, void *workspace, int num_sms, cudaStream_t stream);
 
+// Workspace bytes tv_accept_fused needs: the keys, then one 32-bit counter per sequence.
+size_t accept_fused_workspace_bytes(int V, int B, int nb);
+
+// Argmax and acceptance in one kernel; mask may be null.
+cudaError_t launch_accept_fused(const uint16_t *logits, int V, const int32_t *draft, const int32_t *parent,
+                                const uint32_t *mask, int B, int nb, int32_t *am, int32_t *n_acc, int32_t *path,
+                                int32_t *bonus, int32_t *status, void *workspace, int num_sms, cudaStream_t stream);
+
 // tv_accept on the library's own static scratch (no workspace argument).
 cudaError_t launch_accept_noalloc(const uint16_t *logits, int V, const int32_t *draft, const int32_t *parent,
                                   const uint32_t *mask, int B, int nb, int32_t *am, int32_t *n_acc, int32_t *path,
