@@ -34,8 +34,9 @@
 //      the workspace).
 //   4. Solve, warp per node in dataflow order: node i's r_i and o0_i rows are loaded
 //      (the warp's next node's while this one runs), node i waits (bounded, asleep on
-//      an mbarrier) until its parent's u row is written, then each ancestor costs one broadcast record load, one
-//      u-row load and a few fused multiply-adds (four ancestors in flight at a time).  Warps take nodes in index order, so the
+//      an mbarrier) until its parent's u row is written, then each ancestor costs one
+//      broadcast record load, one u-row load and a few fused multiply-adds (four
+//      ancestors in flight at a time).  Warps take nodes in index order, so the
 //      smallest unfinished node can always run: every wait ends.
 #include <cuda_runtime.h>
 

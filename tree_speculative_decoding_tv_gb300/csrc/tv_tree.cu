@@ -18,7 +18,11 @@
 // reductions), and only the lane owning a changed slot looks again.  The popped
 // entry's sibling successor joins the frontier at once (it was a candidate when
 // the round began); the round's new nodes add their first children only when the
-// round ends, which is what expanding the w nodes together means.
+// round ends, which is what expanding the w nodes together means.  Each slot keeps
+// its parent's score and its depth in registers, and each lane prepares its best
+// slot's successor before the reductions; a lane's best is a 64-bit max over its
+// slots (a tournament after a pop, one comparison after an insertion), so a pop's
+// dependent chain is the two reductions, a shuffle and a few register operations.
 #include <cuda_runtime.h>
 
 #include "tv_device.cuh"
@@ -68,37 +72,61 @@ __global__ void __launch_bounds__(32) build_tree_kernel(const float *__restrict_
     const float *lp = staged ? s_lp : g_lp;
 
     // The frontier lives in registers: slot j is register q = j / 32 of lane j % 32.
-    // rt = (parent << 16) | rank, or kEmpty; rf = the candidate's score.  Slots are
-    // never compacted: a parent whose ranks run out leaves an empty slot behind.
+    // rt = (parent << 16) | rank, or kEmpty; rf = the candidate's score; rp = its
+    // parent's score; rd = its depth.  Slots are never compacted: a parent whose
+    // ranks run out leaves an empty slot behind.
     constexpr uint32_t kEmpty = 0xFFFFFFFFu;
-    float rf[kTreeSlots];
+    float rf[kTreeSlots], rp[kTreeSlots];
     uint32_t rt[kTreeSlots];
+    int rd[kTreeSlots];
 #pragma unroll
     for (int q = 0; q < kTreeSlots; ++q) {
-        rf[q] = 0.f;
+        rf[q] = rp[q] = 0.f;
         rt[q] = kEmpty;
+        rd[q] = 0;
     }
-    uint32_t my_s = 0, my_t = kEmpty;  // this lane's best slot: score key, tie-break, score, register
-    float my_f = 0.f;
-    int my_q = 0;
-    auto lane_best = [&]() {
-        my_s = 0;
-        my_t = kEmpty;
-#pragma unroll
-        for (int q = 0; q < kTreeSlots; ++q) {
-            if (rt[q] != kEmpty) {
-                const uint32_t k = score_key(rf[q]);
-                if (k > my_s || (k == my_s && rt[q] < my_t)) {
-                    my_s = k;
-                    my_t = rt[q];
-                    my_f = rf[q];
-                    my_q = q;
-                }
-            }
+    // this lane's best slot (score key, tie-break, score, depth) and, ready before the
+    // pop that may take it, that slot's replacement: the parent's next rank.  A slot's
+    // order is one 64-bit value, (score key << 32) | ~tie-break (0 for an empty slot),
+    // so the best is a max over the slots.
+    uint32_t my_s = 0, my_t = kEmpty, rep_t = kEmpty;
+    float my_f = 0.f, my_p = 0.f, rep_f = 0.f;
+    int my_d = 0;
+    auto order = [&](float f, uint32_t t) -> uint64_t {
+        return t == kEmpty ? 0ull : (((uint64_t)score_key(f) << 32) | (uint64_t)(~t));
+    };
+    auto prepare = [&]() {  // the replacement of the best slot
+        const int c = (int)(my_t & 0xFFFFu);
+        if (my_t != kEmpty && c + 1 < K) {
+            rep_f = my_p + lp[(size_t)(my_d - 1) * K + c + 1];
+            rep_t = my_t + 1u;
+        } else {
+            rep_t = kEmpty;
         }
     };
-    // slot j <- (f, t), by its owner lane
-    auto put = [&](int j, float f, uint32_t t) {
+    auto lane_best = [&]() {  // full rescan: a tournament over the slots
+        uint64_t o[kTreeSlots];
+#pragma unroll
+        for (int q = 0; q < kTreeSlots; ++q) o[q] = order(rf[q], rt[q]);
+#pragma unroll
+        for (int step = 1; step < kTreeSlots; step <<= 1)
+#pragma unroll
+            for (int q = 0; q + step < kTreeSlots; q += 2 * step) o[q] = o[q] > o[q + step] ? o[q] : o[q + step];
+        my_s = (uint32_t)(o[0] >> 32);
+        my_t = ~(uint32_t)o[0];
+        if (o[0] == 0ull) my_t = kEmpty;
+#pragma unroll
+        for (int q = 0; q < kTreeSlots; ++q)
+            if (rt[q] == my_t && my_t != kEmpty) {
+                my_f = rf[q];
+                my_p = rp[q];
+                my_d = rd[q];
+            }
+        prepare();
+    };
+    // slot j <- a candidate (score f, tie-break t) with parent score ps at depth d, by its
+    // owner lane; the lane's best changes only if the newcomer beats it
+    auto put = [&](int j, float f, uint32_t t, float ps, int d) {
         if ((j & 31) == lane) {
             const int qj = j >> 5;
 #pragma unroll
@@ -106,8 +134,17 @@ __global__ void __launch_bounds__(32) build_tree_kernel(const float *__restrict_
                 if (q == qj) {
                     rf[q] = f;
                     rt[q] = t;
+                    rp[q] = ps;
+                    rd[q] = d;
                 }
-            lane_best();
+            if (order(f, t) > order(my_f, my_t)) {
+                my_s = score_key(f);
+                my_t = t;
+                my_f = f;
+                my_p = ps;
+                my_d = d;
+                prepare();
+            }
         }
     };
 
@@ -118,8 +155,10 @@ __global__ void __launch_bounds__(32) build_tree_kernel(const float *__restrict_
         rank[0] = 0;
     }
     int n = 1, made = 1;  // slots used, nodes made (warp-uniform)
-    put(0, 0.f + lp[0], 0u);
+    put(0, 0.f + lp[0], 0u, 0.f, 1);
     __syncwarp();
+    float last_f = 0.f;  // the last popped node's score and depth (the w = 1 round's only node)
+    int last_d = 0;
     while (made < B) {
         const int take = min(w, B - made);
         const int first = made;
@@ -130,40 +169,41 @@ __global__ void __launch_bounds__(32) build_tree_kernel(const float *__restrict_
             const uint32_t top_t = __reduce_min_sync(0xffffffffu, my_s == top_s ? my_t : kEmpty);
             const int owner = __ffs(__ballot_sync(0xffffffffu, my_s == top_s && my_t == top_t)) - 1;
             const float f = __shfl_sync(0xffffffffu, my_f, owner);
+            const int d = __shfl_sync(0xffffffffu, my_d, owner);
             const int u = (int)(top_t >> 16), c = (int)(top_t & 0xFFFFu), i = made;
-            const int d = dep[u] + 1;
             if (lane == 0) {
                 par[i] = (int16_t)u;
                 dep[i] = (int16_t)d;
                 rank[i] = (int16_t)c;
                 sc[i] = f;
             }
-            // the parent's next rank takes the popped slot, or the slot empties
+            // the parent's next rank (computed ahead) takes the popped slot, or the slot empties
             if (lane == owner) {
-                const int q = my_q;
-                const bool more = c + 1 < K;
-                const float nf = more ? sc[u] + lp[(size_t)(d - 1) * K + c + 1] : 0.f;
 #pragma unroll
-                for (int qq = 0; qq < kTreeSlots; ++qq)
-                    if (qq == q) {
-                        rf[qq] = nf;
-                        rt[qq] = more ? (((uint32_t)u << 16) | (uint32_t)(c + 1)) : kEmpty;
+                for (int q = 0; q < kTreeSlots; ++q)
+                    if (rt[q] == top_t) {
+                        rf[q] = rep_f;
+                        rt[q] = rep_t;
                     }
                 lane_best();
             }
+            last_f = f;
+            last_d = d;
             ++made;
             __syncwarp();
         }
         // the round's nodes join with their first child
         for (int i = first; i < made; ++i) {
-            const int di = dep[i];
+            const bool lastn = i == made - 1;
+            const float fi = lastn ? last_f : sc[i];
+            const int di = lastn ? last_d : dep[i];
             if (di < Dmax) {
-                put(n, sc[i] + lp[(size_t)di * K], (uint32_t)i << 16);
+                put(n, fi + lp[(size_t)di * K], (uint32_t)i << 16, fi, di + 1);
                 ++n;
             }
         }
         __syncwarp();
-        if (__reduce_max_sync(0xffffffffu, my_s) == 0) break;  // no candidate at all: B exceeds the tree
+        if (made == first) break;  // the round found no candidate at all: B exceeds the tree
     }
     if (made < B && lane == 0) report_status(status, TV_ERR_INVALID_ARG);
     for (int i = lane; i < B; i += 32) {
