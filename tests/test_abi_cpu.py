@@ -197,3 +197,16 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         binding.lib()
+
+
+def test_accept_binding_refuses_pageable_or_host_tree_arrays():
+    """The acceptance wrappers put outputs and workspaces on the tree arrays' device; host tree
+    arrays, or logits in pageable host memory, are refused before anything is launched."""
+    import torch
+    import tree_speculative_decoding_tv_gb300 as tv
+    logits = torch.zeros((4, 16), dtype=torch.bfloat16)
+    parent = torch.tensor([[-1, 0, 1, 2]], dtype=torch.int32)
+    draft = torch.zeros((1, 4), dtype=torch.int32)
+    for fn in (tv.accept, tv.accept_fused, tv.accept_noalloc):
+        with pytest.raises(ValueError):
+            fn(logits, draft, parent, None)

@@ -163,6 +163,17 @@ def attn(q, k_cache, v_cache, block_table, prefix_lens, mask, status=None, scale
     return o, lse
 
 
+def _logits_ok(logits, parent):
+    """The device every output and workspace lives on: the tree arrays'.  The logits may be
+    on that device or in pinned host memory (the kernel then reads them over the host link);
+    pageable host memory is refused."""
+    if not parent.is_cuda:
+        raise ValueError("parent (and draft) must be device tensors")
+    if not logits.is_cuda and not logits.is_pinned():
+        raise ValueError("logits must be a device tensor or pinned host memory")
+    return parent.device
+
+
 def accept_workspace_size(V: int, B: int, nb: int) -> int:
     return int(lib().tv_accept_workspace_size(int(V), int(B), int(nb)))
 
@@ -171,7 +182,7 @@ def accept(logits, draft, parent, mask, status=None, out=None, workspace=None, s
     """tv_accept: returns (argmax [nb*B], n_acc [nb], path [nb][B], bonus [nb]) int32 tensors."""
     nb, B = parent.shape
     V = logits.shape[-1]
-    dev = logits.device
+    dev = _logits_ok(logits, parent)
     if out is None:
         out = (torch.empty(nb * B, dtype=torch.int32, device=dev), torch.empty(nb, dtype=torch.int32, device=dev),
                torch.empty((nb, B), dtype=torch.int32, device=dev), torch.empty(nb, dtype=torch.int32, device=dev))
@@ -198,7 +209,7 @@ def accept_fused(logits, draft, parent, mask=None, status=None, out=None, worksp
     """
     nb, B = parent.shape
     V = logits.shape[-1]
-    dev = logits.device
+    dev = _logits_ok(logits, parent)
     if out is None:
         out = (torch.empty(nb * B, dtype=torch.int32, device=dev), torch.empty(nb, dtype=torch.int32, device=dev),
                torch.empty((nb, B), dtype=torch.int32, device=dev), torch.empty(nb, dtype=torch.int32, device=dev))
@@ -222,7 +233,7 @@ def accept_noalloc(logits, draft, parent, mask, status=None, out=None, stream=No
     """
     nb, B = parent.shape
     V = logits.shape[-1]
-    dev = logits.device
+    dev = _logits_ok(logits, parent)
     if out is None:
         out = (torch.empty(nb * B, dtype=torch.int32, device=dev), torch.empty(nb, dtype=torch.int32, device=dev),
                torch.empty((nb, B), dtype=torch.int32, device=dev), torch.empty(nb, dtype=torch.int32, device=dev))
