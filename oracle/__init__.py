@@ -63,8 +63,9 @@ def _load():
                                       C.c_int, P]
         lib.tvo_build_tree.argtypes = [P, P, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, P, P, P]
         lib.tvo_gdn_tree.argtypes = [P, P, P, P, P, P, P, C.c_int, C.c_int, C.c_int, C.c_int, P]
+        lib.tvo_gdn_commit.argtypes = [P, P, P, P, P, P, P, C.c_int, C.c_int, C.c_int, C.c_int, P]
         for f in (lib.tvo_build_mask, lib.tvo_attn, lib.tvo_lse_merge, lib.tvo_argmax, lib.tvo_accept,
-                  lib.tvo_kv_commit, lib.tvo_build_tree, lib.tvo_gdn_tree):
+                  lib.tvo_kv_commit, lib.tvo_build_tree, lib.tvo_gdn_tree, lib.tvo_gdn_commit):
             f.restype = C.c_int
         _lib = lib
     return _lib
@@ -211,3 +212,19 @@ def gdn_tree(q, k, v, alpha, beta, S0, parent):
     _check(_load().tvo_gdn_tree(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0), _ptr(parent),
                                 nb, B, H, D, _ptr(O)), "gdn_tree")
     return O
+
+
+def gdn_commit(k, v, alpha, beta, S0, n_acc, path):
+    """New committed Gated DeltaNet state (fp64 [nb][H][D][D]): the recurrence applied from S0
+    along path[b][0 .. n_acc[b]] (the accepted root path, root first)."""
+    k, v = _c(k, np.uint16), _c(v, np.uint16)
+    alpha, beta, S0 = _c(alpha, np.float32), _c(beta, np.float32), _c(S0, np.float32)
+    n_acc = _c(n_acc, np.int32).reshape(-1)
+    path = _c(path, np.int32)
+    nb, B = path.shape
+    H, D = k.shape[1], k.shape[2]
+    assert k.shape == (nb * B, H, D) and S0.shape == (nb, H, D, D) and alpha.shape == (nb * B, H)
+    S = np.zeros((nb, H, D, D), np.float64)
+    _check(_load().tvo_gdn_commit(_ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0), _ptr(n_acc), _ptr(path),
+                                  nb, B, H, D, _ptr(S)), "gdn_commit")
+    return S

@@ -530,3 +530,53 @@ int tvo_gdn_tree(const uint16_t *q, const uint16_t *k, const uint16_t *v, const 
     free(S); free(kv); free(path);
     return rc;
 }
+
+/* Commit of a Gated DeltaNet layer's state for the accepted branch (DFlash-TfM
+ * summary, §3: the state is committed only in the next decoding iteration, once
+ * the accepted branch is known, so nothing is rolled back).  Per sequence b and
+ * head h the recurrence
+ *   S_t = alpha_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T
+ * is applied from S0 to the nodes path[b][0] (the root) .. path[b][n_acc[b]] in
+ * that order, in fp64, and the result is the new committed state.  The path is
+ * checked as tvo_kv_commit checks it (root first, strictly increasing, inside the
+ * tree, 0 <= n_acc < B).
+ *   k, v: bf16 [nb*B][H][D]; alpha, beta: fp32 [nb*B][H]; S0: fp32 [nb][H][D][D];
+ *   n_acc: int32 [nb]; path: int32 [nb][B]; S_out: fp64 [nb][H][D][D]. */
+int tvo_gdn_commit(const uint16_t *k, const uint16_t *v, const float *alpha, const float *beta, const float *S0,
+                   const int32_t *n_acc, const int32_t *path, int nb, int B, int H, int D, double *S_out)
+{
+    if (!k || !v || !alpha || !beta || !S0 || !n_acc || !path || !S_out || nb < 0 || B < 1 || H < 1 || D < 1)
+        return TVO_ERR_ARG;
+    double *kk = malloc(sizeof(double) * (size_t)D * 3);
+    if (!kk) return TVO_ERR_ARG;
+    double *vv = kk + D, *ks = kk + 2 * D;
+    int rc = TVO_OK;
+    for (int b = 0; b < nb && rc == TVO_OK; b++) {
+        const int n = n_acc[b];
+        const int32_t *pr = path + (size_t)b * B;
+        if (n < 0 || n >= B || pr[0] != 0) { rc = TVO_ERR_ARG; break; }
+        for (int t = 1; t <= n; t++)
+            if (pr[t] <= pr[t - 1] || pr[t] >= B) rc = TVO_ERR_ARG;
+        if (rc != TVO_OK) break;
+        for (int h = 0; h < H; h++) {
+            double *S = S_out + ((size_t)b * H + h) * D * D;
+            const float *s0 = S0 + ((size_t)b * H + h) * D * D;
+            for (int x = 0; x < D * D; x++) S[x] = s0[x];
+            for (int t = 0; t <= n; t++) {
+                const size_t row = ((size_t)b * B + pr[t]) * H + h;
+                const double a = alpha[row], be = beta[row];
+                for (int d = 0; d < D; d++) { kk[d] = bf16_value(k[row * D + d]); vv[d] = bf16_value(v[row * D + d]); }
+                for (int c = 0; c < D; c++) {            /* ks = k^T S */
+                    double acc = 0.0;
+                    for (int r = 0; r < D; r++) acc += kk[r] * S[(size_t)r * D + c];
+                    ks[c] = acc;
+                }
+                for (int r = 0; r < D; r++)
+                    for (int c = 0; c < D; c++)
+                        S[(size_t)r * D + c] = a * (S[(size_t)r * D + c] - be * kk[r] * ks[c]) + be * kk[r] * vv[c];
+            }
+        }
+    }
+    free(kk);
+    return rc;
+}

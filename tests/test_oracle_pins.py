@@ -652,3 +652,90 @@ def test_gdn_invariant_under_sibling_relabelling():
     O2 = oracle.gdn_tree(w.q[old_of_new], w.k[old_of_new], w.v[old_of_new], w.alpha[old_of_new],
                          w.beta[old_of_new], w.S0, new_parent[None])
     assert np.allclose(O2[new_of_old], O, rtol=1e-12, atol=1e-14)
+
+
+# ------------------------------------------- Gated DeltaNet: commit of the accepted branch
+
+def _gdn_accepted(w, seed):
+    """An accepted root path per sequence: a random node's root path (root first)."""
+    rng = np.random.default_rng(seed)
+    n_acc = np.zeros(w.nb, np.int32)
+    path = np.full((w.nb, w.B), -1, np.int32)
+    for b in range(w.nb):
+        p = _gdn_path(w.parent[b], int(rng.integers(0, w.B)))
+        n_acc[b] = len(p) - 1
+        path[b, :len(p)] = p
+    return n_acc, path
+
+
+def test_gdn_commit_zero_write_strength_closed_form():
+    """beta = 0: the state only decays, S_new = (prod of alpha on the accepted path) S0."""
+    w = _gdn_small(21)
+    n_acc, path = _gdn_accepted(w, 1)
+    beta = np.zeros_like(w.beta)
+    S = oracle.gdn_commit(w.k, w.v, w.alpha, beta, w.S0, n_acc, path)
+    for b in range(w.nb):
+        rows = [b * w.B + j for j in path[b, :n_acc[b] + 1]]
+        g = np.prod(w.alpha[rows].astype(np.float64), axis=0)  # [H]
+        for h in range(w.H):
+            assert np.allclose(S[b, h], g[h] * w.S0[b, h].astype(np.float64), rtol=1e-12, atol=1e-14)
+
+
+def test_gdn_commit_matches_the_chunked_form():
+    """The chunked (WY) form along the accepted path p_0 .. p_n: with gamma_t the product of
+    alpha over p_0 .. p_t and r_ts = gamma_t / gamma_s, (I + X) U = beta (V - gamma K S0) with
+    X_ts = beta_t r_ts k_t.k_s (s < t), and S_new = gamma_n S0 + sum_s r_ns k_s u_s^T.  Solved
+    densely by numpy, it must equal the step-by-step recurrence."""
+    w = _gdn_small(22, nb=3, B=16, H=2, D=16)
+    n_acc, path = _gdn_accepted(w, 2)
+    S = oracle.gdn_commit(w.k, w.v, w.alpha, w.beta, w.S0, n_acc, path)
+    for b in range(w.nb):
+        rows = [b * w.B + j for j in path[b, :n_acc[b] + 1]]
+        n = len(rows)
+        for h in range(w.H):
+            Kk, Vv = _f64(w.k[rows, h]), _f64(w.v[rows, h])
+            al, be = w.alpha[rows, h].astype(np.float64), w.beta[rows, h].astype(np.float64)
+            S0 = w.S0[b, h].astype(np.float64)
+            gam = np.cumprod(al)
+            X = np.zeros((n, n))
+            for t in range(n):
+                for s in range(t):
+                    X[t, s] = be[t] * gam[t] / gam[s] * (Kk[t] @ Kk[s])
+            U = np.linalg.solve(np.eye(n) + X, be[:, None] * (Vv - gam[:, None] * (Kk @ S0)))
+            want = gam[-1] * S0 + (Kk * (gam[-1] / gam)[:, None]).T @ U
+            assert np.allclose(S[b, h], want, rtol=1e-9, atol=1e-11)
+
+
+def test_gdn_commit_agrees_with_the_tree_outputs():
+    """The accepted node's tree output is its state's read-out, so S_new^T q_{p_n} equals it."""
+    w = _gdn_small(23, nb=2, B=14, H=3, D=16)
+    n_acc, path = _gdn_accepted(w, 3)
+    S = oracle.gdn_commit(w.k, w.v, w.alpha, w.beta, w.S0, n_acc, path)
+    O = oracle.gdn_tree(w.q, w.k, w.v, w.alpha, w.beta, w.S0, w.parent)
+    for b in range(w.nb):
+        last = b * w.B + int(path[b, n_acc[b]])
+        for h in range(w.H):
+            assert np.allclose(S[b, h].T @ _f64(w.q[last, h]), O[last, h], rtol=1e-10, atol=1e-12)
+
+
+def test_gdn_commit_root_only_is_one_step():
+    """n_acc = 0 commits the root alone: one step of the recurrence from S0."""
+    w = _gdn_small(24, nb=1, B=6, H=2, D=8)
+    path = np.full((1, 6), -1, np.int32)
+    path[0, 0] = 0
+    S = oracle.gdn_commit(w.k, w.v, w.alpha, w.beta, w.S0, np.zeros(1, np.int32), path)
+    for h in range(w.H):
+        kk, vv = _f64(w.k[0, h]), _f64(w.v[0, h])
+        a, be = float(w.alpha[0, h]), float(w.beta[0, h])
+        S0 = w.S0[0, h].astype(np.float64)
+        want = a * (np.eye(w.D) - be * np.outer(kk, kk)) @ S0 + be * np.outer(kk, vv)
+        assert np.allclose(S[0, h], want, rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("bad", [[1, 2], [0, 3, 3], [0, 20]])
+def test_gdn_commit_rejects_a_path_that_is_not_a_root_path(bad):
+    w = _gdn_small(25, nb=1, B=12, H=1, D=8)
+    path = np.full((1, 12), -1, np.int32)
+    path[0, :len(bad)] = bad
+    with pytest.raises(oracle.OracleError):
+        oracle.gdn_commit(w.k, w.v, w.alpha, w.beta, w.S0, np.array([len(bad) - 1], np.int32), path)
