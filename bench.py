@@ -322,8 +322,9 @@ class Step:
         return self.time_stage(g, flush, steps)
 
     def time_gdn(self, flush, steps):
-        """Mean ms of tv_gdn_tree on the Gated DeltaNet tree workload (its own graph, same flush),
-        and that call's algorithmic bytes (q, k, v, gates, S0 in; O out)."""
+        """Mean ms of tv_gdn_tree on the Gated DeltaNet tree workload (its own graph, same flush)
+        and that call's algorithmic bytes (q, k, v, gates, S0 in; O out); then the same for
+        tv_gdn_commit along the tree's deepest root path (S0 in, the path's k/v/gates, S out)."""
         torch, tv = self.torch, self.tv
         g_w = wl.gdn_config(seed=5)
         dev = self.q.device
@@ -340,7 +341,30 @@ class Step:
             tv.gdn_tree(q, k, v, a, b, S0, par, out=out, workspace=ws, status=self.status)
         rows = g_w.nb * g_w.B * g_w.H
         nbytes = rows * g_w.D * (3 * 2 + 4) + rows * 8 + g_w.S0.nbytes + g_w.parent.nbytes
-        return self.time_stage(g, flush, steps), nbytes, g_w.name
+        ms = self.time_stage(g, flush, steps)
+        # the state commit along the deepest root path (the longest accepted branch)
+        h_par = g_w.parent[0]
+        dep = np.zeros(g_w.B, np.int64)
+        for i in range(1, g_w.B):
+            dep[i] = dep[h_par[i]] + 1
+        node, path = int(np.argmax(dep)), []
+        while node != -1:
+            path.append(node)
+            node = int(h_par[node])
+        path = path[::-1]
+        p_host = np.full((1, g_w.B), -1, np.int32)
+        p_host[0, :len(path)] = path
+        n_acc = torch.tensor([len(path) - 1], dtype=torch.int32, device=dev)
+        d_path = f(p_host)
+        S_new = torch.empty_like(S0)
+        tv.gdn_commit(k, v, a, b, S0, n_acc, d_path, out=S_new, status=self.status)
+        torch.cuda.synchronize()
+        gc = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gc):
+            tv.gdn_commit(k, v, a, b, S0, n_acc, d_path, out=S_new, status=self.status)
+        commit_ms = self.time_stage(gc, flush, steps)
+        commit_bytes = 2 * g_w.S0.nbytes + len(path) * g_w.H * (g_w.D * 4 + 8)
+        return ms, nbytes, g_w.name, commit_ms, commit_bytes, len(path)
 
     def time_stage(self, graph, flush, steps):
         """Mean ms of one stage graph replay, L2 flushed before each (CUDA events, current stream)."""
@@ -475,7 +499,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         raise RuntimeError("device status set in the end-to-end run")
     commit_ms, commit_bytes = st.time_commit(flush, args.steps)
     tree_ms = st.time_tree(args.config, flush, args.steps)
-    gdn_ms, gdn_bytes, gdn_name = st.time_gdn(flush, args.steps)
+    gdn_ms, gdn_bytes, gdn_name, gdn_commit_ms, gdn_commit_bytes, gdn_path_len = st.time_gdn(flush, args.steps)
     acc_fused_ms = st.time_accept_fused(flush, args.steps)
     acc_fused_nomask_ms = st.time_accept_fused(flush, args.steps, with_mask=False)
     forms_ms = {f: st.time_step_form(flush, args.steps, f) for f in ("mask", "folded", "fused")}
@@ -546,6 +570,9 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
                 "frac": gdn_bytes / (gdn_ms * 1e-3) / (peaks["hbm_gbs"] * 1e9),
                 "peak_source": peak_src + " burst", "algorithmic_bytes": gdn_bytes,
                 "traffic": profiled_traffic("gdn_tree_kernel", "tv_gdn.cu", "gdn128")},
+            "gdn_commit_ms": gdn_commit_ms, "gdn_commit_bytes": gdn_commit_bytes,
+            "gdn_commit_note": f"tv_gdn_commit of the GDN workload's state along its deepest root path "
+                               f"({gdn_path_len} nodes), its own graph",
             "gdn_tree_note": "tv_gdn_tree (Gated DeltaNet layer verified over the tree without rollback), its own "
                              "graph; a layer of the hybrid model's verification pass, not part of this attention "
                              "step; the dependent chain along each root path bounds it, not HBM",

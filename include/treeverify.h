@@ -269,6 +269,31 @@ TV_API int32_t tv_gdn_tree(const uint16_t *q_d, const uint16_t *k_d, const uint1
                            int32_t *dev_status_d, void *stream);
 
 /*
+ * Commit of a Gated DeltaNet layer's state for the accepted branch  [TfM-3g]
+ *
+ *   Tree verification (tv_gdn_tree) leaves the committed state S0 untouched; once
+ *   the accepted branch is known the state is committed by applying the
+ *   recurrence S_t = alpha_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T from
+ *   S0 to the nodes path[b][0] (the root) .. path[b][n_acc[b]], in that order.
+ *   k_d, v_d        bf16 [nb*B][H][D] (the tree's tokens, as given to tv_gdn_tree), 16-byte aligned
+ *   alpha_d, beta_d fp32 [nb*B][H]
+ *   S0_d            fp32 [nb][H][D][D] (rows: key dimension)
+ *   n_acc_d, path_d int32 [nb] and [nb][B] as tv_accept returns them
+ *   S_out_d         fp32 [nb][H][D][D] (out); may be S0_d (committed in place)
+ *   Shapes: D = 128, 1 <= B <= 256.
+ * One kernel launch (one CTA per (sequence, head)), a programmatic dependent of
+ * the previous kernel on the stream; it waits for it before reading anything, so
+ * it may directly follow tv_accept.  A path that is not a root path of at most B
+ * nodes (root first, strictly increasing, 0 <= n_acc < B) writes
+ * TV_ERR_INVALID_ARG to dev_status_d and copies S0 to S_out unchanged.
+ * Returns TV_OK (nb == 0 launches nothing), TV_ERR_INVALID_ARG, TV_ERR_UNSUPPORTED_SHAPE
+ * or TV_ERR_CUDA.
+ */
+TV_API int32_t tv_gdn_commit(const uint16_t *k_d, const uint16_t *v_d, const float *alpha_d, const float *beta_d,
+                             const float *S0_d, const int32_t *n_acc_d, const int32_t *path_d, int32_t nb,
+                             int32_t B, int32_t H, int32_t D, float *S_out_d, int32_t *dev_status_d, void *stream);
+
+/*
  * Commit of the accepted branch  [TfM-3] (the pages commit state once the
  * accepted branch is known; for a paged K/V cache this library reads that as
  * compaction in path order)

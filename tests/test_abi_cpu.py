@@ -192,6 +192,24 @@ def test_gdn_tree_argument_checks(L):
     assert L.tv_gdn_tree_workspace_size(1, 128, 32, 64) == 0
 
 
+def test_gdn_commit_argument_checks(L):
+    P = C.c_void_p
+    base = dict(k=P(FAKE), v=P(FAKE), a=P(FAKE), b=P(FAKE), s=P(FAKE), n=P(FAKE), path=P(FAKE), nb=1, B=128, H=32,
+                D=128, o=P(FAKE))
+
+    def call(**kw):
+        d = dict(base)
+        d.update(kw)
+        return L.tv_gdn_commit(d["k"], d["v"], d["a"], d["b"], d["s"], d["n"], d["path"], d["nb"], d["B"], d["H"],
+                               d["D"], d["o"], None, None)
+
+    assert call(nb=0) == 0
+    assert call(nb=-1) == 1 and call(H=0) == 1
+    assert call(B=0) == 3 and call(B=257) == 3 and call(D=64) == 3
+    assert call(k=None) == 1 and call(path=None) == 1 and call(o=None) == 1
+    assert call(k=P(FAKE + 8)) == 1 and call(s=P(FAKE + 2)) == 1 and call(n=P(FAKE + 1)) == 1
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "_lib", None)
     monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "missing.so"))

@@ -174,3 +174,97 @@ def test_gdn_tree_in_a_cuda_graph():
     torch.cuda.synchronize()
     assert st.item() == 0
     assert torch.equal(O, eager)
+
+
+# ------------------------------------------- commit of the accepted branch (tv_gdn_commit)
+
+def _accepted_paths(w, seed, deepest=False):
+    """Per sequence, a node's root path (root first): a random node, or the deepest one."""
+    rng = np.random.default_rng(seed)
+    n_acc = np.zeros(w.nb, np.int32)
+    path = np.full((w.nb, w.B), -1, np.int32)
+    for b in range(w.nb):
+        par = w.parent[b]
+        dep = np.zeros(w.B, int)
+        for i in range(1, w.B):
+            dep[i] = dep[par[i]] + 1
+        i = int(np.argmax(dep)) if deepest else int(rng.integers(0, w.B))
+        p = []
+        while i != -1:
+            p.append(i)
+            i = int(par[i])
+        p = p[::-1]
+        n_acc[b] = len(p) - 1
+        path[b, :len(p)] = p
+    return n_acc, path
+
+
+def _commit_tol(n_acc, ref):
+    """fp32 bound per element: (L + 2) length-128 dot products, each within 128 * 2^-24 of the
+    sum of its absolute products, <= sqrt(128) max|S| for unit keys, plus |v| <= 3 terms."""
+    L = n_acc.astype(np.float64) + 1
+    scale = 11.4 * np.abs(ref).max(axis=(1, 2, 3)) + 3.0
+    return ((L + 2) * 128 * 2.0 ** -24 * scale).reshape(-1, 1, 1, 1)
+
+
+def _commit_dev(w, n_acc, path, in_place=False):
+    d = _dev(w)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    S0 = d["S0"].clone()
+    out = tv.gdn_commit(d["k"], d["v"], d["alpha"], d["beta"], S0, torch.from_numpy(n_acc).cuda(),
+                        torch.from_numpy(path).cuda(), out=S0 if in_place else None, status=st)
+    torch.cuda.synchronize()
+    return out, int(st.item())
+
+
+COMMIT_CASES = {
+    "random paths, 3 sequences": (3, 48, 4, lambda r: wl.tree_best_first(r, 48, child_cap=4, max_depth=16), False),
+    "deepest path of a 256-node tree": (1, 256, 2, lambda r: wl.tree_best_first(r, 256, child_cap=4, max_depth=16),
+                                        True),
+    "chain of 64, accepted whole": (2, 64, 2, lambda r: _chain(64), True),
+    "single node": (2, 1, 3, lambda r: np.array([-1], np.int32), False),
+}
+
+
+@pytest.mark.parametrize("in_place", [False, True])
+@pytest.mark.parametrize("case", sorted(COMMIT_CASES))
+def test_gdn_commit_matches_oracle(case, in_place):
+    nb, B, H, trees, deepest = COMMIT_CASES[case]
+    w = wl.make_gdn_workload(case, nb, B, H, 128, trees, seed=zlib.crc32(case.encode()) + 1)
+    n_acc, path = _accepted_paths(w, 7, deepest)
+    out, st = _commit_dev(w, n_acc, path, in_place)
+    assert st == 0
+    ref = oracle.gdn_commit(w.k, w.v, w.alpha, w.beta, w.S0, n_acc, path)
+    err = np.abs(out.cpu().numpy().astype(np.float64) - ref) - _commit_tol(n_acc, ref)
+    assert err.max() <= 0, f"over tolerance by {err.max():.3e}"
+
+
+def test_gdn_commit_reads_out_the_accepted_nodes_tree_output():
+    """On the device too: the committed state read through the last accepted node's query
+    equals that node's tv_gdn_tree output."""
+    w = wl.gdn_config(seed=31)
+    n_acc, path = _accepted_paths(w, 8, deepest=True)
+    S, st = _commit_dev(w, n_acc, path)
+    O, st2 = _run(w)
+    assert st == 0 and st2 == 0
+    last = int(path[0, n_acc[0]])
+    q = torch.from_numpy(wl.bf16_to_f32(w.q[last]).astype(np.float32)).cuda()  # [H][D]
+    readout = torch.einsum("hrc,hr->hc", S[0], q)
+    # both sides approximate S_last^T q_last: the tree output within its per-node bound, the
+    # read-out within sqrt(128) (unit q) times the state's bound plus its own dot product
+    ref = oracle.gdn_commit(w.k, w.v, w.alpha, w.beta, w.S0, n_acc, path)
+    s_tol = float(_commit_tol(n_acc, ref).max())
+    smax = float(np.abs(ref).max())
+    tol = (n_acc[0] + 2) * 128 * 2.0 ** -24 * 4 + 128 ** 0.5 * s_tol + 128 * 2.0 ** -24 * 128 ** 0.5 * smax
+    assert (readout - O[last]).abs().max().item() <= tol
+
+
+def test_gdn_commit_rejects_a_bad_path():
+    w = wl.make_gdn_workload("bad", 2, 16, 2, 128, lambda r: _chain(16), seed=4)
+    n_acc = np.array([3, 2], np.int32)
+    path = np.full((2, 16), -1, np.int32)
+    path[0, :4] = [0, 1, 2, 3]
+    path[1, :3] = [0, 5, 5]  # not strictly increasing
+    out, st = _commit_dev(w, n_acc, path)
+    assert st == 1  # TV_ERR_INVALID_ARG
+    assert torch.equal(out[1].cpu(), torch.from_numpy(w.S0[1]))  # nothing committed there

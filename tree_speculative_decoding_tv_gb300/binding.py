@@ -25,7 +25,7 @@ TV_ERR_UNIMPLEMENTED = 6
 
 EXPORTED = ("tv_status_str", "tv_version", "tv_build_mask", "tv_attn_workspace_size", "tv_attn",
             "tv_accept_workspace_size", "tv_accept", "tv_accept_fused_workspace_size", "tv_accept_fused",
-            "tv_accept_noalloc", "tv_kv_commit", "tv_build_tree", "tv_gdn_tree_workspace_size", "tv_gdn_tree")
+            "tv_accept_noalloc", "tv_kv_commit", "tv_build_tree", "tv_gdn_tree_workspace_size", "tv_gdn_tree", "tv_gdn_commit")
 NOALLOC_MAX_ROWS = 8192  # TV_ACCEPT_NOALLOC_MAX_ROWS
 
 
@@ -86,6 +86,8 @@ def lib() -> C.CDLL:
         L.tv_gdn_tree_workspace_size.restype = C.c_size_t
         L.tv_gdn_tree.argtypes = [P, P, P, P, P, P, P, I, I, I, I, P, P, C.c_size_t, P, P]
         L.tv_gdn_tree.restype = I
+        L.tv_gdn_commit.argtypes = [P, P, P, P, P, P, P, I, I, I, I, P, P, P]
+        L.tv_gdn_commit.restype = I
         _lib = L
     return _lib
 
@@ -287,4 +289,17 @@ def gdn_tree(q, k, v, alpha, beta, S0, parent, out=None, workspace=None, status=
     rc = lib().tv_gdn_tree(_p(q), _p(k), _p(v), _p(alpha), _p(beta), _p(S0), _p(parent), nb, B, H, D, _p(out),
                            _p(workspace), workspace.numel() * workspace.element_size(), _p(status), _stream(stream))
     _check(rc, "tv_gdn_tree")
+    return out
+
+
+def gdn_commit(k, v, alpha, beta, S0, n_acc, path, out=None, status=None, stream=None):
+    """tv_gdn_commit: the new committed state (fp32 [nb][H][D][D]) after the accepted path;
+    out may be S0 itself (committed in place)."""
+    nb, B = path.shape
+    H, D = k.shape[1], k.shape[2]
+    if out is None:
+        out = torch.empty_like(S0)
+    rc = lib().tv_gdn_commit(_p(k), _p(v), _p(alpha), _p(beta), _p(S0), _p(n_acc), _p(path), nb, B, H, D, _p(out),
+                             _p(status), _stream(stream))
+    _check(rc, "tv_gdn_commit")
     return out

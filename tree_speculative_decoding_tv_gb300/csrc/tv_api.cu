@@ -250,6 +250,23 @@ int32_t tv_gdn_tree(const uint16_t *q_d, const uint16_t *k_d, const uint16_t *v_
     return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
 
+int32_t tv_gdn_commit(const uint16_t *k_d, const uint16_t *v_d, const float *alpha_d, const float *beta_d,
+                      const float *S0_d, const int32_t *n_acc_d, const int32_t *path_d, int32_t nb, int32_t B,
+                      int32_t H, int32_t D, float *S_out_d, int32_t *dev_status_d, void *stream)
+{
+    if (nb < 0 || H < 1) return TV_ERR_INVALID_ARG;
+    if (B < 1 || B > kMaxB || D != kHeadDim) return TV_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)nb * B * H * D >= (1ll << 31) || H > 65535 || nb > 65535) return TV_ERR_UNSUPPORTED_SHAPE;
+    if (nb == 0) return TV_OK;
+    if (!k_d || !v_d || !alpha_d || !beta_d || !S0_d || !n_acc_d || !path_d || !S_out_d) return TV_ERR_INVALID_ARG;
+    if (!aligned(k_d, 16) || !aligned(v_d, 16) || !aligned(S0_d, 4) || !aligned(S_out_d, 4) || !aligned(alpha_d, 4) ||
+        !aligned(beta_d, 4) || !aligned(n_acc_d, 4) || !aligned(path_d, 4) || !aligned(dev_status_d, 4))
+        return TV_ERR_INVALID_ARG;
+    cudaError_t e = tv::launch_gdn_commit(k_d, v_d, alpha_d, beta_d, S0_d, n_acc_d, path_d, nb, B, H, S_out_d,
+                                          dev_status_d, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
 int32_t tv_kv_commit(void *k_cache_d, void *v_cache_d, const int32_t *block_table_d, const int32_t *prefix_lens_d,
                      const int32_t *n_acc_d, const int32_t *path_d, int32_t nb, int32_t B, int32_t Hkv, int32_t D,
                      int32_t page_size, int32_t num_blocks, int32_t max_pages, int32_t *new_prefix_lens_d,

@@ -64,6 +64,11 @@ cudaError_t launch_gdn_tree(const uint16_t *q, const uint16_t *k, const uint16_t
                             const float *beta, const float *S0, const int32_t *parent, int nb, int B, int H, float *O,
                             void *workspace, int32_t *status, cudaStream_t stream);
 
+// Gated DeltaNet state commit along the accepted path (one CTA per (sequence, head)).
+cudaError_t launch_gdn_commit(const uint16_t *k, const uint16_t *v, const float *alpha, const float *beta,
+                              const float *S0, const int32_t *n_acc, const int32_t *path, int nb, int B, int H,
+                              float *S_out, int32_t *status, cudaStream_t stream);
+
 // Commit of the accepted branch's K/V (one CTA per (sequence, kv head)).
 cudaError_t launch_kv_commit(uint16_t *k_cache, uint16_t *v_cache, const int32_t *block_table,
                              const int32_t *prefix_lens, const int32_t *n_acc, const int32_t *path, int nb, int B,
