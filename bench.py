@@ -379,6 +379,22 @@ class Step:
         return float(np.mean([a.elapsed_time(b) for a, b in evs]))
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time: every rank calls it (an all-reduce MAX); one rank returns ms."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(nodes_per_rank: int, world: int, total_ms: float, steps: int) -> float:
+    """Whole-job throughput: every rank's nodes over the slowest rank's mean step time."""
+    return nodes_per_rank * world / (total_ms / steps * 1e-3)
+
+
 def run_gpu(args, rank: int, world: int, local_rank: int):
     import torch
     import torch.distributed as dist
@@ -423,10 +439,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     # per-stage times for the roofline: each stage's own graph, same flush, second timed loop
     attn_stage_ms = st.time_stage(st.g_attn, flush, args.steps)
     acc_stage_ms = st.time_stage(st.g_acc, flush, args.steps)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     clocks = sampler.stop(t_begin, t_end)
     if st.status.item() != 0:
         raise RuntimeError(f"device status {st.status.item()} in the timed region")
@@ -505,10 +518,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     forms_ms = {f: st.time_step_form(flush, args.steps, f) for f in ("mask", "folded", "fused")}
     if st.status.item() != 0:
         raise RuntimeError(f"device status {st.status.item()} in the commit stage")
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
 
     if rank != 0:
         return
@@ -536,7 +546,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         r["algorithmic_bytes"] = ab if src == "tv_attn.cu" else lb
     roof = attn_roof if t_attn >= t_acc else acc_roof
     out = {
-        "metric": METRIC, "value": nodes * world / (total_ms / args.steps * 1e-3), "unit": UNIT,
+        "metric": METRIC, "value": job_value(nodes, world, total_ms, args.steps), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; shapes of the pages' Qwen3 workloads, random values)",
@@ -581,7 +591,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         },
         "clocks": clocks,
         "gpu_launches": st.launches_per_step * args.steps,
-        "e2e": {"value": nodes * world / (e2e_ms / args.steps * 1e-3), "unit": UNIT, "h2d_bytes_per_step": bi,
+        "e2e": {"value": job_value(nodes, world, e2e_ms, args.steps), "unit": UNIT, "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo,
                 "pipelined": pipelined,
                 "note": "per step: q, logits, parent, draft tokens, block table, prefix lengths copied in from "
