@@ -223,6 +223,7 @@ COMMIT_CASES = {
                                         True),
     "chain of 64, accepted whole": (2, 64, 2, lambda r: _chain(64), True),
     "single node": (2, 1, 3, lambda r: np.array([-1], np.int32), False),
+    "33 heads, 2 sequences": (2, 32, 33, lambda r: wl.tree_best_first(r, 32, child_cap=3, max_depth=12), True),
 }
 
 
