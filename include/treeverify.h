@@ -249,12 +249,13 @@ TV_API int32_t tv_build_tree(const float *logp_d, const int32_t *tokens_d, int32
  *   parent_d        int32 [nb][B], topologically ordered (as tv_build_mask takes it)
  *   O_d             fp32 [nb*B][H][D] (out), 16-byte aligned
  *   workspace_d     >= tv_gdn_tree_workspace_size(nb, B, H, D) bytes, 16-byte
- *                   aligned: per (sequence, head) a B x B table of 16-byte ancestor
- *                   records, plus (B > 128) two fp32 [B][D] row blocks; concurrent
- *                   calls need their own
+ *                   aligned: per (sequence, head, 32-column value slice) a B x B
+ *                   table of 16-byte ancestor records, plus (B > 128) two fp32
+ *                   [B][32] row blocks; concurrent calls need their own
  *   Shapes: D = 128, 1 <= B <= 256.
- * One kernel launch per call (one CTA per (sequence, head); tensor cores form
- * K S0, Q S0 and the Gram blocks), a programmatic dependent of the previous kernel
+ * One kernel launch per call (4 CTAs per (sequence, head), one per 32 value
+ * columns; tensor cores form the Gram blocks and the slice's K S0 and Q S0), a
+ * programmatic dependent of the previous kernel
  * on the stream (it waits for it before reading anything).  A parent array that is
  * not topological writes TV_ERR_NOT_TOPOLOGICAL to dev_status_d (outputs
  * unspecified); an internal wait that runs out writes TV_ERR_TIMEOUT.

@@ -187,8 +187,9 @@ def test_gdn_tree_argument_checks(L):
     assert call(q=None) == 1 and call(s=None) == 1 and call(o=None) == 1
     assert call(k=P(FAKE + 8)) == 1 and call(s=P(FAKE + 4)) == 1 and call(a=P(FAKE + 2)) == 1
     assert call(ws=None) == 1 and call(wsb=16) == 1
-    assert L.tv_gdn_tree_workspace_size(1, 128, 32, 128) == 32 * 128 * 128 * 16
-    assert L.tv_gdn_tree_workspace_size(2, 256, 4, 128) == 2 * 4 * (256 * 256 * 16 + 2 * 256 * 128 * 4)
+    # per (sequence, head, value-column slice of 32): records [B][B]; B > 128 adds two [B][32] row slices
+    assert L.tv_gdn_tree_workspace_size(1, 128, 32, 128) == 32 * 4 * 128 * 128 * 16
+    assert L.tv_gdn_tree_workspace_size(2, 256, 4, 128) == 2 * 4 * 4 * (256 * 256 * 16 + 2 * 256 * 32 * 4)
     assert L.tv_gdn_tree_workspace_size(1, 128, 32, 64) == 0
 
 

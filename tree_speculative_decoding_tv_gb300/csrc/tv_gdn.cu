@@ -13,30 +13,37 @@
 // (X_ij = beta_i r_ij k_i.k_j and Y_ij = r_ij q_i.k_j are the pages' interaction
 // matrices, restricted to ancestors by the tree mask.)
 //
-// GPU form: one fused kernel, one CTA per (sequence, head), 16 warps.
+// GPU form: one fused kernel, 16 warps per CTA.  The value columns are split: u_i
+// and o_i restricted to a set of value columns need only those columns of S0 and
+// v_i (the Gram entries and decays are shared by all columns), so each (sequence,
+// head) runs as 4 CTAs of 32 value columns each, every one doing the whole tree
+// for its columns (the Gram part is recomputed per CTA: it is the cheap part).
 //   1. Stage, with every global load issued at once: the K and Q rows (cp.async)
-//      as K-major 128-byte-swizzled bf16 tiles, the v rows (B <= 128), S0 (through
-//      registers, split into bf16 hi + lo parts, S0 = hi + lo to ~2^-17, as MN-major
-//      swizzled tiles), the parent array (validated), and a walk up each node's root
-//      path that sets its ancestor bits and writes, per ancestor j (slot = distance
-//      to i - 1), the record (j, r_ij): r_ij is the running product of the alphas
-//      passed, and gamma_i the product over the whole path.
+//      as K-major 128-byte-swizzled bf16 tiles, the slice's v columns (B <= 128),
+//      the slice of S0 (through registers, split into bf16 hi + lo parts, S0 = hi +
+//      lo to ~2^-17, transposed into one K-major swizzled 64-row tile), the parent
+//      array (validated), and a walk up each node's root path that sets its
+//      ancestor bits and writes, per ancestor j (slot = distance to i - 1), the
+//      record (j, r_ij): r_ij is the running product of the alphas passed, and
+//      gamma_i the product over the whole path.
 //   2. Tensor cores (tcgen05, fp32 accumulators in TMEM): the Gram blocks K K^T and
-//      Q K^T (committed first, so the epilogue starts on them early), then K S0 and
-//      Q S0 (each as K hi + K lo, so fp32-accurate), 128 nodes per M tile (two tiles
-//      and three passes for B > 128, so a pass never needs more than the 512 TMEM
-//      columns).
+//      Q K^T (committed first, so the epilogue starts on them early), then the
+//      slice's K S0 and Q S0 (N = 64: the hi and lo parts side by side, added in the
+//      epilogue, so fp32-accurate), 128 nodes per M tile (two tiles and three passes
+//      for B > 128).
 //   3. Epilogue, all warps (warp w reads TMEM lanes 32 (w % 4).. and columns
-//      32 (w / 4)..): r_i = beta_i (v_i - gamma_i (K S0)_i) and o0_i = gamma_i (Q S0)_i
-//      per node, and, for each ancestor j of i (its bit in i's mask; its slot is the
+//      32 (w / 4)..): for each ancestor j of i (its bit in i's mask; its slot is the
 //      count of mask bits above it), the pair (k_i.k_j, q_i.k_j) into j's record
 //      (the first 24 records of a node in shared memory when B <= 128, the rest in
-//      the workspace).
-//   4. Solve, warp per node in dataflow order: node i's r_i and o0_i rows are loaded
-//      (the warp's next node's while this one runs), node i waits (bounded, asleep on
-//      an mbarrier) until its parent's u row is written, then each ancestor costs one
-//      broadcast record load, one u-row load and a few fused multiply-adds (four
-//      ancestors in flight at a time).  Warps take nodes in index order, so the
+//      the workspace); the first four warps also form the slice of
+//      r_i = beta_i (v_i - gamma_i (K S0)_i) and o0_i = gamma_i (Q S0)_i.
+//   4. Solve, warp per node in dataflow order, one value column per lane: node i's
+//      r_i and o0_i rows are loaded (the warp's next node's while this one runs);
+//      node i waits (bounded, asleep on an mbarrier) for its grandparent's u row and
+//      adds the terms of every ancestor above its parent (each one broadcast record
+//      load, one u-row load and two fused multiply-adds, four ancestors in flight),
+//      then waits for its parent's row and adds that term alone, so the chain down
+//      the tree costs one term per level.  Warps take nodes in index order, so the
 //      smallest unfinished node can always run: every wait ends.
 #include <cuda_runtime.h>
 
@@ -52,12 +59,19 @@ constexpr int kGdnWarps = kGdnThreads / 32;
 constexpr uint32_t kGdnTile = 128 * 128 * 2;  // one 128 x 128 bf16 operand tile
 constexpr uint32_t kGdnHalf = kGdnTile / 2;   // one 64-column (128-byte) swizzle block of it
 constexpr int kGdnMaskWords = kGdnMaxB / 32;
-constexpr uint32_t kGdnRowBytes = kGdnD * 4;  // an fp32 row (r, u, o0)
+constexpr int kGdnSlices = 4;                      // CTAs per (sequence, head), one per value-column slice
+constexpr int kGdnCols = kGdnD / kGdnSlices;       // 32 value columns per CTA: one per lane in the solve
+constexpr uint32_t kGdnRowBytes = kGdnCols * 4;    // an fp32 row slice (r, u, o0)
+// The S0 slice as one B operand, transposed and K-major: rows 0..31 its hi part, rows
+// 32..63 its lo part (value column n in rows n and 32 + n), 128 keys per row, bf16
+constexpr uint32_t kGdnSTile = 2 * kGdnCols * kGdnD * 2;
+constexpr uint32_t kGdnSHalf = kGdnSTile / 2;  // its 64-key (128-byte) swizzle column block
+static_assert(kGdnCols == 32, "one value column per lane");
 constexpr int kGdnSmemSlots = 24;             // records per node kept in shared memory (B <= 128)
 constexpr uint32_t kGdnTmemCols = 512;
-// TMEM columns of one pass: K S0, Q S0, then the K K^T and Q K^T blocks
+// TMEM columns of one pass: K S0, Q S0 (32 each), then the K K^T and Q K^T blocks
 constexpr uint32_t kColKS = 0, kColQS = 128, kColKK = 256, kColQK = 384;
-constexpr uint32_t kIdescS = umma_idesc_bf16(128, 128, 1);  // B = S0 part, MN-major
+constexpr uint32_t kIdescS = umma_idesc_bf16(128, 2 * kGdnCols, 0);  // B = the S0 slice's hi and lo rows
 constexpr uint32_t kIdescG = umma_idesc_bf16(128, 128, 0);  // B = K tile, K-major
 
 // One ancestor j of a node i: its index, the decay ratio r_ij (written by the root
@@ -68,8 +82,8 @@ struct __align__(16) GdnRec {
 };
 
 struct GdnSmem {
-    uint32_t k, q, s_hi, s_lo, tiles_end;
-    uint32_t recs, v;  // B <= 128 only: records [128][kGdnSmemSlots], v rows [128][D] bf16
+    uint32_t k, q, s, tiles_end;
+    uint32_t recs, v;  // B <= 128 only: records [kGdnSmemSlots][128] (slot-major), v rows [128][32 columns] bf16
     uint32_t done, parent, alpha, beta, gamma, depth, yii, mask, total;
 };
 
@@ -79,16 +93,15 @@ __host__ __device__ inline GdnSmem gdn_smem_layout(int B)
     const uint32_t T = (uint32_t)(B + 127) / 128;
     L.k = 0;
     L.q = T * kGdnTile;
-    L.s_hi = 2 * T * kGdnTile;
-    L.s_lo = L.s_hi + kGdnTile;
-    L.tiles_end = L.s_lo + kGdnTile;
+    L.s = 2 * T * kGdnTile;
+    L.tiles_end = L.s + kGdnSTile;
     uint32_t o = L.tiles_end;
     L.recs = L.v = 0;
     if (B <= 128) {
         L.recs = o;
         o += 128u * kGdnSmemSlots * 16u;
         L.v = o;
-        o += 128u * kGdnD * 2u;
+        o += 128u * kGdnCols * 2u;
     }
     const uint32_t a = 4u * (uint32_t)B;
     L.done = o; o += 2 * a;  // one mbarrier per node
@@ -103,8 +116,13 @@ __host__ __device__ inline GdnSmem gdn_smem_layout(int B)
     return L;
 }
 
-// byte offset of logical 16-byte chunk c (0..31) of fp32 row i: chunks swizzled by (i & 7)
-__device__ __forceinline__ uint32_t row_chunk(int i, int c) { return (uint32_t)i * kGdnRowBytes + ((c ^ (i & 7)) << 4); }
+// byte offset of column c (0..31) of the fp32 row slice of node i: 16-byte chunks
+// swizzled by (i & 7), so a warp's one-row reads and its 32-row chunk writes are
+// both free of bank conflicts
+__device__ __forceinline__ uint32_t row_col(int i, int c)
+{
+    return (uint32_t)i * kGdnRowBytes + ((((uint32_t)c >> 2) ^ ((uint32_t)i & 7u)) << 4) + ((uint32_t)c & 3u) * 4u;
+}
 
 // round-to-nearest bf16 bits of x
 __device__ __forceinline__ uint32_t bf16_bits(float x)
@@ -114,9 +132,9 @@ __device__ __forceinline__ uint32_t bf16_bits(float x)
     return r;
 }
 
-__device__ __forceinline__ void st_shared_v2(uint32_t addr, uint32_t a, uint32_t b)
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint32_t x)
 {
-    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"((uint16_t)x) : "memory");
 }
 
 // 16-byte global -> shared copy, zero-filled when !valid (nothing is read then)
@@ -130,16 +148,12 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-__device__ __forceinline__ void fma_row(float4 &u, float4 &o, float x, float y, const float4 &uj)
-{
-    u.x -= x * uj.x; u.y -= x * uj.y; u.z -= x * uj.z; u.w -= x * uj.w;
-    o.x += y * uj.x; o.y += y * uj.y; o.z += y * uj.z; o.w += y * uj.w;
-}
-
-// record slot `slot` of node i: the first kGdnSmemSlots in shared memory when B <= 128
+// record slot `slot` of node i: the first kGdnSmemSlots in shared memory when B <= 128,
+// slot-major there (the threads of a warp, one node each, write one slot side by side,
+// free of bank conflicts), node-major in the workspace
 __device__ __forceinline__ GdnRec *rec_at(GdnRec *s_recs, GdnRec *g_recs, bool small, int B, int i, int slot)
 {
-    return (small && slot < kGdnSmemSlots) ? s_recs + i * kGdnSmemSlots + slot : g_recs + (size_t)i * B + slot;
+    return (small && slot < kGdnSmemSlots) ? s_recs + slot * 128 + i : g_recs + (size_t)i * B + slot;
 }
 
 __global__ void __launch_bounds__(kGdnThreads, 1) gdn_tree_kernel(
@@ -165,17 +179,19 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_tree_kernel(
     uint32_t *s_mask = reinterpret_cast<uint32_t *>(gb + L.mask);
 
     const int h = blockIdx.x, b = blockIdx.y, nb = gridDim.y;
+    const int c0 = blockIdx.z * kGdnCols;  // this CTA's value columns c0 .. c0 + 31
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int T = (B + 127) >> 7;
     const bool small = B <= 128;  // one M tile: r / u and o0 rows, records and v rows fit in shared memory
-    const size_t bh = (size_t)b * H + h;
-    // workspace: records [nb][H][B][B]; for B > 128 also r and o0 rows [nb][H][B][D] each
-    GdnRec *g_recs = reinterpret_cast<GdnRec *>(ws) + bh * B * B;
+    const size_t bh = (size_t)b * H + h, bhs = bh * kGdnSlices + blockIdx.z;
+    // workspace, per (sequence, head, slice): records [B][B]; for B > 128 also r and o0
+    // row slices [B][32] each
+    GdnRec *g_recs = reinterpret_cast<GdnRec *>(ws) + bhs * B * B;
     GdnRec *s_recs = reinterpret_cast<GdnRec *>(gb + L.recs);
-    float *g_rows = reinterpret_cast<float *>(reinterpret_cast<GdnRec *>(ws) + (size_t)nb * H * B * B);
-    uint8_t *r_rows = small ? gb : reinterpret_cast<uint8_t *>(g_rows + bh * B * kGdnD);
+    float *g_rows = reinterpret_cast<float *>(reinterpret_cast<GdnRec *>(ws) + (size_t)nb * H * kGdnSlices * B * B);
+    uint8_t *r_rows = small ? gb : reinterpret_cast<uint8_t *>(g_rows + bhs * B * kGdnCols);
     uint8_t *o0_rows = small ? gb + 128 * kGdnRowBytes
-                             : reinterpret_cast<uint8_t *>(g_rows + ((size_t)nb * H + bh) * B * kGdnD);
+                             : reinterpret_cast<uint8_t *>(g_rows + ((size_t)nb * H * kGdnSlices + bhs) * B * kGdnCols);
     const uint32_t bar_g = smem_u32(&s_bar[0]), bar_s = smem_u32(&s_bar[1]);
 
     pdl_wait_primary();  // every input may come from the previous kernel
@@ -203,20 +219,21 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_tree_kernel(
         const uint16_t *src = (which ? q : k) + (((size_t)b * B + min(i, B - 1)) * H + h) * kGdnD + c * 8;
         cp_async16(dst, src, i < B);
     }
-    if (small) {  // v rows [i][16 chunks], chunks swizzled by (i & 7)
-        for (int idx = tid; idx < B * 16; idx += kGdnThreads) {
-            const int i = idx >> 4, c = idx & 15;
-            cp_async16(base + L.v + (uint32_t)i * 256 + ((uint32_t)(c ^ (i & 7)) << 4),
-                       v + (((size_t)b * B + i) * H + h) * kGdnD + c * 8, true);
+    if (small) {  // the slice's v columns [i][4 chunks], chunks swizzled by (i & 3)
+        for (int idx = tid; idx < B * 4; idx += kGdnThreads) {
+            const int i = idx >> 2, c = idx & 3;
+            cp_async16(base + L.v + (uint32_t)i * 64 + ((uint32_t)(c ^ (i & 3)) << 4),
+                       v + (((size_t)b * B + i) * H + h) * kGdnD + c0 + c * 8, true);
         }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
-    constexpr int kPer = kGdnD * kGdnD / 4 / kGdnThreads;  // S0: 8 float4 per thread
+    constexpr int kPer = kGdnD * kGdnCols / 4 / kGdnThreads;  // the S0 slice: 2 float4 per thread
+    static_assert(kPer * 4 * kGdnThreads == kGdnD * kGdnCols, "S0 slice split");
     float4 sv[kPer];
-    {
-        const float4 *src = reinterpret_cast<const float4 *>(S0 + bh * kGdnD * kGdnD);
 #pragma unroll
-        for (int u = 0; u < kPer; ++u) sv[u] = src[tid + u * kGdnThreads];
+    for (int u = 0; u < kPer; ++u) {  // key row r, columns c0 + 4 (idx % 8) ..
+        const int idx = tid + u * kGdnThreads;
+        sv[u] = *reinterpret_cast<const float4 *>(S0 + (bh * kGdnD + (idx >> 3)) * kGdnD + c0 + (idx & 7) * 4);
     }
 
     bool bad = false;
@@ -228,7 +245,7 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_tree_kernel(
             s_parent[i] = pv[e];
             s_alpha[i] = av[e];
             s_beta[i] = bv[e];
-            mbar_init(done_bar + 8u * (uint32_t)i, 1);
+            mbar_init(done_bar + 8u * (uint32_t)i, 32);  // one arrival per lane of the solving warp
         }
     }
     if (tid == 0) {
@@ -265,21 +282,22 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_tree_kernel(
         s_depth[i] = slot;
         s_gamma[i] = r;
     }
-    // S0 [key r][value c] -> hi and lo bf16 parts, MN-major 128B-swizzled (key rows of 64 values)
+    // the S0 slice [key r][value c0 + n] -> hi and lo bf16 parts, transposed: row n
+    // holds keys 0..127 (K-major, 128-byte swizzled, like the K and Q tiles)
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
-        const int idx = tid + u * kGdnThreads, r = idx >> 5, c = (idx & 31) * 4;
+        const int idx = tid + u * kGdnThreads, r = idx >> 3, n0 = (idx & 7) * 4;
         const float x[4] = {sv[u].x, sv[u].y, sv[u].z, sv[u].w};
-        uint32_t hi[4], lo[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            hi[e] = bf16_bits(x[e]);
-            lo[e] = bf16_bits(x[e] - __uint_as_float(hi[e] << 16));
+            const uint32_t hi = bf16_bits(x[e]);
+            const uint32_t lo = bf16_bits(x[e] - __uint_as_float(hi << 16));
+            const int n = n0 + e;  // row n: hi; row 32 + n: lo (same swizzle: 32 is a multiple of 8)
+            const uint32_t off = (uint32_t)(r >> 6) * kGdnSHalf + (uint32_t)n * 128 +
+                                 ((uint32_t)(((r & 63) >> 3) ^ (n & 7)) << 4) + (uint32_t)(r & 7) * 2;
+            st_shared_u16(base + L.s + off, hi);
+            st_shared_u16(base + L.s + off + kGdnCols * 128, lo);
         }
-        const uint32_t off = (uint32_t)(c >> 6) * kGdnHalf + (uint32_t)r * 128 +
-                             ((uint32_t)(((c & 63) >> 3) ^ (r & 7)) << 4) + (uint32_t)(c & 7) * 2;
-        st_shared_v2(base + L.s_hi + off, hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16));
-        st_shared_v2(base + L.s_lo + off, lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
     }
     cp_async_wait_all();
     fence_proxy_async_smem();  // the tensor core reads what these threads wrote
@@ -311,27 +329,25 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_tree_kernel(
                 for (int kk = 0; kk < kGdnD / 16; ++kk) {
                     const uint32_t off = (uint32_t)(kk >> 2) * kGdnHalf + (uint32_t)(kk & 3) * 32;
                     const uint32_t acc = kk > 0 ? 1u : 0u;
-                    const uint64_t sh = sdesc_mnmajor_sw128(base + L.s_hi + kk * 2048, kGdnHalf);
-                    const uint64_t sl = sdesc_mnmajor_sw128(base + L.s_lo + kk * 2048, kGdnHalf);
-                    umma_bf16_ss(tmem + kColKS, sdesc_kmajor_sw128(kA + off), sh, kIdescS, acc);
-                    umma_bf16_ss(tmem + kColKS, sdesc_kmajor_sw128(kA + off), sl, kIdescS, 1u);
-                    umma_bf16_ss(tmem + kColQS, sdesc_kmajor_sw128(qA + off), sh, kIdescS, acc);
-                    umma_bf16_ss(tmem + kColQS, sdesc_kmajor_sw128(qA + off), sl, kIdescS, 1u);
+                    const uint64_t sd =
+                        sdesc_kmajor_sw128(base + L.s + (uint32_t)(kk >> 2) * kGdnSHalf + (uint32_t)(kk & 3) * 32);
+                    umma_bf16_ss(tmem + kColKS, sdesc_kmajor_sw128(kA + off), sd, kIdescS, acc);
+                    umma_bf16_ss(tmem + kColQS, sdesc_kmajor_sw128(qA + off), sd, kIdescS, acc);
                 }
                 umma_commit(bar_s);
             }
         }
         const int i = 128 * m + 32 * quarter + lane;  // this thread's TMEM lane = node
         const bool live = i < B;
+        const bool s_warp = has_s && chunk == 0;  // the first four warps form the r and o0 row slices
         uint4 vv[4];
-        if (has_s && live) {
+        if (s_warp && live) {
             if (small) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    vv[e] = *reinterpret_cast<const uint4 *>(gb + L.v + i * 256 + (((4 * chunk + e) ^ (i & 7)) << 4));
+                    vv[e] = *reinterpret_cast<const uint4 *>(gb + L.v + i * 64 + ((e ^ (i & 3)) << 4));
             } else {
-                const uint4 *vr =
-                    reinterpret_cast<const uint4 *>(v + (((size_t)b * B + i) * H + h) * kGdnD + 32 * chunk);
+                const uint4 *vr = reinterpret_cast<const uint4 *>(v + (((size_t)b * B + i) * H + h) * kGdnD + c0);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) vv[e] = vr[e];
             }
@@ -372,17 +388,26 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_tree_kernel(
         }
         if (ok && has_s) {
             ok = __all_sync(0xffffffffu, mbar_wait(bar_s, (uint32_t)(p & 1), &s_abort, status));
-            if (ok) {
+            if (ok && s_warp) {
                 tc_fence_after();
-                uint32_t x[32], y[32];
-                tmem_ld32(t_lane + kColKS + 32 * chunk, x);
-                tmem_ld32(t_lane + kColQS + 32 * chunk, y);
+                uint32_t x[32], y[32], xl[32];
+                // (K S0)_i = K hi + K lo: the two halves of the 64 accumulator columns
+                tmem_ld32(t_lane + kColKS, x);
+                tmem_ld32(t_lane + kColKS + kGdnCols, xl);
                 tmem_ld_wait(x);
-                reg_order(y);
+                reg_order(xl);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) x[c] = __float_as_uint(__uint_as_float(x[c]) + __uint_as_float(xl[c]));
+                tmem_ld32(t_lane + kColQS, y);
+                tmem_ld32(t_lane + kColQS + kGdnCols, xl);
+                tmem_ld_wait(y);
+                reg_order(xl);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) y[c] = __float_as_uint(__uint_as_float(y[c]) + __uint_as_float(xl[c]));
                 if (live) {
                     const float bi = s_beta[i], gi = s_gamma[i];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {  // 16-byte chunk 8 chunk + e: columns 32 chunk + 4 e ..
+                    for (int e = 0; e < 8; ++e) {  // 16-byte chunk e: slice columns 4 e ..
                         const uint4 w = vv[e >> 1];
                         const uint32_t w0 = (e & 1) ? w.z : w.x, w1 = (e & 1) ? w.w : w.y;
                         const float vx[4] = {bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1)};
@@ -395,7 +420,7 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_tree_kernel(
                         o4.y = gi * __uint_as_float(y[4 * e + 1]);
                         o4.z = gi * __uint_as_float(y[4 * e + 2]);
                         o4.w = gi * __uint_as_float(y[4 * e + 3]);
-                        const uint32_t off = row_chunk(i, 8 * chunk + e);
+                        const uint32_t off = row_col(i, 4 * e);
                         *reinterpret_cast<float4 *>(r_rows + off) = r4;  // over the finished tiles when small
                         *reinterpret_cast<float4 *>(o0_rows + off) = o4;
                     }
@@ -412,51 +437,54 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_tree_kernel(
     }
     if (s_abort) return;
 
-    // ---- solve: warp per node, in index order; the next node's rows load during this one
-    uint8_t *s_u = gb;  // u rows (fp32, swizzled 16-byte chunks) over the finished operand tiles
-    float4 r_n = make_float4(0.f, 0.f, 0.f, 0.f), o_n = r_n;
+    // ---- solve: warp per node, in index order, lane = value column; the next node's
+    // rows load during this one
+    uint8_t *s_u = gb;  // u row slices (fp32, swizzled 16-byte chunks) over the finished operand tiles
+    float r_n = 0.f, o_n = 0.f;
     if (warp < B) {
-        r_n = *reinterpret_cast<const float4 *>(r_rows + row_chunk(warp, lane));
-        o_n = *reinterpret_cast<const float4 *>(o0_rows + row_chunk(warp, lane));
+        r_n = *reinterpret_cast<const float *>(r_rows + row_col(warp, lane));
+        o_n = *reinterpret_cast<const float *>(o0_rows + row_col(warp, lane));
     }
     for (int i = warp; i < B; i += kGdnWarps) {
         const int p = s_parent[i], di = s_depth[i];
         const float bi = s_beta[i], yii = s_yii[i];
-        float4 u = r_n, o = o_n;
+        float u = r_n, o = o_n;
         if (i + kGdnWarps < B) {
-            r_n = *reinterpret_cast<const float4 *>(r_rows + row_chunk(i + kGdnWarps, lane));
-            o_n = *reinterpret_cast<const float4 *>(o0_rows + row_chunk(i + kGdnWarps, lane));
+            r_n = *reinterpret_cast<const float *>(r_rows + row_col(i + kGdnWarps, lane));
+            o_n = *reinterpret_cast<const float *>(o0_rows + row_col(i + kGdnWarps, lane));
         }
-        // wait (bounded; the hardware suspends the warp) until the parent's u row is
-        // written: then every ancestor's is, and the acquire makes them visible
-        if (p >= 0 && !__all_sync(0xffffffffu, mbar_wait(done_bar + 8u * (uint32_t)p, 0, &s_abort, status))) break;
-        auto accumulate = [&](const GdnRec *recs_i) {
-            for (int l0 = 0; l0 < di; l0 += 4) {  // four ancestors in flight
-                GdnRec rc[4];
-                float4 uj[4];
+        // Ancestor terms in slot order from slot l0 on, up to slot l1: four in flight at a time
+        // (records from shared memory), or, for deep paths, 32 records at a time, one per
+        // lane, then broadcast.
+        auto accumulate = [&](int l0, int l1) {
+            if (small && l1 <= kGdnSmemSlots) {
+                const GdnRec *recs_i = s_recs + i;  // slot l at recs_i[128 l]
+                for (int l = l0; l < l1; l += 4) {
+                    GdnRec rc[4];
+                    float uj[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (l0 + e < di) rc[e] = recs_i[l0 + e];
+                    for (int e = 0; e < 4; ++e)
+                        if (l + e < l1) rc[e] = recs_i[128 * (l + e)];
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (l0 + e < di) uj[e] = *reinterpret_cast<const float4 *>(s_u + row_chunk(rc[e].j, lane));
+                    for (int e = 0; e < 4; ++e)
+                        if (l + e < l1) uj[e] = *reinterpret_cast<const float *>(s_u + row_col(rc[e].j, lane));
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (l0 + e < di) fma_row(u, o, bi * rc[e].r * rc[e].kk, rc[e].r * rc[e].qk, uj[e]);
+                    for (int e = 0; e < 4; ++e)
+                        if (l + e < l1) {
+                            u -= bi * rc[e].r * rc[e].kk * uj[e];
+                            o += rc[e].r * rc[e].qk * uj[e];
+                        }
+                }
+                return;
             }
-        };
-        if (small && di <= kGdnSmemSlots) {
-            accumulate(s_recs + i * kGdnSmemSlots);
-        } else {  // deep paths: 32 records at a time, one per lane, then broadcast
-            for (int l0 = 0; l0 < di; l0 += 32) {
-                const int n = min(di - l0, 32);
+            for (int lb = l0; lb < l1; lb += 32) {
+                const int n = min(l1 - lb, 32);
                 GdnRec mine = {0, 0.f, 0.f, 0.f};
-                if (lane < n) mine = *rec_at(s_recs, g_recs, small, B, i, l0 + lane);
+                if (lane < n) mine = *rec_at(s_recs, g_recs, small, B, i, lb + lane);
                 const float xm = bi * mine.r * mine.kk, ym = mine.r * mine.qk;
                 for (int e0 = 0; e0 < n; e0 += 4) {
                     int jj[4];
-                    float xx[4], yy[4];
-                    float4 uj[4];
+                    float xx[4], yy[4], uj[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         jj[e] = __shfl_sync(0xffffffffu, mine.j, e0 + e);
@@ -465,26 +493,45 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_tree_kernel(
                     }
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        if (e0 + e < n) uj[e] = *reinterpret_cast<const float4 *>(s_u + row_chunk(jj[e], lane));
+                        if (e0 + e < n) uj[e] = *reinterpret_cast<const float *>(s_u + row_col(jj[e], lane));
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        if (e0 + e < n) fma_row(u, o, xx[e], yy[e], uj[e]);
+                        if (e0 + e < n) {
+                            u -= xx[e] * uj[e];
+                            o += yy[e] * uj[e];
+                        }
                 }
             }
+        };
+        // Wait (bounded; the hardware suspends the warp) until the grandparent's u row is
+        // written: then every ancestor's above the parent is, and the acquire makes them
+        // visible, so their terms are added while the parent is still being solved.  Then
+        // wait for the parent and add its term: only that one is on the chain down the tree.
+        const int gp = p >= 0 ? s_parent[p] : -1;
+        if (gp >= 0) {
+            if (!__all_sync(0xffffffffu, mbar_wait(done_bar + 8u * (uint32_t)gp, 0, &s_abort, status))) break;
+            accumulate(1, di);
         }
-        *reinterpret_cast<float4 *>(s_u + row_chunk(i, lane)) = u;
-        __threadfence_block();  // every lane's u_i before the arrival
-        __syncwarp();
-        if (lane == 0) mbar_arrive(done_bar + 8u * (uint32_t)i);
-        o.x += yii * u.x; o.y += yii * u.y; o.z += yii * u.z; o.w += yii * u.w;
-        reinterpret_cast<float4 *>(O + (((size_t)b * B + i) * H + h) * kGdnD)[lane] = o;
+        if (p >= 0) {  // slot 0 is the parent: its record is read before the wait, its row after
+            const GdnRec rp = *rec_at(s_recs, g_recs, small, B, i, 0);
+            if (!__all_sync(0xffffffffu, mbar_wait(done_bar + 8u * (uint32_t)p, 0, &s_abort, status))) break;
+            const float up = *reinterpret_cast<const float *>(s_u + row_col(p, lane));
+            u -= bi * rp.r * rp.kk * up;
+            o += rp.r * rp.qk * up;
+        }
+        // every lane arrives (the barrier counts 32): each arrival releases that lane's
+        // part of u_i, so the phase completes once the whole row is written
+        *reinterpret_cast<float *>(s_u + row_col(i, lane)) = u;
+        mbar_arrive(done_bar + 8u * (uint32_t)i);
+        o += yii * u;
+        O[(((size_t)b * B + i) * H + h) * kGdnD + c0 + lane] = o;
     }
 }
 
 size_t gdn_workspace_bytes(int nb, int B, int H)
 {
-    size_t bytes = (size_t)nb * H * B * B * sizeof(GdnRec);
-    if (B > 128) bytes += (size_t)2 * nb * H * B * kGdnD * sizeof(float);
+    size_t bytes = (size_t)nb * H * kGdnSlices * B * B * sizeof(GdnRec);
+    if (B > 128) bytes += (size_t)2 * nb * H * kGdnSlices * B * kGdnCols * sizeof(float);
     return bytes;
 }
 
@@ -504,7 +551,7 @@ cudaError_t launch_gdn_tree(const uint16_t *q, const uint16_t *k, const uint16_t
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) opted_in[dev] = 1;
     }
-    return launch_dependent(gdn_tree_kernel, dim3((unsigned)H, (unsigned)nb), dim3(kGdnThreads),
+    return launch_dependent(gdn_tree_kernel, dim3((unsigned)H, (unsigned)nb, (unsigned)kGdnSlices), dim3(kGdnThreads),
                             gdn_smem_layout(B).total + 1024, stream, q, k, v, alpha, beta, S0, parent, B, H, O,
                             workspace, status);
 }
