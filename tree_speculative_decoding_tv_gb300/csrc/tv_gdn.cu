@@ -132,11 +132,6 @@ __device__ __forceinline__ uint32_t bf16_bits(float x)
     return r;
 }
 
-__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint32_t x)
-{
-    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"((uint16_t)x) : "memory");
-}
-
 // 16-byte global -> shared copy, zero-filled when !valid (nothing is read then)
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid)
 {
@@ -176,7 +171,7 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_tree_kernel(
     int *s_depth = reinterpret_cast<int *>(gb + L.depth);
     float *s_yii = reinterpret_cast<float *>(gb + L.yii);
     const uint32_t done_bar = base + L.done;  // node i's mbarrier at done_bar + 8 i: phase 0 completes when u_i is written
-    uint32_t *s_mask = reinterpret_cast<uint32_t *>(gb + L.mask);
+    uint32_t *s_mask = reinterpret_cast<uint32_t *>(gb + L.mask);  // word w of node i at [w * B + i]
 
     const int h = blockIdx.x, b = blockIdx.y, nb = gridDim.y;
     const int c0 = blockIdx.z * kGdnCols;  // this CTA's value columns c0 .. c0 + 31
@@ -227,14 +222,11 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_tree_kernel(
         }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
-    constexpr int kPer = kGdnD * kGdnCols / 4 / kGdnThreads;  // the S0 slice: 2 float4 per thread
-    static_assert(kPer * 4 * kGdnThreads == kGdnD * kGdnCols, "S0 slice split");
-    float4 sv[kPer];
+    // the S0 slice: warp w, lane l holds value column c0 + l for keys 8 w .. 8 w + 7
+    static_assert(kGdnWarps * 8 == kGdnD, "S0 slice split");
+    float sv[8];
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) {  // key row r, columns c0 + 4 (idx % 8) ..
-        const int idx = tid + u * kGdnThreads;
-        sv[u] = *reinterpret_cast<const float4 *>(S0 + (bh * kGdnD + (idx >> 3)) * kGdnD + c0 + (idx & 7) * 4);
-    }
+    for (int e = 0; e < 8; ++e) sv[e] = S0[(bh * kGdnD + 8 * warp + e) * kGdnD + c0 + lane];
 
     bool bad = false;
 #pragma unroll
@@ -266,14 +258,14 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_tree_kernel(
 
     // root paths: ancestor bits, records (j, r_ij) in slot order, depth and gamma
     for (int i = tid; i < B; i += kGdnThreads) {
-        uint32_t *m = s_mask + i * kGdnMaskWords;
+        uint32_t *m = s_mask + i;  // word w at m[w * B]: the threads of a warp touch consecutive words
 #pragma unroll
-        for (int w = 0; w < kGdnMaskWords; ++w) m[w] = 0;
-        m[i >> 5] = 1u << (i & 31);
+        for (int w = 0; w < kGdnMaskWords; ++w) m[w * B] = 0;  // all 8 words (zeros past B)
+        m[(i >> 5) * B] = 1u << (i & 31);
         float r = s_alpha[i];
         int slot = 0;
         for (int j = s_parent[i]; j >= 0; j = s_parent[j], ++slot) {
-            m[j >> 5] |= 1u << (j & 31);
+            m[(j >> 5) * B] |= 1u << (j & 31);
             GdnRec *rc = rec_at(s_recs, g_recs, small, B, i, slot);
             rc->j = j;
             rc->r = r;
@@ -284,20 +276,21 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_tree_kernel(
     }
     // the S0 slice [key r][value c0 + n] -> hi and lo bf16 parts, transposed: row n
     // holds keys 0..127 (K-major, 128-byte swizzled, like the K and Q tiles)
+    // (keys 8 w .. 8 w + 7 of row n are one 16-byte chunk: one store per part)
+    {
+        uint32_t hi[8], lo[8];
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-        const int idx = tid + u * kGdnThreads, r = idx >> 3, n0 = (idx & 7) * 4;
-        const float x[4] = {sv[u].x, sv[u].y, sv[u].z, sv[u].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const uint32_t hi = bf16_bits(x[e]);
-            const uint32_t lo = bf16_bits(x[e] - __uint_as_float(hi << 16));
-            const int n = n0 + e;  // row n: hi; row 32 + n: lo (same swizzle: 32 is a multiple of 8)
-            const uint32_t off = (uint32_t)(r >> 6) * kGdnSHalf + (uint32_t)n * 128 +
-                                 ((uint32_t)(((r & 63) >> 3) ^ (n & 7)) << 4) + (uint32_t)(r & 7) * 2;
-            st_shared_u16(base + L.s + off, hi);
-            st_shared_u16(base + L.s + off + kGdnCols * 128, lo);
+        for (int e = 0; e < 8; ++e) {
+            hi[e] = bf16_bits(sv[e]);
+            lo[e] = bf16_bits(sv[e] - __uint_as_float(hi[e] << 16));
         }
+        const int n = lane, r0 = 8 * warp;  // row n: hi; row 32 + n: lo (same swizzle: 32 is a multiple of 8)
+        const uint32_t off =
+            (uint32_t)(r0 >> 6) * kGdnSHalf + (uint32_t)n * 128 + ((uint32_t)(((r0 & 63) >> 3) ^ (n & 7)) << 4);
+        st_shared_v4(base + L.s + off, hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16), hi[4] | (hi[5] << 16),
+                     hi[6] | (hi[7] << 16));
+        st_shared_v4(base + L.s + off + kGdnCols * 128, lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16),
+                     lo[4] | (lo[5] << 16), lo[6] | (lo[7] << 16));
     }
     cp_async_wait_all();
     fence_proxy_async_smem();  // the tensor core reads what these threads wrote
@@ -365,11 +358,11 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_tree_kernel(
                 // node i's bits are its ancestors and itself (its highest bit), so ancestor j's
                 // slot (0 = the parent) is the number of bits above j, minus one
                 const int w = 4 * n + chunk;
-                const uint32_t bits = s_mask[i * kGdnMaskWords + w];
+                const uint32_t bits = s_mask[w * B + i];
                 int above = -1;
 #pragma unroll
                 for (int ww = 0; ww < kGdnMaskWords; ++ww)
-                    if (ww > w) above += __popc(s_mask[i * kGdnMaskWords + ww]);
+                    if (ww > w) above += __popc(s_mask[ww * B + i]);
 #pragma unroll
                 for (int t = 0; t < 32; ++t) {
                     if ((bits >> t) & 1u) {
