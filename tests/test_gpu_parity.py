@@ -63,7 +63,10 @@ def test_mask_reports_non_topological_parent():
 
 # ------------------------------------------------------------- a4 + a5 accept
 
-@pytest.mark.parametrize("B,V", [(1, 7), (7, 3), (16, 4096), (33, 1001), (64, 5), (256, 4099), (3, 300001)])
+# (100, 32768): rows of exactly 8 chunks (one per warp of a CTA); (200, 40961): 1200 ragged,
+# unaligned rows of 11 chunks; (3, 65537): 17 chunks, the last one a single element
+@pytest.mark.parametrize("B,V", [(1, 7), (7, 3), (16, 4096), (33, 1001), (64, 5), (256, 4099), (3, 300001),
+                                 (100, 32768), (200, 40961), (3, 65537)])
 def test_accept_bit_exact(B, V):
     rng = np.random.default_rng(B * 1000 + V)
     nb = 6
@@ -107,6 +110,32 @@ def test_argmax_edge_values(V):
     torch.cuda.synchronize()
     ref = oracle.argmax(rows)
     assert am.cpu().numpy().tolist() == ref.tolist() == [5, 0, 10, 0, V - 1, 0]
+
+
+def test_argmax_edge_values_across_spans():
+    """V = 151936 (38 chunks of 4096): ties, signed zeros, NaNs and infinities whose candidates
+    sit in chunks that different warps reduce, combined through the row's key."""
+    V = 151936
+    rows = np.full((6, V), 0xBF80, dtype=np.uint16)            # -1.0 everywhere
+    rows[0, [5, V - 3]] = 0x4000                                 # tie, first and last chunk -> 5
+    rows[1, :] = 0x8000
+    rows[1, 100000] = 0x0000                                     # -0 everywhere, +0 late -> index 0
+    rows[2, [140000, 150000]] = 0x7FC0                           # NaNs late -> the first NaN
+    rows[2, 3] = 0x7F80                                          # +inf early, in another chunk
+    rows[3, :] = 0xFF80                                          # all -inf -> 0
+    rows[4, [40000, 80000, V - 1]] = [0x3F80, 0x3F80, 0x4000]    # max in the tail -> V-1
+    rows[5, 4096 * 16 + 1] = 0x4100                              # a single maximum mid-row
+    nb, B = 1, 6
+    parent = np.array([[-1, 0, 1, 2, 3, 4]], np.int32)
+    logits = torch.from_numpy(rows.view(np.int16)).cuda()
+    d_parent = torch.from_numpy(parent).cuda()
+    import tree_speculative_decoding_tv_gb300 as tv
+    mask, _ = tv.build_mask(d_parent)
+    draft = torch.zeros((nb, B), dtype=torch.int32, device="cuda")
+    am, *_ = tv.accept(logits, draft, d_parent, mask)
+    torch.cuda.synchronize()
+    ref = oracle.argmax(rows)
+    assert am.cpu().numpy().tolist() == ref.tolist() == [5, 0, 140000, 0, V - 1, 4096 * 16 + 1]
 
 
 # ------------------------------------------------------------- a2 + a3 attention

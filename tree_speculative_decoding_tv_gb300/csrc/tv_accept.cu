@@ -425,9 +425,9 @@ __global__ void __launch_bounds__(kMaxB) accept_kernel(const unsigned long long 
     const int b = blockIdx.x;
     const int i = threadIdx.x;
 
-    // The tree inputs were written before the argmax kernel began (the key memset
-    // ahead of it completes only after all earlier work), so they are read while
-    // the argmax is still running; only the keys wait for it.
+    // The argmax CTAs let this kernel launch only after their own dependency wait, so
+    // everything before the argmax (the tree inputs) is complete and is read while the
+    // argmax still runs; only the keys wait for it.
     int p = -1, d = 0;
     bool bad = false;
     if (i < B) {
