@@ -661,6 +661,17 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
             const uint32_t *mrow = p.mask ? p.mask + ((size_t)sg.b * p.B + (valid ? i : 0)) * p.W : nullptr;
             uint32_t mreg[kMaxMaskWords];  // the row's ancestor bits when there is no mask array
             bool mreg_built = false;
+            // Without a mask array, a segment that reaches the tree keys walks the row's root
+            // path (dependent loads over the parent array) now, while the first S of the
+            // segment is still on its way, rather than at its first masked tile.
+            if (!mrow && valid && (long long)sg.j1 * kN > sg.P) {
+                if (!mask_ready) {  // the parents may come from the previous kernel
+                    pdl_wait_primary();
+                    mask_ready = true;
+                }
+                row_mask_from_parents(p.parent + (size_t)sg.b * p.B, i, mreg, p.status);
+                mreg_built = true;
+            }
             float m_run = -INFINITY, l_run = 0.f;  // m_run in log2 units of the scaled score
             for (int lx = 0; lx < nx; ++lx) {
                 const int t = pair ? lx : 2 * lx + x;
