@@ -383,8 +383,9 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
     // stream (normally tv_build_mask), which waits for everything before it and then
     // lets this grid start.  So q, K/V, the block table and prefix_lens (inputs written
     // before that kernel) are read at once (through L2: TMA, __ldcg); only the ancestor
-    // masks, which that kernel may still be writing, wait for it (griddepcontrol.wait
-    // before the first masked tile, and in every thread before it exits).
+    // masks (or the parent array), which that kernel may still be writing, wait for it
+    // (griddepcontrol.wait before the first masked tile, or without a mask array at the
+    // start of a segment that reaches the tree keys, and in every thread before it exits).
     if (warp == 2) {
         const long long total = sched_total(sch, lane);
         const long long C = active_ctas(total, gridDim.x);
