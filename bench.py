@@ -19,6 +19,7 @@ cross-GPU exchange); value = all ranks' nodes / the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import math
 import os
@@ -416,6 +417,10 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     # The timed steps last milliseconds, shorter than one nvidia-smi sample, so the clocks
     # are sampled over a load window of the same steps (--clock-window seconds) that ends
     # where they start.
+    # no collector pause on the host may fall between a step's start event and its launch
+    # (the device work is unchanged; a stall there would add idle time to the step)
+    gc.collect()
+    gc.disable()
     t_begin = time.time()
     while time.time() - t_begin < args.clock_window:
         for _ in range(20):
