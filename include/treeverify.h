@@ -282,9 +282,9 @@ TV_API int32_t tv_gdn_tree(const uint16_t *q_d, const uint16_t *k_d, const uint1
  *   n_acc_d, path_d int32 [nb] and [nb][B] as tv_accept returns them
  *   S_out_d         fp32 [nb][H][D][D] (out); may be S0_d (committed in place)
  *   Shapes: D = 128, 1 <= B <= 256.
- * One kernel launch (one CTA per (sequence, head)), a programmatic dependent of
- * the previous kernel on the stream; it waits for it before reading anything, so
- * it may directly follow tv_accept.  A path that is not a root path of at most B
+ * One kernel launch (8 CTAs per (sequence, head), one per 16 state columns), a
+ * programmatic dependent of the previous kernel on the stream; it waits for it
+ * before reading anything, so it may directly follow tv_accept.  A path that is not a root path of at most B
  * nodes (root first, strictly increasing, 0 <= n_acc < B) writes
  * TV_ERR_INVALID_ARG to dev_status_d and copies S0 to S_out unchanged.
  * Returns TV_OK (nb == 0 launches nothing), TV_ERR_INVALID_ARG, TV_ERR_UNSUPPORTED_SHAPE

@@ -58,13 +58,14 @@ cudaError_t launch_build_tree(const float *logp, const int32_t *tok, int nb, int
                               int32_t *parent, int32_t *token, float *score, int32_t *status, cudaStream_t stream);
 
 // Gated DeltaNet tree verification: dense K S0 / Q S0 products, then the sparse
-// masked solve and outputs (one CTA per (sequence, head)).
+// masked solve and outputs (4 CTAs per (sequence, head), one per 32 value columns).
 size_t gdn_workspace_bytes(int nb, int B, int H);
 cudaError_t launch_gdn_tree(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
                             const float *beta, const float *S0, const int32_t *parent, int nb, int B, int H, float *O,
                             void *workspace, int32_t *status, cudaStream_t stream);
 
-// Gated DeltaNet state commit along the accepted path (one CTA per (sequence, head)).
+// Gated DeltaNet state commit along the accepted path (8 CTAs per (sequence, head), one
+// per 16 state columns).
 cudaError_t launch_gdn_commit(const uint16_t *k, const uint16_t *v, const float *alpha, const float *beta,
                               const float *S0, const int32_t *n_acc, const int32_t *path, int nb, int B, int H,
                               float *S_out, int32_t *status, cudaStream_t stream);
