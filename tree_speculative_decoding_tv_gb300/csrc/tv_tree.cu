@@ -159,7 +159,70 @@ __global__ void __launch_bounds__(32) build_tree_kernel(const float *__restrict_
     __syncwarp();
     float last_f = 0.f;  // the last popped node's score and depth (the w = 1 round's only node)
     int last_d = 0;
-    while (made < B) {
+    // w = 1: every round is one pop, after which the popped node's first child joins.  Both
+    // frontier updates (the popped slot's replacement by its owner lane, the child's slot by
+    // its lane) go in one pass; a lane doing both rescans once, over the same slots the two
+    // steps would compare.  A top score that one lane alone holds needs no second reduction.
+    while (w == 1 && made < B) {
+        const uint32_t top_s = __reduce_max_sync(0xffffffffu, my_s);
+        if (top_s == 0) break;  // no candidate left: B exceeds the tree
+        const unsigned hold = __ballot_sync(0xffffffffu, my_s == top_s);
+        int owner;
+        uint32_t top_t;
+        if (__popc(hold) == 1) {
+            owner = __ffs(hold) - 1;
+            top_t = __shfl_sync(0xffffffffu, my_t, owner);
+        } else {
+            top_t = __reduce_min_sync(0xffffffffu, my_s == top_s ? my_t : kEmpty);
+            owner = __ffs(__ballot_sync(0xffffffffu, my_s == top_s && my_t == top_t)) - 1;
+        }
+        const float f = __shfl_sync(0xffffffffu, my_f, owner);
+        const int d = __shfl_sync(0xffffffffu, my_d, owner);
+        const int i = made;
+        if (lane == 0) {
+            par[i] = (int16_t)(top_t >> 16);
+            dep[i] = (int16_t)d;
+            rank[i] = (int16_t)(top_t & 0xFFFFu);
+            sc[i] = f;
+        }
+        const bool child = d < Dmax;  // node i's first child: slot n, parent score f, depth d + 1
+        const float cf = child ? f + lp[(size_t)d * K] : 0.f;
+        const uint32_t ct = (uint32_t)i << 16;
+        const bool ins = child && (n & 31) == lane, own = lane == owner;
+        if (own) {
+#pragma unroll
+            for (int q = 0; q < kTreeSlots; ++q)
+                if (rt[q] == top_t) {
+                    rf[q] = rep_f;
+                    rt[q] = rep_t;
+                }
+        }
+        if (ins) {
+            const int qn = n >> 5;
+#pragma unroll
+            for (int q = 0; q < kTreeSlots; ++q)
+                if (q == qn) {
+                    rf[q] = cf;
+                    rt[q] = ct;
+                    rp[q] = f;
+                    rd[q] = d + 1;
+                }
+        }
+        if (own) {
+            lane_best();
+        } else if (ins && order(cf, ct) > order(my_f, my_t)) {
+            my_s = score_key(cf);
+            my_t = ct;
+            my_f = cf;
+            my_p = f;
+            my_d = d + 1;
+            prepare();
+        }
+        if (child) ++n;
+        ++made;
+        __syncwarp();
+    }
+    while (w != 1 && made < B) {
         const int take = min(w, B - made);
         const int first = made;
         for (int t = 0; t < take; ++t) {
