@@ -325,7 +325,7 @@ TV_API int32_t tv_kv_commit(void *k_cache_d, void *v_cache_d, const int32_t *blo
                             int32_t max_pages, int32_t *new_prefix_lens_d, int32_t *dev_status_d, void *stream);
 
 /*
- * Argmax and acceptance in one kernel (the survey's fused acceptance)  [JF-4]
+ * Argmax and acceptance in one kernel  [JF-4]
  *
  * The same results as tv_accept (argmax of every row, then the greedy walk), from
  * one kernel launch instead of two: the argmax CTAs own whole rows, and the CTA
