@@ -85,7 +85,7 @@ TV_API const char *tv_status_str(int32_t status);
 TV_API int32_t tv_version(void);
 
 /*
- * a1 — ancestor masks  [JF-2], [TfM-P], [TfM-3]
+ * Ancestor masks  [JF-2], [TfM-P], [TfM-3]
  *
  *   mask[b][i][w] bit j (j = 32*w + bit, LSB first) is 1 iff node j is node i
  *   or one of its ancestors:  anc[0] = {0},  anc[i] = anc[parent[i]] U {i}.
@@ -103,7 +103,7 @@ TV_API int32_t tv_build_mask(const int32_t *parent_d, int32_t B, int32_t nb, uin
                       int32_t *depth_d, int32_t *dev_status_d, void *stream);
 
 /*
- * a2 + a3 — tree-causal paged attention with split-KV merge
+ * Tree-causal paged attention with split-KV merge
  * [JF-2], [JF-3], [TfM-P]
  *
  * For every sequence b, node i, query head h (kv head g = h / G):
@@ -163,7 +163,7 @@ TV_API size_t tv_attn_workspace_size(const tv_attn_args *args);
 TV_API int32_t tv_attn(const tv_attn_args *args, void *workspace_d, size_t workspace_bytes, void *stream);
 
 /*
- * a4 + a5 — vocab argmax and greedy acceptance  [JF-4] (rule: this library's reading)
+ * Vocab argmax and greedy acceptance  [JF-4] (rule: this library's reading)
  *
  *   argmax[b*B+i] = first index of the maximum of logits[b*B+i][0..V)
  *                   (values compared as numbers, -0 == +0; a NaN counts as the maximum)

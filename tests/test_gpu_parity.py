@@ -38,7 +38,7 @@ def _workload(seed, nb, B, Hq, Hkv, prefix, V=1000, kind="mixed", shuffle=True):
                             shuffle_pages=shuffle, extra_pages=2)
 
 
-# -------------------------------------------------------------------- a1 mask
+# -------------------------------------------------------------------- ancestor masks
 
 @pytest.mark.parametrize("B", [1, 2, 15, 16, 17, 31, 32, 33, 64, 100, 255, 256])
 def test_mask_bit_exact(B):
@@ -61,7 +61,7 @@ def test_mask_reports_non_topological_parent():
     assert status.item() == 2  # TV_ERR_NOT_TOPOLOGICAL
 
 
-# ------------------------------------------------------------- a4 + a5 accept
+# ------------------------------------------------------- argmax and acceptance
 
 # (100, 32768): rows of exactly 8 chunks (one per warp of a CTA); (200, 40961): 1200 ragged,
 # unaligned rows of 11 chunks; (3, 65537): 17 chunks, the last one a single element
@@ -138,7 +138,7 @@ def test_argmax_edge_values_across_spans():
     assert am.cpu().numpy().tolist() == ref.tolist() == [5, 0, 140000, 0, V - 1, 4096 * 16 + 1]
 
 
-# ------------------------------------------------------------- a2 + a3 attention
+# --------------------------------------------------- attention and split-KV merge
 
 ATTN_CASES = [
     # (nb, B, Hq, Hkv, prefixes)

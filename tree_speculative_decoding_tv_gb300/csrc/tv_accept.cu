@@ -1,4 +1,4 @@
-// a4 — vocab argmax and a5 — greedy acceptance walk.
+// Vocab argmax and greedy acceptance walk.
 //
 // The pages speak of accepted tokens and longer accepted prefixes (JETFLOW
 // summary, §3 item 2 and §4) without stating a rule; the rule implemented is

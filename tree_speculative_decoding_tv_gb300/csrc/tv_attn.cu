@@ -1,4 +1,4 @@
-// a2 + a3 — tree-causal paged attention over a draft tree, with split-KV
+// Tree-causal paged attention over a draft tree, with split-KV
 // partials merged by a log-sum-exp combine.
 //
 // What it computes (JETFLOW summary, §2 "Arquitectura Central" tree-causal

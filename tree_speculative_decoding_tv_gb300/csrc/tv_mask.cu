@@ -1,4 +1,4 @@
-// a1 — packed ancestor masks and depths of a topologically ordered draft tree.
+// Packed ancestor masks and depths of a topologically ordered draft tree.
 //
 // Definition (JETFLOW summary, §2 "Arquitectura Central", tree-causal mask;
 // DFlash-TfM summary, §3 "Solución", topological order): node i may attend to
