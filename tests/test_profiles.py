@@ -54,3 +54,21 @@ def test_launch_list_summary_names_its_command():
     text = open(os.path.join(ROOT, "profiles", "launches_bench_config2.md")).read()
     assert "--metrics gpu__time_duration.sum --clock-control none" in text
     assert "share of ours" in text
+
+
+def test_bench_reads_traffic_only_from_a_matching_summary(tmp_path, monkeypatch):
+    import bench
+    # the committed summary of the attention kernel matches its source: its traffic is read
+    assert bench.profiled_traffic("tree_attn_kernel", "tv_attn.cu", 2) > 0
+    # the same summary against another source file does not match: no traffic
+    assert bench.profiled_traffic("tree_attn_kernel", "tv_mask.cu", 2) is None
+    # no summary for a workload: no traffic
+    assert bench.profiled_traffic("tree_attn_kernel", "tv_attn.cu", 9) is None
+
+
+def test_peaks_fall_back_when_the_measured_file_is_missing(monkeypatch, tmp_path):
+    import bench
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    peaks, source = bench.load_peaks()
+    assert source.startswith("fallback")
+    assert peaks == bench.FALLBACK_PEAKS
