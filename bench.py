@@ -1,15 +1,16 @@
 """Benchmark of one tree-verification step on GB300.
 
-A step is the whole hot path over one batch: ancestor masks (tv_build_mask),
-tree-causal paged attention with split-KV merge (tv_attn), vocab argmax and
-greedy acceptance (tv_accept), for one layer's attention.  The metric is
-verified tree nodes per second per layer (nb * B / step time).
+A step is the whole hot path over one batch: tree-causal paged attention with
+the ancestor bits derived from the parent array and split-KV merge (tv_attn),
+vocab argmax and greedy acceptance (tv_accept), for one layer's attention.
+The metric is verified tree nodes per second per layer (nb * B / step time).
 
-Default workload: 1 sequence, Qwen3-8B attention shape (32 q / 8 kv heads,
-head dim 128, bf16), 4096-token prefix in shuffled 16-token pages, a 256-node
-best-first draft tree, 151936-entry bf16 logits.  Inputs are seeded synthetic
-tensors of those shapes, resident in HBM; L2 is flushed (a 512 MB write)
-before every timed step.
+Default workload (the largest single-GPU one): 4 sequences, Qwen3-8B attention
+shape (32 q / 8 kv heads, head dim 128, bf16), 32768-token prefixes in shuffled
+16-token pages, 256-node best-first draft trees, 151936-entry bf16 logits.
+Inputs are seeded synthetic tensors of those shapes, resident in HBM; L2 is
+flushed (a 512 MB write) before every timed step.  The same process then
+measures the four smaller workloads (``per_config``) with the same flush.
 
   python bench.py [--gpus N --steps K --warmup W] [--config 1..5] [--impl reference]
 
@@ -37,6 +38,9 @@ import workloads as wl  # noqa: E402
 METRIC = "tree-verify attn verified nodes/s per layer; % of roofline (HBM or TC)"
 UNIT = "nodes/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# GB300 data-sheet figures: HBM3e bandwidth and dense bf16 tensor throughput
+NOMINAL_PEAKS = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0}
+DEFAULT_CONFIG = 5
 
 
 # ----------------------------------------------------------------------------- bookkeeping
@@ -396,6 +400,62 @@ def job_value(nodes_per_rank: int, world: int, total_ms: float, steps: int) -> f
     return nodes_per_rank * world / (total_ms / steps * 1e-3)
 
 
+def stage_rooflines(w: wl.Workload, t_attn: float, t_acc: float, peaks: dict, peak_src: str, config):
+    """Rooflines of the attention stage (tensor- or HBM-bound, whichever floor is higher) and of
+    the acceptance stage (HBM), for stage times in seconds.  frac is against the measured peak
+    (peaks), frac_nominal against the GB300 data-sheet figure (NOMINAL_PEAKS)."""
+    ab, af, lb = attn_bytes(w), attn_flops(w), accept_bytes(w)
+    kname = "attention stage: tree_attn_kernel (ancestor bits from the parent array) + tree_attn_merge_kernel"
+    if af / (peaks["bf16_tflops"] * 1e12) >= ab / (peaks["hbm_gbs"] * 1e9):
+        attn = {"kernel": kname, "bound": "tensor", "achieved": af / t_attn / 1e12, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "peak_nominal": NOMINAL_PEAKS["bf16_tflops"]}
+    else:
+        attn = {"kernel": kname, "bound": "hbm", "achieved": ab / t_attn / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "peak_nominal": NOMINAL_PEAKS["hbm_gbs"]}
+    acc = {"kernel": "argmax_rows_kernel + accept_kernel (tv_accept)", "bound": "hbm",
+           "achieved": lb / t_acc / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+           "peak_nominal": NOMINAL_PEAKS["hbm_gbs"]}
+    for r, src, name in ((attn, "tv_attn.cu", "tree_attn_kernel"), (acc, "tv_accept.cu", "argmax_rows_kernel")):
+        r["frac"] = r["achieved"] / r["peak"]
+        r["frac_nominal"] = r["achieved"] / r["peak_nominal"]
+        r["peak_source"] = peak_src + " burst; frac_nominal is of the GB300 data-sheet figure"
+        r["traffic"] = profiled_traffic(name, src, config)
+        r["algorithmic_bytes"] = ab if src == "tv_attn.cu" else lb
+        if src == "tv_attn.cu":
+            r["algorithmic_flops"] = af
+    return attn, acc
+
+
+def measure_config(n: int, dev: str, flush, steps: int, warmup: int, seed: int) -> dict:
+    """Step, attention-stage and acceptance-stage times of workload n, each from its own
+    graph replayed `steps` times with the L2 flush before every replay (the headline's timing
+    rules), and the stages' roofline fractions."""
+    import torch
+    w = wl.config(n, seed=seed)
+    st = Step(w, dev)
+    st.capture()
+    for _ in range(warmup):
+        st.run()
+    torch.cuda.synchronize()
+    step_ms = st.time_stage(st.g_step, flush, steps)
+    attn_ms = st.time_stage(st.g_attn, flush, steps)
+    acc_ms = st.time_stage(st.g_acc, flush, steps)
+    if st.status.item() != 0:
+        raise RuntimeError(f"device status {st.status.item()} on workload {n}")
+    peaks, peak_src = load_peaks()
+    attn, acc = stage_rooflines(w, attn_ms * 1e-3, acc_ms * 1e-3, peaks, peak_src, n)
+    nodes = w.nb * w.B
+    out = {"workload": wl.CONFIG_NAMES[n], "nodes_per_s": nodes / (step_ms * 1e-3), "step_us": step_ms * 1e3,
+           "attention_stage_us": attn_ms * 1e3, "attention_bound": attn["bound"],
+           "attention_frac": attn["frac"], "attention_frac_nominal": attn["frac_nominal"],
+           "attention_traffic": attn["traffic"], "accept_us": acc_ms * 1e3, "accept_frac": acc["frac"],
+           "accept_frac_nominal": acc["frac_nominal"], "attention_bytes": attn_bytes(w),
+           "attention_flops": attn_flops(w), "accept_bytes": accept_bytes(w)}
+    del st
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_gpu(args, rank: int, world: int, local_rank: int):
     import torch
     import torch.distributed as dist
@@ -525,6 +585,13 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         raise RuntimeError(f"device status {st.status.item()} in the commit stage")
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
 
+    per_config = {}
+    if not args.no_per_config:
+        del sets
+        for n in sorted(wl.CONFIG_NAMES):
+            if n != args.config:
+                per_config[str(n)] = measure_config(n, dev, flush, args.steps, args.warmup, 1234 + rank)
+
     if rank != 0:
         return
     nodes = w.nb * w.B
@@ -533,22 +600,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     t_attn = attn_stage_ms * 1e-3
     t_acc = acc_stage_ms * 1e-3
     ab, af, lb = attn_bytes(w), attn_flops(w), accept_bytes(w)
-    attn_tc = af / (peaks["bf16_tflops"] * 1e12)
-    attn_hbm = ab / (peaks["hbm_gbs"] * 1e9)
-    if attn_tc >= attn_hbm:
-        attn_roof = {"kernel": "attention stage: tree_attn_kernel (ancestor bits from the parent array) + tree_attn_merge_kernel", "bound": "tensor",
-                     "achieved": af / t_attn / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
-    else:
-        attn_roof = {"kernel": "attention stage: tree_attn_kernel (ancestor bits from the parent array) + tree_attn_merge_kernel", "bound": "hbm",
-                     "achieved": ab / t_attn / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    acc_roof = {"kernel": "argmax_rows_kernel + accept_kernel (tv_accept)", "bound": "hbm",
-                "achieved": lb / t_acc / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    for r, src, name in ((attn_roof, "tv_attn.cu", "tree_attn_kernel"),
-                         (acc_roof, "tv_accept.cu", "argmax_rows_kernel")):
-        r["frac"] = r["achieved"] / r["peak"]
-        r["peak_source"] = peak_src + " burst"
-        r["traffic"] = profiled_traffic(name, src, args.config)
-        r["algorithmic_bytes"] = ab if src == "tv_attn.cu" else lb
+    attn_roof, acc_roof = stage_rooflines(w, t_attn, t_acc, peaks, peak_src, args.config)
     roof = attn_roof if t_attn >= t_acc else acc_roof
     out = {
         "metric": METRIC, "value": job_value(nodes, world, total_ms, args.steps), "unit": UNIT,
@@ -573,6 +625,11 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
                            "step's mask, accept_fused_nomask_ms the same building the mask from the parent array",
             "stage_timing": "each stage's own graph replayed K times with the same L2 flush, after the timed steps",
             "attention_nodes_per_s": nodes / t_attn, "attention_roofline": attn_roof, "accept_roofline": acc_roof,
+            "per_config": per_config,
+            "per_config_note": "the other four workloads in the same process after the headline: each one's step, "
+                               "attention stage and acceptance stage from their own graphs, K replays each with "
+                               "the same 512 MB L2 flush before every replay; fractions of the measured peaks "
+                               "(frac) and of the GB300 data-sheet peaks (frac_nominal)",
             "attention_bytes": ab, "attention_flops": af, "accept_bytes": lb,
             "kv_commit_ms": commit_ms, "kv_commit_bytes": commit_bytes,
             "build_tree_ms": tree_ms,
@@ -612,50 +669,50 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
 
 # ----------------------------------------------------------------------------- CPU oracle legs
 
-def oracle_step(w: wl.Workload, heads: int):
-    """One oracle verify step on a head sample; returns (wall seconds for the full step, threads, note)."""
+def oracle_step(w: wl.Workload, group: int = 0):
+    """One oracle verify step with the attention on one kv-head group (its G query heads over
+    every sequence and node), scaled to all Hkv groups; the mask and the argmax + acceptance run
+    in full.  Returns (wall seconds for the full step, threads, q heads computed)."""
     import oracle
     G = w.G
-    groups = max(1, heads // G)
+    g = group % w.Hkv
     t0 = time.perf_counter()
     oracle.build_mask(w.parent)
     t1 = time.perf_counter()
-    q = np.ascontiguousarray(w.q[:, :groups * G])
-    kc = np.ascontiguousarray(w.k_cache[:, :groups])
-    vc = np.ascontiguousarray(w.v_cache[:, :groups])
+    q = np.ascontiguousarray(w.q[:, g * G:(g + 1) * G])
+    kc = np.ascontiguousarray(w.k_cache[:, g:g + 1])
+    vc = np.ascontiguousarray(w.v_cache[:, g:g + 1])
     t2 = time.perf_counter()
-    _, _, threads = oracle.attn(q, kc, vc, w.block_table, w.prefix_lens, w.parent, groups * G, groups,
-                                return_threads=True)
+    _, _, threads = oracle.attn(q, kc, vc, w.block_table, w.prefix_lens, w.parent, G, 1, return_threads=True)
     t3 = time.perf_counter()
     oracle.accept(w.logits, w.draft, w.parent)
     t4 = time.perf_counter()
-    full = (t1 - t0) + (t3 - t2) * (w.Hq / (groups * G)) + (t4 - t3)
-    return full, threads, groups * G
+    full = (t1 - t0) + (t3 - t2) * w.Hkv + (t4 - t3)
+    return full, threads, G
 
 
-def cpu_baseline(w: wl.Workload, heads: int | None = None):
-    heads = heads or w.Hq
-    full, threads, used = oracle_step(w, heads)
+def cpu_baseline(w: wl.Workload):
+    full, threads, used = oracle_step(w)
     return {"value": w.nb * w.B / full, "unit": UNIT, "cores": threads, "kind": "oracle",
             "host_cores": os.cpu_count(),
-            "sample": f"one full step of the same workload (mask, attention on {used} of {w.Hq} query heads "
-                      f"scaled by {w.Hq / used:g}, argmax + acceptance over all {w.nb * w.B} logits rows); "
-                      f"fp64 C oracle, wall clock"}
+            "sample": f"one step of the same workload: mask, attention on kv head 0's {used} query heads over all "
+                      f"{w.nb} sequences and {w.B} nodes scaled by {w.Hkv}, argmax + acceptance over all "
+                      f"{w.nb * w.B} logits rows; fp64 C oracle, wall clock"}
 
 
 def run_reference(args, rank: int, world: int):
     if rank != 0:
         return
     w = wl.config(args.config, seed=1234)
-    # a head sample that keeps every host core busy (whole kv-head groups) and each step to seconds
-    heads = args.ref_heads or min(w.Hq, max(w.G, ((os.cpu_count() or 1) // w.G) * w.G))
-    for _ in range(args.warmup):
-        oracle_step(w, heads)
+    # each step samples one kv-head group (step k takes group k mod Hkv, so Hkv steps cover every
+    # head once), which keeps a step to seconds on the host cores
+    for k in range(args.warmup):
+        oracle_step(w, k)
     times = []
     threads = 0
-    used = heads
-    for _ in range(args.steps):
-        t, threads, used = oracle_step(w, heads)
+    used = w.G
+    for k in range(args.steps):
+        t, threads, used = oracle_step(w, k)
         times.append(t)
     ms = float(np.mean(times)) * 1e3
     v = w.nb * w.B / (ms * 1e-3)
@@ -665,8 +722,9 @@ def run_reference(args, rank: int, world: int):
            "config": {"workload": wl.CONFIG_NAMES[args.config], "nb": w.nb, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
                       "D": w.D, "V": w.V},
            "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
-                            "sample": f"each step: mask, attention on {used} of {w.Hq} query heads scaled by "
-                                      f"{w.Hq / used:g}, argmax + acceptance over all rows; fp64 C oracle"},
+                            "sample": f"each step: mask, attention on one kv-head group ({used} of {w.Hq} query "
+                                      f"heads, step k takes group k mod {w.Hkv}) scaled by {w.Hkv}, argmax + "
+                                      f"acceptance over all rows; fp64 C oracle"},
            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
 
@@ -676,10 +734,10 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--ref-heads", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="measure the headline workload only")
     ap.add_argument("--clock-window", type=float, default=0.4,
                     help="seconds of untimed steps, sampled for clocks, before the timed steps (0 under a profiler)")
     args = ap.parse_args()

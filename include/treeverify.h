@@ -118,6 +118,13 @@ TV_API int32_t tv_build_mask(const int32_t *parent_d, int32_t B, int32_t nb, uin
  * depth).  Cache slots past P_b + B inside the last page must hold finite
  * values (zero-initialised caches satisfy this): they are multiplied by zero
  * probabilities.
+ *
+ * Value range: a row tile whose key range is split between CTAs parks its
+ * normalised partial output in fp16 before the merge, so every V entry must
+ * satisfy |v| <= 65504 (fp16's largest finite value; the partial output of a
+ * row is a convex combination of V rows).  Larger values make only the split
+ * rows overflow.  Activations of the models these shapes come from stay far
+ * below that.
  */
 typedef struct tv_attn_args {
     const void *q_d;             /* bf16 [nb*B][Hq][D], 16-byte aligned */
@@ -189,8 +196,10 @@ TV_API int32_t tv_attn(const tv_attn_args *args, void *workspace_d, size_t works
  *                  bytes (one 8-byte argmax key per logits row), 8-byte aligned,
  *                  contents ignored on entry (the call writes every key before
  *                  reading it; concurrent calls need separate workspaces)
- * Returns TV_OK, TV_ERR_INVALID_ARG, TV_ERR_UNSUPPORTED_SHAPE or TV_ERR_CUDA.
- * A parent array that is not topological is reported through dev_status_d.
+ * Returns TV_OK, TV_ERR_INVALID_ARG, TV_ERR_UNSUPPORTED_SHAPE (B outside
+ * [1, 256], V > INT32_MAX - 8192, or nb * B * ceil(V / 4096) >= 2^31) or
+ * TV_ERR_CUDA.  A parent array that is not topological is reported through
+ * dev_status_d.
  */
 TV_API size_t tv_accept_workspace_size(int32_t V, int32_t B, int32_t nb);
 
@@ -365,12 +374,16 @@ TV_API int32_t tv_accept_fused(const uint16_t *logits_d, int32_t V, const int32_
  * image.
  *
  *   - Limit: nb * B <= TV_ACCEPT_NOALLOC_MAX_ROWS; larger calls return
- *     TV_ERR_UNSUPPORTED_SHAPE and enqueue nothing.
+ *     TV_ERR_UNSUPPORTED_SHAPE and enqueue nothing, as do V > INT32_MAX - 8192
+ *     and the other shape limits of tv_accept.
  *   - The array exists once per GPU that loads the library and stays allocated
  *     until the process exits.
  *   - The first call on a device looks up the array's device address (with that
- *     device current) and caches it; make that first call before any stream
- *     capture.
+ *     device current) and caches it together with the id of the device's
+ *     context; make that first call before any stream capture.  After
+ *     cudaDeviceReset the next call sees a new context and looks the address
+ *     up again (the module, and so the array, may move), so make that call
+ *     outside a capture too.
  *   - Every call on a device shares the array and leaves its last contents
  *     there; each call writes every part it reads before reading it.  Calls whose work
  *     overlaps on the GPU (different streams, no ordering between them) race on
@@ -382,6 +395,24 @@ TV_API int32_t tv_accept_noalloc(const uint16_t *logits_d, int32_t V, const int3
                                  const int32_t *parent_d, const uint32_t *mask_d, int32_t B, int32_t nb,
                                  int32_t *argmax_d, int32_t *n_acc_d, int32_t *path_d, int32_t *bonus_d,
                                  int32_t *dev_status_d, void *stream);
+
+/*
+ * tv_selftest_wait — exercises the failure path of the bounded device waits.
+ * (The pages have no counterpart: this checks the library's own fault handling.)
+ *
+ * The pipelined kernels (tv_attn, tv_gdn_tree) wait on shared-memory barriers
+ * with a time limit; a wait that runs out writes TV_ERR_TIMEOUT to
+ * *dev_status_d, stops the kernel cleanly (copies in flight land, tensor memory
+ * is freed) and leaves the context usable.  This call launches one small kernel
+ * that allocates tensor memory, waits on a barrier that nothing arrives at for
+ * limit_us microseconds, reports TV_ERR_TIMEOUT, frees the tensor memory and
+ * returns, so a test can see that path work without breaking a real kernel.
+ *
+ *   limit_us      1 .. 1000000
+ *   dev_status_d  device int32, required (the caller zeroes it first)
+ * Returns TV_OK (kernel enqueued), TV_ERR_INVALID_ARG or TV_ERR_CUDA.
+ */
+TV_API int32_t tv_selftest_wait(uint32_t limit_us, int32_t *dev_status_d, void *stream);
 
 #ifdef __cplusplus
 }

@@ -110,6 +110,26 @@ def test_accept_argument_checks(L):
     assert L.tv_accept_workspace_size(0, 16, 1) == 0 and L.tv_accept_workspace_size(10, 300, 1) == 0
 
 
+def test_accept_entry_points_reject_a_vocabulary_near_int_max(L):
+    # the kernels index a row with 32-bit ints: V must stay 8192 below INT32_MAX
+    P = C.c_void_p
+    f = P(FAKE)
+    for V in (2**31 - 1, 2**31 - 8192):
+        assert L.tv_accept(f, V, f, f, f, 16, 1, f, f, f, f, None, f, 1 << 40, None) == 3
+        assert L.tv_accept_fused(f, V, f, f, f, 16, 1, f, f, f, f, None, f, 1 << 40, None) == 3
+        assert L.tv_accept_noalloc(f, V, f, f, f, 16, 1, f, f, f, f, None, None) == 3
+    # the unit count (rows x 4096-logit units) must stay below 2^31 as well
+    assert L.tv_accept_noalloc(f, 2**31 - 8193, f, f, f, 256, 32, f, f, f, f, None, None) == 3
+
+
+def test_selftest_wait_argument_checks(L):
+    P = C.c_void_p
+    assert L.tv_selftest_wait(0, P(FAKE), None) == 1
+    assert L.tv_selftest_wait(1000001, P(FAKE), None) == 1
+    assert L.tv_selftest_wait(1000, None, None) == 1
+    assert L.tv_selftest_wait(1000, P(FAKE + 2), None) == 1
+
+
 def test_accept_fused_argument_checks(L):
     P = C.c_void_p
     ok = [P(FAKE)] * 4

@@ -37,11 +37,22 @@ def test_noalloc_matches_workspace_entry_point_twice():
 
 @pytest.mark.gpu
 def test_noalloc_rejects_too_many_rows():
-    nb, B = 2, 256
-    assert nb * B <= tv.binding.NOALLOC_MAX_ROWS
+    # real device buffers sized for the oversized call, so that a regression of the row
+    # limit would give a wrong return code, not kernels writing through made-up addresses
+    B, V = 256, 100
     big = tv.binding.NOALLOC_MAX_ROWS // B + 1
+    dev = "cuda"
+    logits = torch.zeros((big * B, V), dtype=torch.int16, device=dev)
+    draft = torch.zeros((big, B), dtype=torch.int32, device=dev)
+    parent = torch.arange(-1, B - 1, dtype=torch.int32, device=dev).repeat(big, 1)
+    am = torch.zeros(big * B, dtype=torch.int32, device=dev)
+    n_acc = torch.zeros(big, dtype=torch.int32, device=dev)
+    path = torch.zeros((big, B), dtype=torch.int32, device=dev)
+    bonus = torch.zeros(big, dtype=torch.int32, device=dev)
     P = C.c_void_p
-    fake = [P(0x10000)] * 9
-    rc = tv.lib().tv_accept_noalloc(fake[0], 100, fake[1], fake[2], fake[3], B, big, fake[4], fake[5], fake[6],
-                                    fake[7], None, None)
+    rc = tv.lib().tv_accept_noalloc(P(logits.data_ptr()), V, P(draft.data_ptr()), P(parent.data_ptr()), None, B,
+                                    big, P(am.data_ptr()), P(n_acc.data_ptr()), P(path.data_ptr()),
+                                    P(bonus.data_ptr()), None, None)
+    torch.cuda.synchronize()
     assert rc == 3  # TV_ERR_UNSUPPORTED_SHAPE
+    assert int(n_acc.abs().sum()) == 0  # nothing was enqueued

@@ -25,7 +25,8 @@ TV_ERR_UNIMPLEMENTED = 6
 
 EXPORTED = ("tv_status_str", "tv_version", "tv_build_mask", "tv_attn_workspace_size", "tv_attn",
             "tv_accept_workspace_size", "tv_accept", "tv_accept_fused_workspace_size", "tv_accept_fused",
-            "tv_accept_noalloc", "tv_kv_commit", "tv_build_tree", "tv_gdn_tree_workspace_size", "tv_gdn_tree", "tv_gdn_commit")
+            "tv_accept_noalloc", "tv_kv_commit", "tv_build_tree", "tv_gdn_tree_workspace_size", "tv_gdn_tree", "tv_gdn_commit",
+            "tv_selftest_wait")
 NOALLOC_MAX_ROWS = 8192  # TV_ACCEPT_NOALLOC_MAX_ROWS
 
 
@@ -88,6 +89,8 @@ def lib() -> C.CDLL:
         L.tv_gdn_tree.restype = I
         L.tv_gdn_commit.argtypes = [P, P, P, P, P, P, P, I, I, I, I, P, P, P]
         L.tv_gdn_commit.restype = I
+        L.tv_selftest_wait.argtypes = [C.c_uint32, P, P]
+        L.tv_selftest_wait.restype = I
         _lib = L
     return _lib
 
@@ -303,3 +306,8 @@ def gdn_commit(k, v, alpha, beta, S0, n_acc, path, out=None, status=None, stream
                              _p(status), _stream(stream))
     _check(rc, "tv_gdn_commit")
     return out
+
+
+def selftest_wait(limit_us: int, status: torch.Tensor, stream=None):
+    """tv_selftest_wait: a kernel whose bounded wait runs out; status gets TV_ERR_TIMEOUT."""
+    _check(lib().tv_selftest_wait(int(limit_us), _p(status), _stream(stream)), "tv_selftest_wait")

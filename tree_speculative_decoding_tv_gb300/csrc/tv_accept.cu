@@ -36,6 +36,7 @@
 // CTA's keys before its addition, and the walking CTA's fence after it before
 // it reads them).  Nothing waits on another CTA.  Without a mask the walking CTA
 // builds node i's ancestor bits in shared memory by walking i's root path.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -538,23 +539,56 @@ cudaError_t launch_accept_fused(const uint16_t *logits, int V, const int32_t *dr
 // tv_accept_noalloc on that GPU shares it.
 static __device__ __align__(256) unsigned long long g_noalloc_keys[TV_ACCEPT_NOALLOC_MAX_ROWS];
 
-// The device address of g_noalloc_keys on the current device.  Host code only sees a
+// The device address of g_noalloc_keys in the current context.  Host code only sees a
 // host-side stand-in under that name, so the address is looked up with
-// cudaGetSymbolAddress once per device (with that device current) and cached.
+// cudaGetSymbolAddress (with the device current) the first time a context calls, and
+// cached per device together with the context's unique id: a context created after
+// cudaDeviceReset loads the module again, possibly elsewhere, and gets a fresh lookup.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+static unsigned long long current_context_id()
+{
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *a = nullptr, *b = nullptr;
+        cudaDriverEntryPointQueryResult qa, qb;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) == cudaSuccess &&
+            qa == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) == cudaSuccess &&
+            qb == cudaDriverEntryPointSuccess) {
+            get_current = reinterpret_cast<CtxGetCurrentFn>(a);
+            get_id = reinterpret_cast<CtxGetIdFn>(b);
+        }
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx && get_id(ctx, &id) == CUDA_SUCCESS)
+        return id;
+    return 0;  // unknown: the lookup is then repeated on every call
+}
+
 static cudaError_t noalloc_keys_address(void **out)
 {
     static std::mutex mu;
     static void *addr[64] = {nullptr};
+    static unsigned long long ctx_id[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    // 0 before the device's context exists (the lookup below creates it) or when the
+    // driver cannot say: the address is then looked up again
+    const unsigned long long id = current_context_id();
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
+    if (!addr[dev] || id == 0 || ctx_id[dev] != id) {
         void *ptr = nullptr;
         e = cudaGetSymbolAddress(&ptr, g_noalloc_keys);
         if (e != cudaSuccess) return e;
         addr[dev] = ptr;
+        ctx_id[dev] = id;
     }
     *out = addr[dev];
     return cudaSuccess;

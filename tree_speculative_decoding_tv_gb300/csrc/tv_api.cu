@@ -54,6 +54,14 @@ int32_t check_attn(const tv_attn_args *a)
     return TV_OK;
 }
 
+// The acceptance kernels index a row with 32-bit ints and cut it into 4096-logit
+// units: V and the unit count must stay clear of 2^31.
+bool accept_shape_ok(int32_t V, int32_t B, int32_t nb)
+{
+    if ((long long)V > (long long)INT32_MAX - 8192) return false;
+    return (long long)nb * B * (((long long)V + 4095) / 4096) < (1ll << 31);
+}
+
 int attn_ctas(const tv_attn_args *a)
 {
     if (a->num_ctas > 0) return a->num_ctas;
@@ -134,7 +142,7 @@ int32_t tv_accept(const uint16_t *logits_d, int32_t V, const int32_t *draft_toke
         !aligned(argmax_d, 4) || !aligned(n_acc_d, 4) || !aligned(path_d, 4) || !aligned(bonus_d, 4) ||
         !aligned(dev_status_d, 4))
         return TV_ERR_INVALID_ARG;
-    if ((long long)nb * B * (((long long)V + 4095) / 4096) >= (1ll << 31)) return TV_ERR_UNSUPPORTED_SHAPE;
+    if (!accept_shape_ok(V, B, nb)) return TV_ERR_UNSUPPORTED_SHAPE;
     if (nb == 0) return TV_OK;
     if (!workspace_d || !aligned(workspace_d, 8) || workspace_bytes < tv::accept_workspace_bytes(V, B, nb))
         return TV_ERR_INVALID_ARG;
@@ -165,7 +173,7 @@ int32_t tv_accept_fused(const uint16_t *logits_d, int32_t V, const int32_t *draf
         !aligned(argmax_d, 4) || !aligned(n_acc_d, 4) || !aligned(path_d, 4) || !aligned(bonus_d, 4) ||
         !aligned(dev_status_d, 4))
         return TV_ERR_INVALID_ARG;
-    if ((long long)nb * B * (((long long)V + 4095) / 4096) >= (1ll << 31)) return TV_ERR_UNSUPPORTED_SHAPE;
+    if (!accept_shape_ok(V, B, nb)) return TV_ERR_UNSUPPORTED_SHAPE;
     if (nb == 0) return TV_OK;
     if (!workspace_d || !aligned(workspace_d, 8) || workspace_bytes < tv::accept_fused_workspace_bytes(V, B, nb))
         return TV_ERR_INVALID_ARG;
@@ -184,6 +192,7 @@ int32_t tv_accept_noalloc(const uint16_t *logits_d, int32_t V, const int32_t *dr
     if (nb < 0 || V < 1) return TV_ERR_INVALID_ARG;
     if (B < 1 || B > kMaxB) return TV_ERR_UNSUPPORTED_SHAPE;
     if ((long long)nb * B > TV_ACCEPT_NOALLOC_MAX_ROWS) return TV_ERR_UNSUPPORTED_SHAPE;
+    if (!accept_shape_ok(V, B, nb)) return TV_ERR_UNSUPPORTED_SHAPE;
     if (!logits_d || !draft_tokens_d || !parent_d || !argmax_d || !n_acc_d || !path_d || !bonus_d)
         return TV_ERR_INVALID_ARG;
     if (!aligned(logits_d, 2) || !aligned(draft_tokens_d, 4) || !aligned(parent_d, 4) || !aligned(mask_d, 4) ||
@@ -287,6 +296,14 @@ int32_t tv_kv_commit(void *k_cache_d, void *v_cache_d, const int32_t *block_tabl
     cudaError_t e = tv::launch_kv_commit(static_cast<uint16_t *>(k_cache_d), static_cast<uint16_t *>(v_cache_d),
                                          block_table_d, prefix_lens_d, n_acc_d, path_d, nb, B, Hkv, D, num_blocks,
                                          max_pages, new_prefix_lens_d, dev_status_d, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
+int32_t tv_selftest_wait(uint32_t limit_us, int32_t *dev_status_d, void *stream)
+{
+    if (limit_us < 1 || limit_us > 1000000u || !dev_status_d || !aligned(dev_status_d, 4)) return TV_ERR_INVALID_ARG;
+    cudaError_t e = tv::launch_selftest_wait((uint64_t)limit_us * 1000ull, dev_status_d,
+                                             static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
 

@@ -70,10 +70,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 }
 
 // Wait for the phase of parity `parity` to complete.  Returns false when the
-// CTA-wide abort flag is raised or the wait runs past kWaitLimitNs (the flag is
+// CTA-wide abort flag is raised or the wait runs past `limit_ns` (the flag is
 // then raised and TV_ERR_TIMEOUT reported).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          int32_t *status)
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                              int32_t *status, uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
@@ -81,13 +81,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 31) == 0) {
             if (*abort_flag) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (global_timer_ns() - t0 > limit_ns) {
                 *abort_flag = 1;
                 report_status(status, TV_ERR_TIMEOUT);
                 return false;
             }
         }
     }
+}
+
+// mbar_wait_for with the library-wide limit kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          int32_t *status)
+{
+    return mbar_wait_for(bar, parity, abort_flag, status, kWaitLimitNs);
 }
 
 // ----------------------------------------------------------------------- TMA

@@ -76,6 +76,9 @@ cudaError_t launch_kv_commit(uint16_t *k_cache, uint16_t *v_cache, const int32_t
                              int Hkv, int D, int num_blocks, int max_pages, int32_t *new_prefix_lens, int32_t *status,
                              cudaStream_t stream);
 
+// A kernel whose only job is to take the bounded-wait timeout path (see tv_selftest.cu).
+cudaError_t launch_selftest_wait(uint64_t limit_ns, int32_t *status, cudaStream_t stream);
+
 // Workspace bytes the attention needs with `ctas` CTAs over `row_tiles`
 // (sequence, kv head, 128-row tile) units, and that unit count for `a`.
 size_t attn_workspace_bytes(int ctas, int row_tiles);
