@@ -126,6 +126,7 @@ struct AttnParams {
 struct Sched {
     const int32_t *prefix_lens;
     int nb, B, Hkv, NT, MT, max_tokens;
+    int NP;  // pair tiles per unit: (MT + 1) / 2
 };
 
 __device__ __forceinline__ int mtile_tiles(int P, int B, int NT, int mt)
@@ -140,14 +141,13 @@ __device__ __forceinline__ int pair_tiles(const Sched &s, int P, int mp)
     return mtile_tiles(P, s.B, s.NT, min(2 * mp + 1, s.MT - 1));
 }
 
-// Items of one (sequence, kv head); 0 for a sequence whose prefix does not fit
-// its block table (reported as TV_ERR_INVALID_ARG).
-__device__ __forceinline__ int head_tiles(const Sched &s, int P)
+// Group items of one (sequence, kv head) unit: the KV tiles of its last pair tile, which
+// needs the most keys; 0 for a sequence whose prefix does not fit its block table
+// (reported as TV_ERR_INVALID_ARG).
+__device__ __forceinline__ int unit_tiles(const Sched &s, int P)
 {
     if (P < 0 || P > s.max_tokens - s.B) return 0;
-    int t = 0;
-    for (int mp = 0; 2 * mp < s.MT; ++mp) t += pair_tiles(s, P, mp);
-    return t;
+    return pair_tiles(s, P, s.NP - 1);
 }
 
 __device__ __forceinline__ long long warp_sum_ll(long long v)
@@ -157,25 +157,25 @@ __device__ __forceinline__ long long warp_sum_ll(long long v)
     return v;
 }
 
-// Total items.  Whole warp.
+// Total group items.  Whole warp.
 __device__ long long sched_total(const Sched &s, int lane)
 {
     long long tot = 0;
     for (int base = 0; base < s.nb; base += 32) {
         const int b = base + lane;
-        const long long t = (b < s.nb) ? (long long)s.Hkv * head_tiles(s, __ldcg(s.prefix_lens + b)) : 0;
+        const long long t = (b < s.nb) ? (long long)s.Hkv * unit_tiles(s, __ldcg(s.prefix_lens + b)) : 0;
         tot += warp_sum_ll(t);
     }
     return tot;
 }
 
-// Sequence and offset inside it of global item index t (t < total).  Whole warp.
+// Sequence and offset inside it of global group item t (t < total).  Whole warp.
 __device__ void sched_locate(const Sched &s, long long t, int lane, int &b_out, long long &off_out)
 {
     long long acc = 0;
     for (int base = 0; base < s.nb; base += 32) {
         const int b = base + lane;
-        const long long tb = (b < s.nb) ? (long long)s.Hkv * head_tiles(s, __ldcg(s.prefix_lens + b)) : 0;
+        const long long tb = (b < s.nb) ? (long long)s.Hkv * unit_tiles(s, __ldcg(s.prefix_lens + b)) : 0;
         long long incl = tb;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -196,18 +196,32 @@ __device__ void sched_locate(const Sched &s, long long t, int lane, int &b_out, 
     off_out = 0;
 }
 
-// CTAs that get work: at least kMinTilesPerCta items each, at most the grid.
-__device__ __forceinline__ long long active_ctas(long long total, int grid)
+// Groups that get work: at least kMinTilesPerCta group items each, at most `groups`.
+__device__ __forceinline__ long long active_groups(long long total, int groups)
 {
     long long c = (total + kMinTilesPerCta - 1) / kMinTilesPerCta;
-    if (c > grid) c = grid;
+    if (c > groups) c = groups;
     return c < 1 ? 1 : c;
+}
+
+// Groups the grid forms: NP CTAs each (one per pair tile of a unit), or a single group
+// whose lanes the grid's CTAs share when the grid is smaller than NP.
+__device__ __forceinline__ int grid_groups(int grid, int NP) { return grid >= NP ? grid / NP : 1; }
+
+// Group containing group item t, when `total` items are cut evenly into G groups.
+__device__ __forceinline__ long long group_of(long long t, long long total, long long G)
+{
+    return ((t + 1) * G - 1) / total;
 }
 
 struct Cursor {
     int b;
-    long long off;   // item offset inside sequence b
-    long long left;  // items this CTA still has to visit
+    long long off;   // group-item offset inside sequence b
+    long long left;  // group items this CTA still has to visit for its current lane
+    int lane;        // the pair tile (of every unit) this CTA computes
+    int lane_step;   // next lane: lane + lane_step (only when the grid is smaller than NP)
+    int b0;          // the range's start and length, to revisit it for the next lane
+    long long off0, left0;
 };
 
 struct Seg {
@@ -215,41 +229,45 @@ struct Seg {
     bool has_b;
 };
 
-// Next segment (a run of KV tiles of one pair tile) of this CTA's share.
-// Pair tiles are ordered (sequence, kv head, pair), KV tiles ascending.
+// Next segment (a run of KV tiles of one pair tile) of this CTA's share.  A group's CTAs
+// walk the same range of group items -- (sequence, kv head, KV tile) ascending -- each for
+// its own pair tile of every unit in it, so they read the same K/V pages at about the same
+// time and all but the first find them in L2.  A pair tile skips the unit's last tiles when
+// only later pair tiles need them.
 __device__ __forceinline__ bool next_seg(const Sched &s, Cursor &c, Seg &sg)
 {
-    while (c.left > 0 && c.b < s.nb) {
-        const int P = __ldcg(s.prefix_lens + c.b);
-        const int ht = head_tiles(s, P);
-        if (c.off >= (long long)ht * s.Hkv) {
-            ++c.b;
-            c.off = 0;
-            continue;
+    for (;;) {
+        while (c.left > 0 && c.b < s.nb) {
+            const int P = __ldcg(s.prefix_lens + c.b);
+            const int ut = unit_tiles(s, P);
+            if (c.off >= (long long)ut * s.Hkv) {
+                ++c.b;
+                c.off = 0;
+                continue;
+            }
+            const int g = (int)(c.off / ut);
+            const int rem = (int)(c.off - (long long)g * ut);
+            const int take = (int)min((long long)(ut - rem), c.left);
+            c.off += take;
+            c.left -= take;
+            const int n = pair_tiles(s, P, c.lane);
+            if (rem >= n) continue;  // tiles only this unit's later pair tiles need
+            sg.b = c.b;
+            sg.g = g;
+            sg.mp = c.lane;
+            sg.j0 = rem;
+            sg.j1 = min(rem + take, n);
+            sg.n_row = n;
+            sg.P = P;
+            sg.has_b = 2 * c.lane + 1 < s.MT;
+            return true;
         }
-        const int g = (int)(c.off / ht);
-        int rem = (int)(c.off - (long long)g * ht);
-        int mp = 0;
-        int n = pair_tiles(s, P, 0);
-        while (rem >= n) {
-            rem -= n;
-            ++mp;
-            n = pair_tiles(s, P, mp);
-        }
-        const int take = (int)min((long long)(n - rem), c.left);
-        sg.b = c.b;
-        sg.g = g;
-        sg.mp = mp;
-        sg.j0 = rem;
-        sg.j1 = rem + take;
-        sg.n_row = n;
-        sg.P = P;
-        sg.has_b = 2 * mp + 1 < s.MT;
-        c.off += take;
-        c.left -= take;
-        return true;
+        if (c.left0 <= 0 || c.lane + c.lane_step >= s.NP) return false;
+        c.lane += c.lane_step;
+        c.b = c.b0;
+        c.off = c.off0;
+        c.left = c.left0;
     }
-    return false;
 }
 
 constexpr int kMaxMaskWords = 8;  // ceil(256 / 32)
@@ -346,10 +364,12 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
     int *sh_b0 = reinterpret_cast<int *>(gbase + kOffMisc + 8);
     long long *sh_off0 = reinterpret_cast<long long *>(gbase + kOffMisc + 16);
     long long *sh_left = reinterpret_cast<long long *>(gbase + kOffMisc + 24);
+    int *sh_lane = reinterpret_cast<int *>(gbase + kOffMisc + 32);
+    int *sh_step = reinterpret_cast<int *>(gbase + kOffMisc + 36);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const Sched sch{p.prefix_lens, p.nb, p.B, p.Hkv, p.NT, p.MT, p.max_pages * kPage};
+    const Sched sch{p.prefix_lens, p.nb, p.B, p.Hkv, p.NT, p.MT, p.max_pages * kPage, (p.MT + 1) / 2};
 
     if (threadIdx.x == 0) {
         mbar_init(BAR(BAR_Q_FULL), 1);
@@ -387,13 +407,18 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
     // (griddepcontrol.wait before the first masked tile, or without a mask array at the
     // start of a segment that reaches the tree keys, and in every thread before it exits).
     if (warp == 2) {
+        // CTA c runs lane (pair tile) c % NP of group c / NP; each group takes an equal
+        // share of the group items.  A grid smaller than NP forms one group whose lanes
+        // its CTAs take in turn.
         const long long total = sched_total(sch, lane);
-        const long long C = active_ctas(total, gridDim.x);
-        const long long c = blockIdx.x;
+        const int grid = (int)gridDim.x;
+        const long long G = active_groups(total, grid_groups(grid, sch.NP));
+        const int grp = grid >= sch.NP ? (int)blockIdx.x / sch.NP : 0;
+        const int lane0 = grid >= sch.NP ? (int)blockIdx.x % sch.NP : (int)blockIdx.x;
         long long t0 = 0, t1 = 0;
-        if (c < C) {
-            t0 = total * c / C;
-            t1 = total * (c + 1) / C;
+        if (grp < G) {
+            t0 = total * grp / G;
+            t1 = total * (grp + 1) / G;
         }
         int b0 = sch.nb;
         long long off0 = 0;
@@ -402,6 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
             *sh_b0 = b0;
             *sh_off0 = off0;
             *sh_left = t1 - t0;
+            *sh_lane = lane0;
+            *sh_step = grid >= sch.NP ? sch.NP : grid;
         }
         if (blockIdx.x == 0) {
             for (int b = lane; b < sch.nb; b += 32) {
@@ -414,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const Cursor cur0{*sh_b0, *sh_off0, *sh_left};
+    const Cursor cur0{*sh_b0, *sh_off0, *sh_left, *sh_lane, *sh_step, *sh_b0, *sh_off0, *sh_left};
     pdl_launch_dependents();
 
     if (warp == 0) {
@@ -898,13 +925,13 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
 constexpr int kMergeThreads = 128;  // 32 rows x 4 column quarters
 constexpr int kMergeSplit = kM / 32; // CTAs per M tile
 
-// Pieces before sequence b_end.  Whole warp.
+// Group items before sequence b_end.  Whole warp.
 __device__ long long sched_prefix(const Sched &s, int b_end, int lane)
 {
     long long tot = 0;
     for (int base = 0; base < b_end; base += 32) {
         const int b = base + lane;
-        const long long t = (b < b_end) ? (long long)s.Hkv * head_tiles(s, __ldcg(s.prefix_lens + b)) : 0;
+        const long long t = (b < b_end) ? (long long)s.Hkv * unit_tiles(s, __ldcg(s.prefix_lens + b)) : 0;
         tot += warp_sum_ll(t);
     }
     return tot;
@@ -920,16 +947,17 @@ struct MergeParams {
 };
 
 // kMergeSplit CTAs per M tile (sequence, kv head, mt), each for 32 of its rows;
-// thread (warp q, lane l) owns row 32s + l and the columns 32q .. 32q+31.  An M
-// tile whose pair was cut between CTAs c0..c1 of the attention grid has one
-// piece in each: in c0's last slot (or its first, when the pair starts c0's
-// share) and in the first slot of c0+1 .. c1.  lse = ln sum_u e^{lse_u},
+// thread (warp q, lane l) owns row 32s + l and the columns 32q .. 32q+31.  The
+// attention grid's groups k0..k1 hold the pieces of an M tile whose pair tile (lane
+// mp of its unit) was cut between groups: lane mp of group k0 keeps its piece in its
+// last slot (or its first, when nothing of that lane comes before it in k0), lanes
+// mp of groups k0+1 .. k1 in their first.  lse = ln sum_u e^{lse_u},
 // O = sum_u e^{lse_u - lse} O_u, in one pass over batches of four pieces whose
 // lse and O loads are all in flight together (chunk-major partials: a warp's
 // loads are 512 contiguous bytes), with a running maximum between batches.
 __global__ void __launch_bounds__(kMergeThreads) tree_attn_merge_kernel(const MergeParams mp)
 {
-    __shared__ int s_c0, s_c1, s_first0;
+    __shared__ int s_k0, s_k1, s_first0;
     const int id = blockIdx.x / kMergeSplit;
     const int split = blockIdx.x % kMergeSplit;
     const int b = id / (mp.Hkv * mp.MT);
@@ -938,55 +966,74 @@ __global__ void __launch_bounds__(kMergeThreads) tree_attn_merge_kernel(const Me
     const int x = mt & 1;
     const int pm = mt >> 1;
     const int lane = threadIdx.x & 31, q = threadIdx.x >> 5;
-    const Sched sch{mp.prefix_lens, mp.nb, mp.B, mp.Hkv, mp.NT, mp.MT, mp.max_pages * kPage};
+    const Sched sch{mp.prefix_lens, mp.nb, mp.B, mp.Hkv, mp.NT, mp.MT, mp.max_pages * kPage, (mp.MT + 1) / 2};
 
     pdl_launch_dependents();  // the next kernel (its own wait keeps it ordered) may start launching
     if (q == 0) {  // prefix_lens is an input of both kernels: safe to read before the dependency wait
         const long long total = sched_total(sch, lane);
-        const long long C = active_ctas(total, mp.attn_grid);
+        const long long G = active_groups(total, grid_groups(mp.attn_grid, sch.NP));
         const long long start_b = sched_prefix(sch, b, lane);
         const int P = __ldcg(mp.prefix_lens + b);
-        const int ht = head_tiles(sch, P);
-        int c0 = 0, c1 = 0, first0 = 0;
-        if (ht > 0 && total > 0) {
-            long long r0 = start_b + (long long)g * ht;
-            for (int m = 0; m < pm; ++m) r0 += pair_tiles(sch, P, m);
-            const long long r1 = r0 + pair_tiles(sch, P, pm);
-            c0 = (int)(((r0 + 1) * C - 1) / total);
-            c1 = (int)((r1 * C - 1) / total);
-            first0 = (r0 == total * c0 / C) ? 0 : 1;
+        const int ut = unit_tiles(sch, P);
+        int k0 = 0, k1 = 0, first0 = 0;
+        if (ut > 0 && total > 0) {
+            const long long su = start_b + (long long)g * ut;  // the unit's first group item
+            const long long r1 = su + pair_tiles(sch, P, pm);   // past this pair tile's last one
+            k0 = (int)group_of(su, total, G);
+            k1 = (int)group_of(r1 - 1, total, G);
+            if (k1 > k0) {
+                // Lane pm has something in group k0 before this unit unless k0 starts with
+                // this unit, or k0 starts inside the unit right before it, past the tiles
+                // this lane needs there.
+                const long long s0 = total * k0 / G;
+                first0 = 1;
+                if (s0 == su) {
+                    first0 = 0;
+                } else {
+                    int bb;
+                    long long off;
+                    sched_locate(sch, s0, lane, bb, off);
+                    const int Pb = __ldcg(mp.prefix_lens + bb);
+                    const int utb = unit_tiles(sch, Pb);
+                    const long long rem = off % utb;
+                    if (s0 - rem + utb == su && rem >= pair_tiles(sch, Pb, pm)) first0 = 0;
+                }
+            }
         }
         if (lane == 0) {
-            s_c0 = c0;
-            s_c1 = c1;
+            s_k0 = k0;
+            s_k1 = k1;
             s_first0 = first0;
         }
     }
     __syncthreads();
-    const int c0 = s_c0, c1 = s_c1, first0 = s_first0;
+    const int k0 = s_k0, k1 = s_k1, first0 = s_first0;
     // Every CTA waits for the attention grid (so this grid never completes before it);
     // past this point the partials are complete and visible.
     pdl_wait_primary();
-    if (c0 == c1) return;  // the attention kernel wrote this M tile itself
+    if (k0 == k1) return;  // the attention kernel wrote this M tile itself
     const int r = split * 32 + lane;
     const int i = mt * mp.NT + r / mp.G;
     if (i >= mp.B) return;  // a row past the tree
 
-    auto slot_of = [&](int c) -> size_t { return (2 * (size_t)c + (c == c0 ? first0 : 0)) * 2 + x; };
+    // group k's lane pm is CTA k * NP + pm (several groups exist only when the grid holds NP CTAs)
+    auto slot_of = [&](int k) -> size_t {
+        return (2 * ((size_t)k * sch.NP + pm) + (k == k0 ? first0 : 0)) * 2 + x;
+    };
     // One pass: each batch's lse and O loads are in flight together; a running
     // maximum rescales the sums between batches.
     float m = -INFINITY, wsum = 0.f;
     float4 acc[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int cb = c0; cb <= c1; cb += 4) {
+    for (int kb = k0; kb <= k1; kb += 4) {
         float l[4];
         uint4 v[4][4];  // 8 fp16 columns each: this thread's 32 columns of 4 pieces
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const int c = cb + u;
-            const bool in = c <= c1;
-            const size_t slot = slot_of(in ? c : c0);
+            const int k = kb + u;
+            const bool in = k <= k1;
+            const size_t slot = slot_of(in ? k : k0);
             l[u] = in ? __ldcg(mp.ws_lse + slot * kM + r) : -INFINITY;
             const uint4 *src = mp.ws_o + (slot * (kHeadDim / 8) + q * 4) * kM + r;
 #pragma unroll
