@@ -63,6 +63,7 @@ constexpr int kHeadDim = 128;  // D
 constexpr int kPage = 16;      // tokens per KV page
 constexpr int kSlots = 5;      // K/V ring: K(j) -> slot (2j) % 5, V(j) -> slot (2j + 1) % 5
 constexpr int kThreads = 384;
+constexpr int kSoftmaxWarps = kM / 32;  // warps of one softmax warpgroup: each arrives once per phase
 constexpr int kMinTilesPerCta = 2;
 constexpr uint32_t kRegsLow = 64;    // warpgroup 0 after setmaxnreg.dec (128 x 64 + 256 x 216 <= 384 x 168)
 constexpr uint32_t kRegsHigh = 216; // softmax warpgroups after setmaxnreg.inc
@@ -380,13 +381,13 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(BAR(BAR_S_FULL + x), 1);
-            mbar_init(BAR(BAR_P_FULL + x), kM);
+            mbar_init(BAR(BAR_P_FULL + x), kSoftmaxWarps);
             mbar_init(BAR(BAR_PV_DONE + x), 1);
-            mbar_init(BAR(BAR_O_EMPTY + x), kM);
+            mbar_init(BAR(BAR_O_EMPTY + x), kSoftmaxWarps);
         }
         mbar_init(BAR(BAR_MMA_DONE), 1);
-        mbar_init(BAR(BAR_ML_FULL), kM);
-        mbar_init(BAR(BAR_ML_READ), kM);
+        mbar_init(BAR(BAR_ML_FULL), kSoftmaxWarps);
+        mbar_init(BAR(BAR_ML_READ), kSoftmaxWarps);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -444,17 +445,23 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
     const Cursor cur0{*sh_b0, *sh_off0, *sh_left, *sh_lane, *sh_step, *sh_b0, *sh_off0, *sh_left};
     pdl_launch_dependents();
 
-    if (warp == 0) {
-        // ---------------------------------------------------------- TMA producer
+    if (warp == 0 || warp == 2) {
+        // ---------------------------------------------------------- TMA producers
+        // Warp 0 loads Q and the K tiles, warp 2 the V tiles.  A 16-row page half is a
+        // 2 KB copy, and one warp issues them at ~26 B/clk/SM on GB300, below the MMA
+        // loop's need; two issuing warps overlap their copies.  Each warp waits its own
+        // ring positions in order, and the MMA warp releases positions in order, so no
+        // wait can alias a later phase of its slot.
         regs_decrease<kRegsLow>();
+        const int kvh = warp == 0 ? 0 : 1;
         Cursor cur = cur0;
         Seg sg;
         uint32_t kv = 0, seg_i = 0;
         bool ok = true;
         const int oob_row = p.num_blocks * p.Hkv * kPage;  // first row past the cache: zero fill
         while (ok && next_seg(sch, cur, sg)) {
-            if (seg_i > 0 && !mbar_wait(BAR(BAR_Q_EMPTY), (seg_i - 1) & 1, abort_flag, p.status)) break;
-            if (lane == 0) {
+            if (kvh == 0 && seg_i > 0 && !mbar_wait(BAR(BAR_Q_EMPTY), (seg_i - 1) & 1, abort_flag, p.status)) break;
+            if (kvh == 0 && lane == 0) {
                 mbar_arrive_expect_tx(BAR(BAR_Q_FULL), kTileBytes * (sg.has_b ? 2 : 1));
                 for (int x = 0; x < (sg.has_b ? 2 : 1); ++x) {
                     const int node0 = (2 * sg.mp + x) * p.NT;
@@ -489,20 +496,17 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                 }
                 const int my_row = __shfl_sync(0xffffffffu, rows_cur, in_batch * 8 + (lane >> 1));
                 const uint32_t dst_off = (uint32_t)(lane & 1) * kHalfBytes + (uint32_t)(lane >> 1) * (kPage * 128);
-                for (int kvh = 0; kvh < 2; ++kvh) {  // K(j), then V(j)
-                    const uint32_t q = 2 * kv + kvh;
-                    const uint32_t sl = ring_slot(q);
-                    if (!mbar_wait(BAR(BAR_KV_EMPTY + sl), ring_phase(q) ^ 1, abort_flag, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    if (lane == 0) mbar_arrive_expect_tx(BAR(BAR_KV_FULL + sl), kTileBytes);
-                    __syncwarp();
-                    if (lane < 16)
-                        tma_load_2d(sKV + sl * kTileBytes + dst_off, kvh ? (const void *)&p.tm_v : (const void *)&p.tm_k,
-                                    (lane & 1) * 64, my_row, BAR(BAR_KV_FULL + sl));
+                const uint32_t q = 2 * kv + kvh;  // ring position of K(j) or V(j)
+                const uint32_t sl = ring_slot(q);
+                if (!mbar_wait(BAR(BAR_KV_EMPTY + sl), ring_phase(q) ^ 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
                 }
-                if (!ok) break;
+                if (lane == 0) mbar_arrive_expect_tx(BAR(BAR_KV_FULL + sl), kTileBytes);
+                __syncwarp();
+                if (lane < 16)
+                    tma_load_2d(sKV + sl * kTileBytes + dst_off, kvh ? (const void *)&p.tm_v : (const void *)&p.tm_k,
+                                (lane & 1) * 64, my_row, BAR(BAR_KV_FULL + sl));
             }
             ++seg_i;
         }
@@ -532,21 +536,26 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
         // ring position q: K(j) = 2j, V(j) = 2j + 1 (KV tile counter j over the whole CTA)
         auto full = [&](uint32_t q) { return wait_bar(BAR_KV_FULL + ring_slot(q), ring_phase(q)); };
         auto release = [&](uint32_t q) { umma_commit(BAR(BAR_KV_EMPTY + ring_slot(q))); };
+        // Descriptors are built once per call and only their start-address field moves
+        // per K slice (see umma_bf16_ss_lohi).
+        const uint64_t dq0 = sdesc_kmajor_sw128(sQ), dkv0 = sdesc_kmajor_sw128(sKV);
+        const uint64_t dv0 = sdesc_mnmajor_sw128(sKV, kHalfBytes);
+        const uint32_t dq_lo = (uint32_t)dq0, dk_lo = (uint32_t)dkv0, dv_lo = (uint32_t)dv0;
+        const uint32_t dk_hi = (uint32_t)(dkv0 >> 32), dv_hi = (uint32_t)(dv0 >> 32);
         auto qk = [&](int x, int qx, uint32_t kt) {  // S_x = Q_qx K(kt)^T (lane 0)
-            const uint32_t qb = sQ + qx * kTileBytes, kb = sKV + ring_slot(2 * kt) * kTileBytes;
+            const uint32_t qa = dq_lo + qx * (kTileBytes >> 4), ka = dk_lo + ring_slot(2 * kt) * (kTileBytes >> 4);
 #pragma unroll
             for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                umma_bf16_ss(tmem + tmem_s(x), sdesc_kmajor_sw128(qb + off), sdesc_kmajor_sw128(kb + off), kIdescQK,
-                             kk > 0 ? 1u : 0u);
+                const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+                umma_bf16_ss_lohi(tmem + tmem_s(x), qa + off, dk_hi, ka + off, dk_hi, kIdescQK, kk > 0 ? 1u : 0u);
             }
         };
         auto pv = [&](int x, uint32_t kt, bool accumulate) {  // O_x (+)= P_x V(kt) (lane 0)
-            const uint32_t vb = sKV + ring_slot(2 * kt + 1) * kTileBytes;
+            const uint32_t va = dv_lo + ring_slot(2 * kt + 1) * (kTileBytes >> 4);
 #pragma unroll
             for (int kk = 0; kk < kN / 16; ++kk)
-                umma_bf16_ts(tmem + tmem_o(x), tmem + tmem_s(x) + kk * 8, sdesc_mnmajor_sw128(vb + kk * 2048, kHalfBytes),
-                             kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+                umma_bf16_ts_lohi(tmem + tmem_o(x), tmem + tmem_s(x) + kk * 8, va + kk * (2048 >> 4), dv_hi, kIdescPV,
+                                  (accumulate || kk > 0) ? 1u : 0u);
         };
         // P_x of the slot's lx-th tile in the segment is in TMEM; before the slot's first PV
         // of a segment, the previous segment's epilogue of slot x has read O_x
@@ -656,7 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
             const uint64_t t0 = global_timer_ns();
             while (!mbar_try_wait(BAR(BAR_MMA_DONE), 0) && global_timer_ns() - t0 < kWaitLimitNs) { }
         }
-    } else if (warp < 4) {
+    } else if (warp == 3) {
         regs_decrease<kRegsLow>();
     } else {
         // ------------------------------------------------ softmax + epilogue of slot x
@@ -800,7 +809,8 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                 }
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(BAR(BAR_P_FULL + x));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(BAR_P_FULL + x));
             }
             if (!ok) break;
 
@@ -814,10 +824,11 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                 sh_m[row] = m_run;
                 sh_l[row] = l_run;
                 tc_fence_before();
-                mbar_arrive(BAR(BAR_ML_FULL));
-                if (!mbar_wait(BAR(BAR_ML_READ), n_merge & 1, abort_flag, p.status)) break;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(BAR_ML_FULL));
+                if (!__all_sync(0xffffffffu, mbar_wait(BAR(BAR_ML_READ), n_merge & 1, abort_flag, p.status))) break;
                 tc_fence_after();
-                mbar_arrive(BAR(BAR_O_EMPTY + 1));
+                if (lane == 0) mbar_arrive(BAR(BAR_O_EMPTY + 1));
                 gx += nx;
                 ++seg_i;
                 ++n_merge;
@@ -892,11 +903,13 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
             }
             if (merge_slots) {
                 tc_fence_before();
-                mbar_arrive(BAR(BAR_ML_READ));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(BAR_ML_READ));
                 ++n_merge;
             }
             tc_fence_before();
-            mbar_arrive(BAR(BAR_O_EMPTY + x));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(BAR_O_EMPTY + x));
             if (valid) {
                 if (whole)
                     p.lse[orow] = lse_nat;
