@@ -100,6 +100,13 @@ constexpr uint32_t kTmemCols = 512;
 __host__ __device__ constexpr uint32_t tmem_s(int x) { return (uint32_t)x * 256; }        // S_x, P_x over its first 64
 __host__ __device__ constexpr uint32_t tmem_o(int x) { return (uint32_t)x * 256 + 128; }  // O_x
 
+// Shared-memory descriptor halves of the 128-byte-swizzled operand tiles (the fields of
+// sdesc_kmajor_sw128 / sdesc_mnmajor_sw128): high half SBO = 1024 bytes, the fixed
+// version bit and the swizzle mode; low half leading byte offset (K-major: unused, 1;
+// MN-major: the 64-column block stride) above the start address, which is added in.
+constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+constexpr uint32_t kDescLoK = 1u << 16;
+constexpr uint32_t kDescLoV = (kHalfBytes >> 4) << 16;
 constexpr uint32_t kIdescQK = umma_idesc_bf16(kM, kN, 0);        // B = K tile, K-major
 constexpr uint32_t kIdescPV = umma_idesc_bf16(kM, kHeadDim, 1);  // B = V tile, MN-major
 constexpr float kRescaleLog2 = 8.0f;
@@ -525,143 +532,165 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
         // go out back to back under one commit (S_FULL, which the softmax needs anyway),
         // a step's K/V waits are done once up front, PV_DONE is committed only after a
         // slot's last PV of the segment, and ring releases follow both slots' groups.
+        // The warp shares its SM sub-partition with two softmax warps, so its own
+        // instruction count matters too: ring positions advance incrementally and the
+        // descriptors come from one register.  The control flow stays warp-uniform (lane 0
+        // alone issues), which lets the loop's invariants live in uniform registers.
         regs_decrease<kRegsLow>();
-        Cursor cur = cur0;
-        Seg sg;
-        uint32_t kv = 0, seg_i = 0;
-        // tiles and segments per slot so far (barrier phases)
-        uint32_t gs0 = 0, gs1 = 0, sc0 = 0, sc1 = 0;
-        bool ok = true;
-        auto wait_bar = [&](int idx, uint32_t parity) { return mbar_wait(BAR(idx), parity, abort_flag, p.status); };
-        // ring position q: K(j) = 2j, V(j) = 2j + 1 (KV tile counter j over the whole CTA)
-        auto full = [&](uint32_t q) { return wait_bar(BAR_KV_FULL + ring_slot(q), ring_phase(q)); };
-        auto release = [&](uint32_t q) { umma_commit(BAR(BAR_KV_EMPTY + ring_slot(q))); };
-        // Descriptors are built once per call and only their start-address field moves
-        // per K slice (see umma_bf16_ss_lohi).
-        const uint64_t dq0 = sdesc_kmajor_sw128(sQ), dkv0 = sdesc_kmajor_sw128(sKV);
-        const uint64_t dv0 = sdesc_mnmajor_sw128(sKV, kHalfBytes);
-        const uint32_t dq_lo = (uint32_t)dq0, dk_lo = (uint32_t)dkv0, dv_lo = (uint32_t)dv0;
-        const uint32_t dk_hi = (uint32_t)(dkv0 >> 32), dv_hi = (uint32_t)(dv0 >> 32);
-        auto qk = [&](int x, int qx, uint32_t kt) {  // S_x = Q_qx K(kt)^T (lane 0)
-            const uint32_t qa = dq_lo + qx * (kTileBytes >> 4), ka = dk_lo + ring_slot(2 * kt) * (kTileBytes >> 4);
+        {
+            Cursor cur = cur0;
+            Seg sg;
+            uint32_t kv = 0, seg_i = 0;
+            // tiles and segments per slot so far (barrier phases)
+            uint32_t gs0 = 0, gs1 = 0, sc0 = 0, sc1 = 0;
+            bool ok = true;
+            auto wait_bar = [&](int idx, uint32_t parity) { return mbar_wait(BAR(idx), parity, abort_flag, p.status); };
+            // ring position q: K(j) = 2j, V(j) = 2j + 1 (KV tile counter j over the whole CTA)
+            struct RingPos {
+                uint32_t slot, phase;  // q % kSlots, (q / kSlots) & 1
+            };
+            auto at = [](uint32_t q) { return RingPos{q % kSlots, (q / kSlots) & 1u}; };
+            auto ahead = [](RingPos r, uint32_t d) {  // position q + d, d < kSlots
+                r.slot += d;
+                if (r.slot >= (uint32_t)kSlots) {
+                    r.slot -= kSlots;
+                    r.phase ^= 1u;
+                }
+                return r;
+            };
+            auto full = [&](RingPos r) { return wait_bar(BAR_KV_FULL + r.slot, r.phase); };
+            // Descriptors: the high halves are constants and every low half is the
+            // 1024-aligned shared-memory base (in 16-byte units) plus a constant, so one
+            // register holds them all (this warp runs in 64 registers); only the
+            // start-address field moves per K slice (see umma_bf16_ss_lohi).
+            const uint32_t d0 = base >> 4;
+            auto qk = [&](int x, int qx, RingPos rk) {  // S_x = Q_qx K^T, K in ring slot rk
+                const uint32_t qa = d0 + kDescLoK + ((kOffQ + qx * kTileBytes) >> 4);
+                const uint32_t ka = d0 + kDescLoK + (kOffKV >> 4) + rk.slot * (kTileBytes >> 4);
 #pragma unroll
-            for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-                const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
-                umma_bf16_ss_lohi(tmem + tmem_s(x), qa + off, dk_hi, ka + off, dk_hi, kIdescQK, kk > 0 ? 1u : 0u);
-            }
-        };
-        auto pv = [&](int x, uint32_t kt, bool accumulate) {  // O_x (+)= P_x V(kt) (lane 0)
-            const uint32_t va = dv_lo + ring_slot(2 * kt + 1) * (kTileBytes >> 4);
+                for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+                    const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+                    umma_bf16_ss_lohi(tmem + tmem_s(x), qa + off, kDescHi, ka + off, kDescHi, kIdescQK,
+                                      kk > 0 ? 1u : 0u);
+                }
+            };
+            auto pv = [&](int x, RingPos rv, bool accumulate) {  // O_x (+)= P_x V, V in ring slot rv
+                const uint32_t va = d0 + kDescLoV + (kOffKV >> 4) + rv.slot * (kTileBytes >> 4);
 #pragma unroll
-            for (int kk = 0; kk < kN / 16; ++kk)
-                umma_bf16_ts_lohi(tmem + tmem_o(x), tmem + tmem_s(x) + kk * 8, va + kk * (2048 >> 4), dv_hi, kIdescPV,
-                                  (accumulate || kk > 0) ? 1u : 0u);
-        };
-        // P_x of the slot's lx-th tile in the segment is in TMEM; before the slot's first PV
-        // of a segment, the previous segment's epilogue of slot x has read O_x
-        auto wait_p = [&](int x, int lx) -> bool {
-            const uint32_t gsx = x ? gs1 : gs0, scx = x ? sc1 : sc0;
-            if (!wait_bar(BAR_P_FULL + x, (gsx + lx) & 1)) return false;
-            return !(lx == 0 && scx > 0 && !wait_bar(BAR_O_EMPTY + x, (scx - 1) & 1));
-        };
-        while (ok && next_seg(sch, cur, sg)) {
-            const int n = sg.j1 - sg.j0;
-            const bool pair = sg.has_b;
-            const int nx0 = pair ? n : (n + 1) / 2, nx1 = pair ? n : n / 2;
-            if (!wait_bar(BAR_Q_FULL, seg_i & 1)) { ok = false; break; }
-            if (pair) {
-                if (!full(2 * kv)) { ok = false; break; }
-                tc_fence_after();
-                if (lane == 0) {
-                    qk(0, 0, kv);
-                    umma_commit(BAR(BAR_S_FULL + 0));
-                    qk(1, 1, kv);
-                    umma_commit(BAR(BAR_S_FULL + 1));
-                    release(2 * kv);
-                    if (n == 1) umma_commit(BAR(BAR_Q_EMPTY));
-                }
-                __syncwarp();
-                for (int t = 0; t < n; ++t) {
-                    const uint32_t kt = kv + t;
-                    const bool more = t + 1 < n;
-                    if (!full(2 * kt + 1) || (more && !full(2 * kt + 2))) { ok = false; break; }
-                    for (int x = 0; x < 2; ++x) {
-                        if (!wait_p(x, t)) { ok = false; break; }
-                        tc_fence_after();
-                        if (lane == 0) {
-                            pv(x, kt, t > 0);
-                            if (more) {
-                                qk(x, x, kt + 1);
-                                umma_commit(BAR(BAR_S_FULL + x));
-                            } else {
-                                umma_commit(BAR(BAR_PV_DONE + x));
-                            }
-                        }
-                        __syncwarp();
-                    }
-                    if (!ok) break;
-                    if (lane == 0) {
-                        release(2 * kt + 1);
-                        if (more) release(2 * kt + 2);
-                        if (t + 2 == n) umma_commit(BAR(BAR_Q_EMPTY));
-                    }
-                    __syncwarp();
-                }
-            } else {
-                // issue order: QK_0(0), QK_1(1), then per tile t: PV_{t%2}(t), QK_{t%2}(t+2)
-                if (!full(2 * kv) || (n > 1 && !full(2 * kv + 2))) { ok = false; break; }
-                tc_fence_after();
-                if (lane == 0) {
-                    qk(0, 0, kv);
-                    umma_commit(BAR(BAR_S_FULL + 0));
-                    release(2 * kv);
-                    if (n > 1) {
-                        qk(1, 0, kv + 1);
-                        umma_commit(BAR(BAR_S_FULL + 1));
-                        release(2 * kv + 2);
-                    }
-                    if (n <= 2) umma_commit(BAR(BAR_Q_EMPTY));
-                }
-                __syncwarp();
-                for (int t = 0; t < n; ++t) {
-                    const uint32_t kt = kv + t;
-                    const int x = t & 1;
-                    const bool more = t + 2 < n;
-                    // PV(t) waits only for V(t): these segments are bandwidth-bound, and K(t+2)
-                    // is two tiles further out in the ring
-                    if (!full(2 * kt + 1) || !wait_p(x, t >> 1)) { ok = false; break; }
+                for (int kk = 0; kk < kN / 16; ++kk)
+                    umma_bf16_ts_lohi(tmem + tmem_o(x), tmem + tmem_s(x) + kk * 8, va + kk * (2048 >> 4), kDescHi,
+                                      kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+            };
+            // P_x of the slot's lx-th tile in the segment is in TMEM; before the slot's first PV
+            // of a segment, the previous segment's epilogue of slot x has read O_x
+            auto wait_p = [&](int x, int lx) -> bool {
+                const uint32_t gsx = x ? gs1 : gs0, scx = x ? sc1 : sc0;
+                if (!wait_bar(BAR_P_FULL + x, (gsx + lx) & 1)) return false;
+                return !(lx == 0 && scx > 0 && !wait_bar(BAR_O_EMPTY + x, (scx - 1) & 1));
+            };
+            while (ok && next_seg(sch, cur, sg)) {
+                const int n = sg.j1 - sg.j0;
+                const bool pair = sg.has_b;
+                const int nx0 = pair ? n : (n + 1) / 2, nx1 = pair ? n : n / 2;
+                if (!wait_bar(BAR_Q_FULL, seg_i & 1)) { ok = false; break; }
+                const RingPos r0 = at(2 * kv);  // K of the segment's first tile
+                if (pair) {
+                    if (!full(r0)) { ok = false; break; }
                     tc_fence_after();
                     if (lane == 0) {
-                        pv(x, kt, t > 1);
-                        if (!more) umma_commit(BAR(BAR_PV_DONE + x));
-                        release(2 * kt + 1);
+                        qk(0, 0, r0);
+                        umma_commit(BAR(BAR_S_FULL + 0));
+                        qk(1, 1, r0);
+                        umma_commit(BAR(BAR_S_FULL + 1));
+                        umma_commit(BAR(BAR_KV_EMPTY + r0.slot));
+                        if (n == 1) umma_commit(BAR(BAR_Q_EMPTY));
                     }
                     __syncwarp();
-                    if (more) {
-                        if (!full(2 * kt + 4)) { ok = false; break; }
-                        tc_fence_after();
+                    RingPos rv = ahead(r0, 1), rk = ahead(r0, 2);  // V(t), K(t + 1)
+                    for (int t = 0; t < n; ++t) {
+                        const bool more = t + 1 < n;
+                        if (!full(rv) || (more && !full(rk))) { ok = false; break; }
+                        for (int x = 0; x < 2; ++x) {
+                            if (!wait_p(x, t)) { ok = false; break; }
+                            tc_fence_after();
+                            if (lane == 0) {
+                                pv(x, rv, t > 0);
+                                if (more) {
+                                    qk(x, x, rk);
+                                    umma_commit(BAR(BAR_S_FULL + x));
+                                } else {
+                                    umma_commit(BAR(BAR_PV_DONE + x));
+                                }
+                            }
+                            __syncwarp();
+                        }
+                        if (!ok) break;
                         if (lane == 0) {
-                            qk(x, 0, kt + 2);
-                            umma_commit(BAR(BAR_S_FULL + x));
-                            release(2 * kt + 4);
-                            if (t + 3 == n) umma_commit(BAR(BAR_Q_EMPTY));
+                            umma_commit(BAR(BAR_KV_EMPTY + rv.slot));
+                            if (more) umma_commit(BAR(BAR_KV_EMPTY + rk.slot));
+                            if (t + 2 == n) umma_commit(BAR(BAR_Q_EMPTY));
                         }
                         __syncwarp();
+                        rv = ahead(rv, 2);
+                        rk = ahead(rk, 2);
+                    }
+                } else {
+                    // issue order: QK_0(0), QK_1(1), then per tile t: PV_{t%2}(t), QK_{t%2}(t+2)
+                    const RingPos r2 = ahead(r0, 2);  // K of the second tile
+                    if (!full(r0) || (n > 1 && !full(r2))) { ok = false; break; }
+                    tc_fence_after();
+                    if (lane == 0) {
+                        qk(0, 0, r0);
+                        umma_commit(BAR(BAR_S_FULL + 0));
+                        umma_commit(BAR(BAR_KV_EMPTY + r0.slot));
+                        if (n > 1) {
+                            qk(1, 0, r2);
+                            umma_commit(BAR(BAR_S_FULL + 1));
+                            umma_commit(BAR(BAR_KV_EMPTY + r2.slot));
+                        }
+                        if (n <= 2) umma_commit(BAR(BAR_Q_EMPTY));
+                    }
+                    __syncwarp();
+                    RingPos rv = ahead(r0, 1), rk = ahead(r0, 4);  // V(t), K(t + 2)
+                    for (int t = 0; t < n; ++t) {
+                        const int x = t & 1;
+                        const bool more = t + 2 < n;
+                        // PV(t) waits only for V(t): these segments are bandwidth-bound, and K(t+2)
+                        // is two tiles further out in the ring
+                        if (!full(rv) || !wait_p(x, t >> 1)) { ok = false; break; }
+                        tc_fence_after();
+                        if (lane == 0) {
+                            pv(x, rv, t > 1);
+                            if (!more) umma_commit(BAR(BAR_PV_DONE + x));
+                            umma_commit(BAR(BAR_KV_EMPTY + rv.slot));
+                        }
+                        __syncwarp();
+                        if (more) {
+                            if (!full(rk)) { ok = false; break; }
+                            tc_fence_after();
+                            if (lane == 0) {
+                                qk(x, 0, rk);
+                                umma_commit(BAR(BAR_S_FULL + x));
+                                umma_commit(BAR(BAR_KV_EMPTY + rk.slot));
+                                if (t + 3 == n) umma_commit(BAR(BAR_Q_EMPTY));
+                            }
+                            __syncwarp();
+                        }
+                        rv = ahead(rv, 2);
+                        rk = ahead(rk, 2);
                     }
                 }
+                if (!ok) break;
+                kv += n;
+                gs0 += nx0;
+                gs1 += nx1;
+                if (nx0 > 0) ++sc0;
+                if (nx1 > 0) ++sc1;
+                ++seg_i;
             }
-            if (!ok) break;
-            kv += n;
-            gs0 += nx0;
-            gs1 += nx1;
-            if (nx0 > 0) ++sc0;
-            if (nx1 > 0) ++sc1;
-            ++seg_i;
-        }
-        // Every MMA this CTA issued completes before TMEM is released.
-        if (lane == 0) umma_commit(BAR(BAR_MMA_DONE));
-        __syncwarp();
-        {
+            // Every MMA this CTA issued completes before TMEM is released.
+            if (lane == 0) umma_commit(BAR(BAR_MMA_DONE));
+            __syncwarp();
             const uint64_t t0 = global_timer_ns();
             while (!mbar_try_wait(BAR(BAR_MMA_DONE), 0) && global_timer_ns() - t0 < kWaitLimitNs) { }
         }
@@ -774,24 +803,25 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                 // The scale and the row sum use packed f32x2 math: these warps share each SM
                 // sub-partition with the MMA and TMA warps, and every issue slot they leave free
                 // lets those keep the tensor pipe and the K/V ring fed.
-                float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+                const float2 scale2 = make_float2(sl2, sl2), negm2 = make_float2(neg_m, neg_m);
+                float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
 #pragma unroll
                     for (int e2 = 0; e2 < 16; ++e2) {
-                        float a = __uint_as_float(s[c][2 * e2]), b = __uint_as_float(s[c][2 * e2 + 1]);
-                        ffma2(a, b, sl2, neg_m);
-                        a = ex2_approx(a);
-                        b = ex2_approx(b);
+                        float2 v = make_float2(__uint_as_float(s[c][2 * e2]), __uint_as_float(s[c][2 * e2 + 1]));
+                        v = __ffma2_rn(v, scale2, negm2);
+                        v.x = ex2_approx(v.x);
+                        v.y = ex2_approx(v.y);
                         if (e2 & 1)
-                            fadd2(l2, l3, a, b);
+                            lb = __fadd2_rn(lb, v);
                         else
-                            fadd2(l0, l1, a, b);
-                        s[c][e2] = pack_bf16x2(a, b);
+                            la = __fadd2_rn(la, v);
+                        s[c][e2] = pack_bf16x2(v.x, v.y);
                     }
                     if (c & 1) tmem_st16x2(lane_addr + col_s + (c >> 1) * 32, s[c - 1], s[c]);
                 }
-                l_run += (l0 + l1) + (l2 + l3);
+                l_run += (la.x + la.y) + (lb.x + lb.y);
                 // O_x *= alpha before PV(t) adds this tile (PV(t) waits for P_FULL below).  TMEM
                 // loads/stores are warp-wide (.sync.aligned), so the whole warp takes the branch
                 // when any lane needs it, each lane with its own factor.  Before this slot's first

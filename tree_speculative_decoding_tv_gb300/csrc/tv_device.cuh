@@ -320,27 +320,6 @@ __device__ __forceinline__ void tmem_st16x2(uint32_t taddr, const uint32_t (&a)[
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// (a, b) = (a, b) * s + c as one packed f32x2 FMA (one issue slot for two lanes of math)
-__device__ __forceinline__ void ffma2(float &a, float &b, float s, float c)
-{
-    uint64_t x, ss, cc, r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a), "f"(b));
-    asm("mov.b64 %0, {%1, %1};" : "=l"(ss) : "f"(s));
-    asm("mov.b64 %0, {%1, %1};" : "=l"(cc) : "f"(c));
-    asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(x), "l"(ss), "l"(cc));
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
-}
-
-// (a, b) += (x, y) as one packed f32x2 add
-__device__ __forceinline__ void fadd2(float &a, float &b, float x, float y)
-{
-    uint64_t p, q, r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(p) : "f"(a), "f"(b));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(q) : "f"(x), "f"(y));
-    asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(r) : "l"(p), "l"(q));
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
-}
-
 // max of three floats (a NaN operand is ignored, like fmaxf)
 __device__ __forceinline__ float fmax3(float a, float b, float c)
 {
