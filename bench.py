@@ -184,7 +184,7 @@ class Step:
                         torch.empty(w.nb, dtype=torch.int32, device=dev),
                         torch.empty((w.nb, w.B), dtype=torch.int32, device=dev),
                         torch.empty(w.nb, dtype=torch.int32, device=dev))
-        self.acc_ws = torch.empty(tv.accept_workspace_size(w.V, w.B, w.nb), dtype=torch.uint8, device=dev)
+        self.acc_ws = torch.zeros(tv.accept_workspace_size(w.V, w.B, w.nb), dtype=torch.uint8, device=dev)
         self.launches_per_step = 4  # attention, merge, argmax, acceptance (the masks are folded in)
         self.g_step = self.g_attn = self.g_acc = None
 

@@ -194,8 +194,13 @@ TV_API int32_t tv_attn(const tv_attn_args *args, void *workspace_d, size_t works
  *   bonus_d        int32 [nb] (out)
  *   workspace_d    device buffer of at least tv_accept_workspace_size(V, B, nb)
  *                  bytes (one 8-byte argmax key per logits row), 8-byte aligned,
- *                  contents ignored on entry (the call writes every key before
- *                  reading it; concurrent calls need separate workspaces)
+ *                  ZEROED before the first call that uses it (cudaMemsetAsync
+ *                  once): the argmax combines partial maxima into the keys with
+ *                  atomic maxima, and the acceptance kernel sets every key it
+ *                  reads back to zero, so each call leaves the workspace zeroed for
+ *                  the next.  A call that returns TV_ERR_CUDA may leave keys behind:
+ *                  zero the workspace again before reusing it.  Concurrent calls need
+ *                  separate workspaces.
  * Returns TV_OK, TV_ERR_INVALID_ARG, TV_ERR_UNSUPPORTED_SHAPE (B outside
  * [1, 256], V > INT32_MAX - 8192, or nb * B * ceil(V / 4096) >= 2^31) or
  * TV_ERR_CUDA.  A parent array that is not topological is reported through
@@ -384,10 +389,13 @@ TV_API int32_t tv_accept_fused(const uint16_t *logits_d, int32_t V, const int32_
  *     cudaDeviceReset the next call sees a new context and looks the address
  *     up again (the module, and so the array, may move), so make that call
  *     outside a capture too.
- *   - Every call on a device shares the array and leaves its last contents
- *     there; each call writes every part it reads before reading it.  Calls whose work
- *     overlaps on the GPU (different streams, no ordering between them) race on
- *     the array and their results are undefined: order them on one stream.
+ *   - Every call on a device shares the array.  The array starts at zero when the
+ *     library is loaded and every call leaves it at zero (the argmax combines
+ *     into it with atomic maxima, the acceptance kernel resets what it read); if
+ *     a call returns TV_ERR_CUDA, the next call on that device first launches a
+ *     small kernel that zeroes it again.  Calls whose work overlaps on the GPU
+ *     (different streams, no ordering between them) race on the array and their
+ *     results are undefined: order them on one stream.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  */
 #define TV_ACCEPT_NOALLOC_MAX_ROWS 8192

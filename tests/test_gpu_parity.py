@@ -9,6 +9,7 @@ import pytest
 import torch
 
 import oracle
+import tree_speculative_decoding_tv_gb300 as tv
 import workloads as wl
 from tests.helpers import DevWorkload, assert_attn_close
 
@@ -210,3 +211,28 @@ def test_attention_reports_short_block_table():
     d.attn(mask)
     torch.cuda.synchronize()
     assert d.status.item() == 1  # TV_ERR_INVALID_ARG
+
+
+def test_accept_workspace_is_left_zeroed_and_reused():
+    """tv_accept combines per-row maxima into zeroed keys and resets them after the walk:
+    two calls in a row on one workspace (different vocabularies and trees) are both
+    bit-exact, and the workspace is all zero after each."""
+    ws = None
+    for seed, (nb, B, V) in ((11, (3, 40, 9000)), (12, (2, 256, 151936)), (13, (5, 7, 33))):
+        rng = np.random.default_rng(seed)
+        trees = [wl.tree_best_first(rng, B, child_cap=3, max_depth=B) for _ in range(nb)]
+        w = wl.make_workload("ws-reuse", nb, B, 8, 2, 128, V, [3] * nb, trees, seed, extra_pages=1)
+        d = DevWorkload(w)
+        need = tv.accept_workspace_size(V, B, nb)
+        if ws is None:
+            ws = torch.zeros(2 * 256 * 8 * 8, dtype=torch.uint8, device="cuda")
+        assert need <= ws.numel()
+        am, n_acc, path, bonus = tv.accept(d.logits, d.draft, d.parent, None, status=d.status, workspace=ws)
+        torch.cuda.synchronize()
+        assert d.status.item() == 0
+        r_am, r_n, r_path, r_bonus = oracle.accept(w.logits, w.draft, w.parent)
+        assert np.array_equal(am.cpu().numpy(), r_am)
+        assert np.array_equal(n_acc.cpu().numpy(), r_n)
+        assert np.array_equal(path.cpu().numpy(), r_path)
+        assert np.array_equal(bonus.cpu().numpy(), r_bonus)
+        assert int(ws.count_nonzero()) == 0

@@ -184,7 +184,11 @@ def accept_workspace_size(V: int, B: int, nb: int) -> int:
 
 
 def accept(logits, draft, parent, mask, status=None, out=None, workspace=None, stream=None):
-    """tv_accept: returns (argmax [nb*B], n_acc [nb], path [nb][B], bonus [nb]) int32 tensors."""
+    """tv_accept: returns (argmax [nb*B], n_acc [nb], path [nb][B], bonus [nb]) int32 tensors.
+
+    A workspace passed in must have been zeroed once before its first use (every call
+    leaves it zeroed); without one, a zeroed workspace is allocated for this call.
+    """
     nb, B = parent.shape
     V = logits.shape[-1]
     dev = _logits_ok(logits, parent)
@@ -194,7 +198,7 @@ def accept(logits, draft, parent, mask, status=None, out=None, workspace=None, s
     am, n_acc, path, bonus = out
     need = accept_workspace_size(V, B, nb)
     if workspace is None or workspace.numel() * workspace.element_size() < need:
-        workspace = torch.empty(max(need, 8), dtype=torch.uint8, device=dev)
+        workspace = torch.zeros(max(need, 8), dtype=torch.uint8, device=dev)
     rc = lib().tv_accept(_p(logits), V, _p(draft), _p(parent), _p(mask), B, nb, _p(am), _p(n_acc), _p(path),
                          _p(bonus), _p(status), _p(workspace), workspace.numel() * workspace.element_size(),
                          _stream(stream))

@@ -6,20 +6,18 @@
 // draft token equals the target argmax at the parent; the deepest accepted
 // node wins, ties to the smallest index.
 //
-// argmax (kernel 1): the logits are cut into (row, 4096-element chunk) units,
-// one warp per unit, and a grid of at most two CTAs per SM walks them row group
-// by row group.  A lane holds 16 16-byte vectors
-// of its unit in registers (all in flight at once); bf16x2 NaN-propagating max
-// instructions reduce them (about one per two logits), the warp agrees on the
-// unit's maximum with shuffles, and only the lanes holding it look for its
-// first position.
-//
-// A CTA owns whole rows: R = max(1, 8 / chunks per row) rows at a time, whose
-// (row, chunk) units its 8 warps share out; each warp folds a unit into a 64-bit
-// order-preserving key (value rank, then the smaller index) and takes the maximum
-// into the row's shared-memory slot, and the CTA stores one key per row in the
-// caller's workspace.  Every key is written by exactly one CTA before the
-// acceptance kernel reads it, so no global atomics and no zeroing are needed.
+// argmax (kernel 1): the logits are cut into (row, 4096-element chunk) units, one
+// warp per unit.  A lane holds 16 16-byte vectors of its unit in registers (all in
+// flight at once); bf16x2 NaN-propagating max instructions reduce them (about one per
+// two logits), the warp agrees on the unit's maximum with shuffles, and only the lanes
+// holding it look for its first position.  Each unit folds into a 64-bit
+// order-preserving key (value rank, then the smaller index).  The units of all rows,
+// row-major, are cut into equal contiguous shares, one per warp of a grid of two CTAs
+// per SM, so every warp streams the same number of 8 KB units however many rows there
+// are; a warp combines its units of one row in registers and adds the result to the
+// row's key in the workspace with one 64-bit atomicMax per row it touches.  The keys
+// start at zero, below every real key, and the acceptance kernel sets each back to
+// zero once it has read it, so no memset runs between calls.
 //
 // accept (kernel 2): one CTA per sequence, one thread per node, launched as a
 // programmatic dependent of the argmax.  The tree inputs (parent, draft, the
@@ -29,7 +27,9 @@
 // ok), the best (depth, -index) key is a block max, and the path is read off
 // the chosen node's mask bits in ascending order.
 //
-// fused (tv_accept_fused, one kernel): the same argmax CTAs, and after a CTA
+// fused (tv_accept_fused, one kernel): CTAs that own whole rows (R = max(1, 8 / chunks
+// per row) at a time, whose units their 8 warps share, combined in shared memory into
+// one key per row stored with a plain store), and after a CTA
 // stores a row group's keys it adds the group's row count to a per-sequence
 // counter in the workspace; the CTA whose addition completes sequence b's B rows
 // resets the counter and runs b's acceptance walk itself (a fence orders every
@@ -40,6 +40,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "tv_device.cuh"
@@ -248,6 +249,99 @@ __device__ void fused_walk(AcceptSmem &s, int b, int B, int W, const unsigned lo
     accept_core(s, b, B, W, p, d, n_acc, path, bonus, status);
 }
 
+// One unit: logits [lo, min(lo + kArgChunk, V)) of one row, reduced by one warp to the
+// 64-bit order-preserving key of its maximum (value rank, then the smaller index); the
+// result is the same in every lane.  Each lane holds kArgVec 16-byte vectors in
+// registers (all loads in flight at once) and folds them as a tree of bf16x2 maxima,
+// keeping each vector's maximum; the warp agrees on the unit's maximum with one integer
+// max-reduction of its rank, the lanes holding it find their first position in two
+// steps (first vector whose maximum matches, then the element inside it), and one
+// integer min-reduction picks the smallest.  32-bit index arithmetic.
+__device__ __forceinline__ unsigned long long unit_key(const uint16_t *__restrict__ row, int lo, int V, int lane)
+{
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    const int hi = min(lo + kArgChunk, V);
+
+    // scalar head up to the first 16-byte boundary, 16-byte vectors, scalar tail
+    const int head = min((int)(((16u - ((uint32_t)(uintptr_t)(row + lo) & 15u)) & 15u) >> 1), hi - lo);
+    const int vstart = lo + head;
+    const int nvec = (hi - vstart) >> 3;
+    const int tail = vstart + nvec * 8;
+    const uint4 *vp = reinterpret_cast<const uint4 *>(row + vstart);
+    uint4 v[kArgVec];
+    if (nvec > 0) {
+#pragma unroll
+        for (int k = 0; k < kArgVec; ++k) v[k] = ld_stream_v4(vp + min(lane + k * 32, nvec - 1));
+        // dependency points: every load is issued before any of them is used
+        asm volatile("" : "+r"(v[0].x), "+r"(v[0].y), "+r"(v[0].z), "+r"(v[0].w), "+r"(v[1].x), "+r"(v[1].y),
+                     "+r"(v[1].z), "+r"(v[1].w), "+r"(v[2].x), "+r"(v[2].y), "+r"(v[2].z), "+r"(v[2].w),
+                     "+r"(v[3].x), "+r"(v[3].y), "+r"(v[3].z), "+r"(v[3].w), "+r"(v[4].x), "+r"(v[4].y),
+                     "+r"(v[4].z), "+r"(v[4].w), "+r"(v[5].x), "+r"(v[5].y), "+r"(v[5].z), "+r"(v[5].w),
+                     "+r"(v[6].x), "+r"(v[6].y), "+r"(v[6].z), "+r"(v[6].w), "+r"(v[7].x), "+r"(v[7].y),
+                     "+r"(v[7].z), "+r"(v[7].w));
+        asm volatile("" : "+r"(v[8].x), "+r"(v[8].y), "+r"(v[8].z), "+r"(v[8].w), "+r"(v[9].x), "+r"(v[9].y),
+                     "+r"(v[9].z), "+r"(v[9].w), "+r"(v[10].x), "+r"(v[10].y), "+r"(v[10].z), "+r"(v[10].w),
+                     "+r"(v[11].x), "+r"(v[11].y), "+r"(v[11].z), "+r"(v[11].w), "+r"(v[12].x), "+r"(v[12].y),
+                     "+r"(v[12].z), "+r"(v[12].w), "+r"(v[13].x), "+r"(v[13].y), "+r"(v[13].z), "+r"(v[13].w),
+                     "+r"(v[14].x), "+r"(v[14].y), "+r"(v[14].z), "+r"(v[14].w), "+r"(v[15].x), "+r"(v[15].y),
+                     "+r"(v[15].z), "+r"(v[15].w));
+    }
+    const bool has_head = lane < head, has_tail = lane < hi - tail;
+    const float xh = has_head ? bf16_bits_to_float(row[lo + lane]) : NEG_INF;
+    const float xt = has_tail ? bf16_bits_to_float(row[tail + lane]) : NEG_INF;
+
+    // lane maximum: a bf16x2 tree over the vectors (clamped duplicates of the last
+    // vector do not change it); the vector maxima stay for the search
+    __nv_bfloat162 vm[kArgVec];
+#pragma unroll
+    for (int k = 0; k < kArgVec; ++k) vm[k] = vec_max2(v[k]);
+    __nv_bfloat162 t[kArgVec / 2];
+#pragma unroll
+    for (int k = 0; k < kArgVec / 2; ++k) t[k] = __hmax2_nan(vm[2 * k], vm[2 * k + 1]);
+#pragma unroll
+    for (int w = kArgVec / 4; w > 0; w >>= 1)
+#pragma unroll
+        for (int k = 0; k < w; ++k) t[k] = __hmax2_nan(t[2 * k], t[2 * k + 1]);
+    const float vmax = nvec > 0 ? __bfloat162float(__hmax_nan(t[0].x, t[0].y)) : NEG_INF;
+    const float tm = max_nan(max_nan(vmax, xh), xt);
+    const uint32_t r = value_rank(tm);
+    const uint32_t wr = __reduce_max_sync(0xffffffffu, r);
+
+    // first position of the unit maximum in this lane (index order: head, vectors, tail)
+    uint32_t idx = 0x7fffffffu;
+    if (r == wr) {
+        const bool nan = tm != tm;
+        if (has_head && (nan ? (xh != xh) : (xh == tm))) {
+            idx = lo + lane;
+        } else {
+            int kf = -1;
+#pragma unroll
+            for (int k = kArgVec - 1; k >= 0; --k) {
+                const float x = __bfloat162float(__hmax_nan(vm[k].x, vm[k].y));
+                if (lane + k * 32 < nvec && (nan ? (x != x) : (x == tm))) kf = k;
+            }
+            if (kf >= 0) {
+                uint4 w = v[0];
+#pragma unroll
+                for (int k = 1; k < kArgVec; ++k)
+                    if (k == kf) w = v[k];
+                const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+                int e_first = 7;
+#pragma unroll
+                for (int e = 7; e >= 0; --e) {
+                    const float x = bf16_bits_to_float((w4[e >> 1] >> ((e & 1) * 16)) & 0xFFFFu);
+                    if (nan ? (x != x) : (x == tm)) e_first = e;
+                }
+                idx = vstart + (lane + kf * 32) * 8 + e_first;
+            } else if (has_tail) {
+                idx = tail + lane;
+            }
+        }
+    }
+    idx = __reduce_min_sync(0xffffffffu, idx);
+    return ((unsigned long long)wr << 32) | (0xFFFFFFFFu - idx);
+}
+
 // One unit = kArgChunk logits of one row = one warp: each lane holds kArgVec
 // 16-byte vectors in registers (all loads in flight at once) and folds them as
 // a tree of bf16x2 maxima, keeping each vector's maximum; the warp agrees on the
@@ -274,7 +368,6 @@ __global__ void __launch_bounds__(kArgThreads) argmax_rows_kernel(const uint16_t
     static_assert(kArgChunk == 32 * kArgVec * 8, "one warp per unit");
     static_assert(kArgVec == 16, "the dependency points below list 16 vectors");
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const float NEG_INF = -__int_as_float(0x7f800000);
     pdl_wait_primary();  // the logits may come from the previous kernel in the stream
     pdl_launch_dependents();
     if constexpr (kFused) {
@@ -302,87 +395,8 @@ __global__ void __launch_bounds__(kArgThreads) argmax_rows_kernel(const uint16_t
         const int lr = u / nchunk;
         const int row_id = r0 + lr;
         const int lo = (u - lr * nchunk) * kArgChunk;
-        const int hi = min(lo + kArgChunk, V);
-        const uint16_t *row = logits + (size_t)row_id * V;
-
-        // scalar head up to the first 16-byte boundary, 16-byte vectors, scalar tail
-        const int head = min((int)(((16u - ((uint32_t)(uintptr_t)(row + lo) & 15u)) & 15u) >> 1), hi - lo);
-        const int vstart = lo + head;
-        const int nvec = (hi - vstart) >> 3;
-        const int tail = vstart + nvec * 8;
-        const uint4 *vp = reinterpret_cast<const uint4 *>(row + vstart);
-        uint4 v[kArgVec];
-        if (nvec > 0) {
-#pragma unroll
-            for (int k = 0; k < kArgVec; ++k) v[k] = ld_stream_v4(vp + min(lane + k * 32, nvec - 1));
-            // dependency points: every load is issued before any of them is used
-            asm volatile("" : "+r"(v[0].x), "+r"(v[0].y), "+r"(v[0].z), "+r"(v[0].w), "+r"(v[1].x), "+r"(v[1].y),
-                         "+r"(v[1].z), "+r"(v[1].w), "+r"(v[2].x), "+r"(v[2].y), "+r"(v[2].z), "+r"(v[2].w),
-                         "+r"(v[3].x), "+r"(v[3].y), "+r"(v[3].z), "+r"(v[3].w), "+r"(v[4].x), "+r"(v[4].y),
-                         "+r"(v[4].z), "+r"(v[4].w), "+r"(v[5].x), "+r"(v[5].y), "+r"(v[5].z), "+r"(v[5].w),
-                         "+r"(v[6].x), "+r"(v[6].y), "+r"(v[6].z), "+r"(v[6].w), "+r"(v[7].x), "+r"(v[7].y),
-                         "+r"(v[7].z), "+r"(v[7].w));
-            asm volatile("" : "+r"(v[8].x), "+r"(v[8].y), "+r"(v[8].z), "+r"(v[8].w), "+r"(v[9].x), "+r"(v[9].y),
-                         "+r"(v[9].z), "+r"(v[9].w), "+r"(v[10].x), "+r"(v[10].y), "+r"(v[10].z), "+r"(v[10].w),
-                         "+r"(v[11].x), "+r"(v[11].y), "+r"(v[11].z), "+r"(v[11].w), "+r"(v[12].x), "+r"(v[12].y),
-                         "+r"(v[12].z), "+r"(v[12].w), "+r"(v[13].x), "+r"(v[13].y), "+r"(v[13].z), "+r"(v[13].w),
-                         "+r"(v[14].x), "+r"(v[14].y), "+r"(v[14].z), "+r"(v[14].w), "+r"(v[15].x), "+r"(v[15].y),
-                         "+r"(v[15].z), "+r"(v[15].w));
-        }
-        const bool has_head = lane < head, has_tail = lane < hi - tail;
-        const float xh = has_head ? bf16_bits_to_float(row[lo + lane]) : NEG_INF;
-        const float xt = has_tail ? bf16_bits_to_float(row[tail + lane]) : NEG_INF;
-
-        // lane maximum: a bf16x2 tree over the vectors (clamped duplicates of the last
-        // vector do not change it); the vector maxima stay for the search
-        __nv_bfloat162 vm[kArgVec];
-#pragma unroll
-        for (int k = 0; k < kArgVec; ++k) vm[k] = vec_max2(v[k]);
-        __nv_bfloat162 t[kArgVec / 2];
-#pragma unroll
-        for (int k = 0; k < kArgVec / 2; ++k) t[k] = __hmax2_nan(vm[2 * k], vm[2 * k + 1]);
-#pragma unroll
-        for (int w = kArgVec / 4; w > 0; w >>= 1)
-#pragma unroll
-            for (int k = 0; k < w; ++k) t[k] = __hmax2_nan(t[2 * k], t[2 * k + 1]);
-        const float vmax = nvec > 0 ? __bfloat162float(__hmax_nan(t[0].x, t[0].y)) : NEG_INF;
-        const float tm = max_nan(max_nan(vmax, xh), xt);
-        const uint32_t r = value_rank(tm);
-        const uint32_t wr = __reduce_max_sync(0xffffffffu, r);
-
-        // first position of the unit maximum in this lane (index order: head, vectors, tail)
-        uint32_t idx = 0x7fffffffu;
-        if (r == wr) {
-            const bool nan = tm != tm;
-            if (has_head && (nan ? (xh != xh) : (xh == tm))) {
-                idx = lo + lane;
-            } else {
-                int kf = -1;
-#pragma unroll
-                for (int k = kArgVec - 1; k >= 0; --k) {
-                    const float x = __bfloat162float(__hmax_nan(vm[k].x, vm[k].y));
-                    if (lane + k * 32 < nvec && (nan ? (x != x) : (x == tm))) kf = k;
-                }
-                if (kf >= 0) {
-                    uint4 w = v[0];
-#pragma unroll
-                    for (int k = 1; k < kArgVec; ++k)
-                        if (k == kf) w = v[k];
-                    const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
-                    int e_first = 7;
-#pragma unroll
-                    for (int e = 7; e >= 0; --e) {
-                        const float x = bf16_bits_to_float((w4[e >> 1] >> ((e & 1) * 16)) & 0xFFFFu);
-                        if (nan ? (x != x) : (x == tm)) e_first = e;
-                    }
-                    idx = vstart + (lane + kf * 32) * 8 + e_first;
-                } else if (has_tail) {
-                    idx = tail + lane;
-                }
-            }
-        }
-        idx = __reduce_min_sync(0xffffffffu, idx);
-        if (lane == 0) atomicMax(&s_key[lr], ((unsigned long long)wr << 32) | (0xFFFFFFFFu - idx));
+        const unsigned long long key = unit_key(logits + (size_t)row_id * V, lo, V, lane);
+        if (lane == 0) atomicMax(&s_key[lr], key);
       }
       __syncthreads();
       if (threadIdx.x < nr) best[r0 + threadIdx.x] = s_key[threadIdx.x];
@@ -414,7 +428,39 @@ __global__ void __launch_bounds__(kArgThreads) argmax_rows_kernel(const uint16_t
     }
 }
 
-__global__ void __launch_bounds__(kMaxB) accept_kernel(const unsigned long long *__restrict__ best,
+// tv_accept's argmax: the (row, chunk) units of all rows, row-major, are cut into equal
+// contiguous shares, one per warp of the grid, so every warp streams the same number
+// of 8 KB units whatever the row count (no tail of SMs holding an extra row).  A warp
+// folds the units of one row into a register key and adds it to the row's key with one
+// 64-bit atomicMax when it moves to the next row or ends; the keys start at zero (below
+// every real key) and the acceptance kernel sets them back to zero after reading them.
+__global__ void __launch_bounds__(kArgThreads) argmax_span_kernel(const uint16_t *__restrict__ logits, int V,
+                                                                  int nchunk, long long units,
+                                                                  unsigned long long *__restrict__ keys)
+{
+    const int lane = threadIdx.x & 31;
+    const long long W = (long long)gridDim.x * (kArgThreads / 32);
+    const long long w = (long long)blockIdx.x * (kArgThreads / 32) + (threadIdx.x >> 5);
+    pdl_wait_primary();  // the logits may come from the previous kernel in the stream
+    pdl_launch_dependents();
+    const long long u0 = units * w / W, u1 = units * (w + 1) / W;
+    int row = -1;
+    unsigned long long best = 0ull;
+    for (long long u = u0; u < u1; ++u) {
+        const int r = (int)(u / nchunk);
+        const int c = (int)(u - (long long)r * nchunk);
+        if (r != row) {
+            if (row >= 0 && lane == 0) atomicMax(keys + row, best);
+            row = r;
+            best = 0ull;
+        }
+        const unsigned long long k = unit_key(logits + (size_t)r * V, c * kArgChunk, V, lane);
+        best = k > best ? k : best;
+    }
+    if (row >= 0 && lane == 0) atomicMax(keys + row, best);
+}
+
+__global__ void __launch_bounds__(kMaxB) accept_kernel(unsigned long long *__restrict__ best,
                                                        const int32_t *__restrict__ draft,
                                                        const int32_t *__restrict__ parent,
                                                        const uint32_t *__restrict__ mask, int B, int W,
@@ -453,9 +499,11 @@ __global__ void __launch_bounds__(kMaxB) accept_kernel(const unsigned long long 
     if (!mask && !bad_tree) accept_rows_from_parents(s, B, W);
     pdl_wait_primary();  // the argmax keys are complete from here on
 
-    // every row's argmax is the low half of its key: 0xFFFFFFFF - index
+    // every row's argmax is the low half of its key: 0xFFFFFFFF - index; the key goes back
+    // to zero for the next call (the argmax combines into zeroed keys)
     if (i < B) {
         const unsigned long long top = __ldcg(best + (size_t)b * B + i);
+        best[(size_t)b * B + i] = 0ull;
         const int a = (int)(0xFFFFFFFFu - (uint32_t)top);
         s.am[i] = a;
         am[(size_t)b * B + i] = a;
@@ -479,22 +527,19 @@ cudaError_t launch_accept(const uint16_t *logits, int V, const int32_t *draft, c
                           int32_t *bonus, int32_t *status, void *workspace, int num_sms, cudaStream_t stream)
 {
     const int nchunk = (V + kArgChunk - 1) / kArgChunk;
-    const int rows = nb * B;
-    const int wpc = kArgThreads / 32;
-    const int R = nchunk >= wpc ? 1 : wpc / nchunk;  // rows per CTA group
+    const long long units = (long long)nb * B * nchunk;
     long long grid = (long long)num_sms * kArgCtasPerSm;
-    const long long need = ((long long)rows + R - 1) / R;
+    const long long need = (units + kArgThreads / 32 - 1) / (kArgThreads / 32);  // at least one unit per warp
     if (grid > need) grid = need;
     if (grid < 1) grid = 1;
     unsigned long long *best = static_cast<unsigned long long *>(workspace);
-    cudaError_t e = launch_dependent(argmax_rows_kernel<false>, dim3((unsigned)grid), dim3(kArgThreads), 0, stream,
-                                     logits, V, nchunk, R, rows, best, FusedAccept{});
+    cudaError_t e = launch_dependent(argmax_span_kernel, dim3((unsigned)grid), dim3(kArgThreads), 0, stream, logits, V,
+                                     nchunk, units, best);
     if (e != cudaSuccess) return e;
     const int W = (B + 31) / 32;
     // its launch overlaps the argmax tail; it waits before reading the keys
-    return launch_dependent(accept_kernel, dim3((unsigned)nb), dim3(kMaxB), 0, stream,
-                            (const unsigned long long *)best, draft, parent, mask, B, W, am, n_acc, path, bonus,
-                            status);
+    return launch_dependent(accept_kernel, dim3((unsigned)nb), dim3(kMaxB), 0, stream, best, draft, parent, mask, B, W,
+                            am, n_acc, path, bonus, status);
 }
 
 size_t accept_fused_workspace_bytes(int V, int B, int nb)
@@ -594,15 +639,36 @@ static cudaError_t noalloc_keys_address(void **out)
     return cudaSuccess;
 }
 
+// Sets every key of the allocation-free scratch back to zero (used only after a call
+// whose acceptance kernel failed to launch left keys behind).
+__global__ void zero_noalloc_keys_kernel()
+{
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < TV_ACCEPT_NOALLOC_MAX_ROWS; i += gridDim.x * blockDim.x)
+        g_noalloc_keys[i] = 0ull;
+}
+
 cudaError_t launch_accept_noalloc(const uint16_t *logits, int V, const int32_t *draft, const int32_t *parent,
                                   const uint32_t *mask, int B, int nb, int32_t *am, int32_t *n_acc, int32_t *path,
                                   int32_t *bonus, int32_t *status, int num_sms, cudaStream_t stream)
 {
+    static std::atomic<uint64_t> dirty{0};  // per device: a failed call may have left keys non-zero
     void *keys = nullptr;
-    const cudaError_t e = noalloc_keys_address(&keys);
+    cudaError_t e = noalloc_keys_address(&keys);
     if (e != cudaSuccess) return e;
-    // the same kernels as tv_accept; every key a call reads is written by that call first
-    return launch_accept(logits, V, draft, parent, mask, B, nb, am, n_acc, path, bonus, status, keys, num_sms, stream);
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+    if (dirty.load() & bit) {
+        zero_noalloc_keys_kernel<<<(TV_ACCEPT_NOALLOC_MAX_ROWS + 255) / 256, 256, 0, stream>>>();
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        dirty.fetch_and(~bit);
+    }
+    // the same kernels as tv_accept, on keys that start (and are left) at zero
+    e = launch_accept(logits, V, draft, parent, mask, B, nb, am, n_acc, path, bonus, status, keys, num_sms, stream);
+    if (e != cudaSuccess) dirty.fetch_or(bit);
+    return e;
 }
 
 }  // namespace tv

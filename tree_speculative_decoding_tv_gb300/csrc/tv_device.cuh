@@ -69,6 +69,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return done != 0;
 }
 
+// try_wait that lets the hardware suspend the thread for up to `hint_ns` while the
+// phase is incomplete (it resumes as soon as the phase completes), so a waiting warp
+// does not spin and take issue slots from the warps it shares a sub-partition with.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0;
+}
+
+// Suspend hint of the bounded waits: far below the limit, so the abort flag and the
+// time limit are still checked often.
+constexpr uint32_t kSuspendHintNs = 20000;
+
 // Wait for the phase of parity `parity` to complete.  Returns false when the
 // CTA-wide abort flag is raised or the wait runs past `limit_ns` (the flag is
 // then raised and TV_ERR_TIMEOUT reported).
@@ -78,8 +98,8 @@ __device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, vol
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 31) == 0) {
+        if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
+        if ((it & 3) == 0) {
             if (*abort_flag) return false;
             if (global_timer_ns() - t0 > limit_ns) {
                 *abort_flag = 1;
