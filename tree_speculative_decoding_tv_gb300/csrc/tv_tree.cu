@@ -9,20 +9,18 @@
 // for every node at depth d-1; a candidate child (u, c) scores score[u] +
 // logp[d][c] in fp32; ties go to the smaller parent index, then the smaller rank.
 //
-// GPU form: one warp per sequence.  Because each depth's log-probs are sorted,
-// a node's best remaining candidate is always its next rank, so the frontier
-// holds one entry per node (its next child) instead of all K: at most B entries,
-// kept in registers (9 slots per lane).  Each lane keeps the best of its own
-// slots; a pop is a warp max of the order-preserving score followed by a warp min
-// of (parent, rank) among the lanes holding it (two single-instruction
-// reductions), and only the lane owning a changed slot looks again.  The popped
-// entry's sibling successor joins the frontier at once (it was a candidate when
-// the round began); the round's new nodes add their first children only when the
-// round ends, which is what expanding the w nodes together means.  Each slot keeps
-// its parent's score and its depth in registers, and each lane prepares its best
-// slot's successor before the reductions; a lane's best is a 64-bit max over its
-// slots (a tournament after a pop, one comparison after an insertion), so a pop's
-// dependent chain is the two reductions, a shuffle and a few register operations.
+// GPU form: one CTA of 256 threads per sequence, thread j owning node j's frontier
+// slot.  Because each depth's log-probs are sorted, a node's best remaining
+// candidate is always its next rank, so the frontier holds one entry per node (B at
+// most) and a node's slot simply moves to the next rank when it is popped.  Every
+// slot's order is one 64-bit key, (order-preserving score << 32) | ~((parent << 16) |
+// rank), 0 when empty, so a pop is a block-wide maximum: a warp reduction, one
+// barrier (the warp maxima are double-buffered in shared memory, so no second barrier
+// is needed), and every thread folding the 8 warp maxima itself.  After a pop only two
+// threads act: the owner of the popped slot swaps in its next rank's key (computed
+// ahead, off the critical path) and the new node's thread adds its first child, at
+// once for w = 1 and when the round ends for w > 1.  The score comes back exactly
+// from the winning key, so no other broadcast is needed.
 #include <cuda_runtime.h>
 
 #include "tv_device.cuh"
@@ -31,26 +29,40 @@
 namespace tv {
 
 constexpr int kTreeMaxB = 256;
-constexpr int kTreeSlots = 9;  // frontier slots per lane: 9 x 32 >= kTreeMaxB
+constexpr int kTreeThreads = 256;  // one frontier slot (node) per thread
+constexpr int kTreeWarps = kTreeThreads / 32;
 
-// Order-preserving image of a finite score (larger score -> larger value, never 0).
+// Order-preserving image of a finite score (larger score -> larger value, never 0), and back.
 __device__ __forceinline__ uint32_t score_key(float s)
 {
     const uint32_t b = __float_as_uint(s);
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
+__device__ __forceinline__ float key_score(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// A slot's order: larger score first, then smaller (parent, rank); 0 = empty.
+__device__ __forceinline__ unsigned long long slot_order(float f, int parent, int rank)
+{
+    return ((unsigned long long)score_key(f) << 32) | (uint32_t)(~(((uint32_t)parent << 16) | (uint32_t)rank));
+}
 
 constexpr int kTreeSmemLp = 8192;  // log-prob tables up to this size are staged in shared memory
 
-__global__ void __launch_bounds__(32) build_tree_kernel(const float *__restrict__ logp, const int32_t *__restrict__ tok,
-                                                        int Dmax, int K, int B, int w, int32_t *__restrict__ parent,
-                                                        int32_t *__restrict__ token, float *__restrict__ score,
-                                                        int32_t *status)
+__global__ void __launch_bounds__(kTreeThreads) build_tree_kernel(const float *__restrict__ logp,
+                                                                  const int32_t *__restrict__ tok, int Dmax, int K,
+                                                                  int B, int w, int32_t *__restrict__ parent,
+                                                                  int32_t *__restrict__ token,
+                                                                  float *__restrict__ score, int32_t *status)
 {
     __shared__ float sc[kTreeMaxB];
     __shared__ int16_t dep[kTreeMaxB], par[kTreeMaxB], rank[kTreeMaxB];
     __shared__ float s_lp[kTreeSmemLp];
-    const int b = blockIdx.x, lane = threadIdx.x;
+    __shared__ unsigned long long s_best[2][kTreeWarps];
+    __shared__ int s_bad;
+    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const float *g_lp = logp + (size_t)b * Dmax * K;
     const int32_t *tk = tok + (size_t)b * Dmax * K;
 
@@ -58,218 +70,101 @@ __global__ void __launch_bounds__(32) build_tree_kernel(const float *__restrict_
     pdl_launch_dependents();
     // each depth's log-probs finite and sorted best first; small tables go to shared memory
     const bool staged = Dmax * K <= kTreeSmemLp;
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
     bool bad = false;
-    for (int t = lane; t < Dmax * K; t += 32) {
+    for (int t = tid; t < Dmax * K; t += kTreeThreads) {
         const float x = g_lp[t];
         if (!(fabsf(x) <= 3.0e38f)) bad = true;
         if (t % K + 1 < K && !(x >= g_lp[t + 1])) bad = true;
         if (staged) s_lp[t] = x;
     }
-    if (__any_sync(0xffffffffu, bad)) {
-        if (lane == 0) report_status(status, TV_ERR_INVALID_ARG);
+    if (bad) s_bad = 1;
+    __syncthreads();
+    if (s_bad) {
+        if (tid == 0) report_status(status, TV_ERR_INVALID_ARG);
         return;
     }
     const float *lp = staged ? s_lp : g_lp;
 
-    // The frontier lives in registers: slot j is register q = j / 32 of lane j % 32.
-    // rt = (parent << 16) | rank, or kEmpty; rf = the candidate's score; rp = its
-    // parent's score; rd = its depth.  Slots are never compacted: a parent whose
-    // ranks run out leaves an empty slot behind.
-    constexpr uint32_t kEmpty = 0xFFFFFFFFu;
-    float rf[kTreeSlots], rp[kTreeSlots];
-    uint32_t rt[kTreeSlots];
-    int rd[kTreeSlots];
-#pragma unroll
-    for (int q = 0; q < kTreeSlots; ++q) {
-        rf[q] = rp[q] = 0.f;
-        rt[q] = kEmpty;
-        rd[q] = 0;
-    }
-    // this lane's best slot (score key, tie-break, score, depth) and, ready before the
-    // pop that may take it, that slot's replacement: the parent's next rank.  A slot's
-    // order is one 64-bit value, (score key << 32) | ~tie-break (0 for an empty slot),
-    // so the best is a max over the slots.
-    uint32_t my_s = 0, my_t = kEmpty, rep_t = kEmpty;
-    float my_f = 0.f, my_p = 0.f, rep_f = 0.f;
-    int my_d = 0;
-    auto order = [&](float f, uint32_t t) -> uint64_t {
-        return t == kEmpty ? 0ull : (((uint64_t)score_key(f) << 32) | (uint64_t)(~t));
+    // Thread j's slot is node j's next child.  key: its order now; nxt: the order of the
+    // rank after it (ready before the pop that may take this one); my_f, my_d: node j's
+    // score and depth; my_c: the rank the slot holds.
+    unsigned long long key = 0ull, nxt = 0ull;
+    float my_f = 0.f;
+    int my_d = 0, my_c = 0;
+    auto prepare_next = [&]() {  // the order of rank my_c + 1, or empty
+        nxt = (my_c + 1 < K) ? slot_order(my_f + lp[(size_t)my_d * K + my_c + 1], tid, my_c + 1) : 0ull;
     };
-    auto prepare = [&]() {  // the replacement of the best slot
-        const int c = (int)(my_t & 0xFFFFu);
-        if (my_t != kEmpty && c + 1 < K) {
-            rep_f = my_p + lp[(size_t)(my_d - 1) * K + c + 1];
-            rep_t = my_t + 1u;
+    auto open_slot = [&]() {  // node tid (score my_f, depth my_d) offers its first child
+        my_c = 0;
+        if (my_d < Dmax) {
+            key = slot_order(my_f + lp[(size_t)my_d * K], tid, 0);
+            prepare_next();
         } else {
-            rep_t = kEmpty;
+            key = 0ull;
         }
     };
-    auto lane_best = [&]() {  // full rescan: a tournament over the slots
-        uint64_t o[kTreeSlots];
-#pragma unroll
-        for (int q = 0; q < kTreeSlots; ++q) o[q] = order(rf[q], rt[q]);
-#pragma unroll
-        for (int step = 1; step < kTreeSlots; step <<= 1)
-#pragma unroll
-            for (int q = 0; q + step < kTreeSlots; q += 2 * step) o[q] = o[q] > o[q + step] ? o[q] : o[q + step];
-        my_s = (uint32_t)(o[0] >> 32);
-        my_t = ~(uint32_t)o[0];
-        if (o[0] == 0ull) my_t = kEmpty;
-#pragma unroll
-        for (int q = 0; q < kTreeSlots; ++q)
-            if (rt[q] == my_t && my_t != kEmpty) {
-                my_f = rf[q];
-                my_p = rp[q];
-                my_d = rd[q];
-            }
-        prepare();
-    };
-    // slot j <- a candidate (score f, tie-break t) with parent score ps at depth d, by its
-    // owner lane; the lane's best changes only if the newcomer beats it
-    auto put = [&](int j, float f, uint32_t t, float ps, int d) {
-        if ((j & 31) == lane) {
-            const int qj = j >> 5;
-#pragma unroll
-            for (int q = 0; q < kTreeSlots; ++q)
-                if (q == qj) {
-                    rf[q] = f;
-                    rt[q] = t;
-                    rp[q] = ps;
-                    rd[q] = d;
-                }
-            if (order(f, t) > order(my_f, my_t)) {
-                my_s = score_key(f);
-                my_t = t;
-                my_f = f;
-                my_p = ps;
-                my_d = d;
-                prepare();
-            }
-        }
-    };
-
-    if (lane == 0) {
+    if (tid == 0) {
         sc[0] = 0.f;
         dep[0] = 0;
         par[0] = -1;
         rank[0] = 0;
+        my_f = 0.f;
+        my_d = 0;
+        open_slot();
     }
-    int n = 1, made = 1;  // slots used, nodes made (warp-uniform)
-    put(0, 0.f + lp[0], 0u, 0.f, 1);
-    __syncwarp();
-    float last_f = 0.f;  // the last popped node's score and depth (the w = 1 round's only node)
-    int last_d = 0;
-    // w = 1: every round is one pop, after which the popped node's first child joins.  Both
-    // frontier updates (the popped slot's replacement by its owner lane, the child's slot by
-    // its lane) go in one pass; a lane doing both rescans once, over the same slots the two
-    // steps would compare.  A top score that one lane alone holds needs no second reduction.
-    while (w == 1 && made < B) {
-        const uint32_t top_s = __reduce_max_sync(0xffffffffu, my_s);
-        if (top_s == 0) break;  // no candidate left: B exceeds the tree
-        const unsigned hold = __ballot_sync(0xffffffffu, my_s == top_s);
-        int owner;
-        uint32_t top_t;
-        if (__popc(hold) == 1) {
-            owner = __ffs(hold) - 1;
-            top_t = __shfl_sync(0xffffffffu, my_t, owner);
-        } else {
-            top_t = __reduce_min_sync(0xffffffffu, my_s == top_s ? my_t : kEmpty);
-            owner = __ffs(__ballot_sync(0xffffffffu, my_s == top_s && my_t == top_t)) - 1;
-        }
-        const float f = __shfl_sync(0xffffffffu, my_f, owner);
-        const int d = __shfl_sync(0xffffffffu, my_d, owner);
-        const int i = made;
-        if (lane == 0) {
-            par[i] = (int16_t)(top_t >> 16);
-            dep[i] = (int16_t)d;
-            rank[i] = (int16_t)(top_t & 0xFFFFu);
-            sc[i] = f;
-        }
-        const bool child = d < Dmax;  // node i's first child: slot n, parent score f, depth d + 1
-        const float cf = child ? f + lp[(size_t)d * K] : 0.f;
-        const uint32_t ct = (uint32_t)i << 16;
-        const bool ins = child && (n & 31) == lane, own = lane == owner;
-        if (own) {
-#pragma unroll
-            for (int q = 0; q < kTreeSlots; ++q)
-                if (rt[q] == top_t) {
-                    rf[q] = rep_f;
-                    rt[q] = rep_t;
-                }
-        }
-        if (ins) {
-            const int qn = n >> 5;
-#pragma unroll
-            for (int q = 0; q < kTreeSlots; ++q)
-                if (q == qn) {
-                    rf[q] = cf;
-                    rt[q] = ct;
-                    rp[q] = f;
-                    rd[q] = d + 1;
-                }
-        }
-        if (own) {
-            lane_best();
-        } else if (ins && order(cf, ct) > order(my_f, my_t)) {
-            my_s = score_key(cf);
-            my_t = ct;
-            my_f = cf;
-            my_p = f;
-            my_d = d + 1;
-            prepare();
-        }
-        if (child) ++n;
-        ++made;
-        __syncwarp();
-    }
-    while (w != 1 && made < B) {
+    int made = 1, buf = 0;
+    bool pending = false;  // this thread's node was made in the current round
+    // A round takes up to w candidates (the popped slot moves to its next rank at once:
+    // that sibling was a candidate when the round began), then the round's nodes offer
+    // their first children; w = 1 is plain best-first expansion.
+    while (made < B) {
         const int take = min(w, B - made);
-        const int first = made;
-        for (int t = 0; t < take; ++t) {
-            // the best entry: largest score key, then smallest (parent, rank)
-            const uint32_t top_s = __reduce_max_sync(0xffffffffu, my_s);
-            if (top_s == 0) break;  // no candidate left this round
-            const uint32_t top_t = __reduce_min_sync(0xffffffffu, my_s == top_s ? my_t : kEmpty);
-            const int owner = __ffs(__ballot_sync(0xffffffffu, my_s == top_s && my_t == top_t)) - 1;
-            const float f = __shfl_sync(0xffffffffu, my_f, owner);
-            const int d = __shfl_sync(0xffffffffu, my_d, owner);
-            const int u = (int)(top_t >> 16), c = (int)(top_t & 0xFFFFu), i = made;
-            if (lane == 0) {
-                par[i] = (int16_t)u;
-                dep[i] = (int16_t)d;
-                rank[i] = (int16_t)c;
-                sc[i] = f;
-            }
-            // the parent's next rank (computed ahead) takes the popped slot, or the slot empties
-            if (lane == owner) {
+        int got = 0;
+        for (; got < take; ++got) {
+            // block-wide maximum of the slot keys (warp maximum, then the 8 warp maxima)
+            const uint32_t hi = (uint32_t)(key >> 32);
+            const uint32_t whi = __reduce_max_sync(0xffffffffu, hi);
+            const uint32_t wlo = __reduce_max_sync(0xffffffffu, hi == whi ? (uint32_t)key : 0u);
+            if (lane == 0) s_best[buf][wid] = ((unsigned long long)whi << 32) | wlo;
+            __syncthreads();
+            unsigned long long top = s_best[buf][0];
 #pragma unroll
-                for (int q = 0; q < kTreeSlots; ++q)
-                    if (rt[q] == top_t) {
-                        rf[q] = rep_f;
-                        rt[q] = rep_t;
-                    }
-                lane_best();
+            for (int k = 1; k < kTreeWarps; ++k) {
+                const unsigned long long v = s_best[buf][k];
+                top = v > top ? v : top;
             }
-            last_f = f;
-            last_d = d;
-            ++made;
-            __syncwarp();
-        }
-        // the round's nodes join with their first child
-        for (int i = first; i < made; ++i) {
-            const bool lastn = i == made - 1;
-            const float fi = lastn ? last_f : sc[i];
-            const int di = lastn ? last_d : dep[i];
-            if (di < Dmax) {
-                put(n, fi + lp[(size_t)di * K], (uint32_t)i << 16, fi, di + 1);
-                ++n;
+            buf ^= 1;
+            if (top == 0ull) break;  // no candidate left this round
+            const uint32_t t = ~(uint32_t)top;
+            const int u = (int)(t >> 16), c = (int)(t & 0xFFFFu), i = made + got;
+            const float f = key_score((uint32_t)(top >> 32));
+            if (tid == u) {  // node i = (u, rank c); u's slot moves on to rank c + 1
+                sc[i] = f;
+                dep[i] = (int16_t)(my_d + 1);
+                par[i] = (int16_t)u;
+                rank[i] = (int16_t)c;
+                key = nxt;
+                my_c = c + 1;
+                if (key != 0ull) prepare_next();
+            }
+            if (tid == i) {  // the new node: its children wait for the end of the round
+                my_f = f;
+                my_d = dep[u] + 1;
+                pending = true;
             }
         }
-        __syncwarp();
-        if (made == first) break;  // the round found no candidate at all: B exceeds the tree
+        made += got;
+        if (pending) {
+            open_slot();
+            pending = false;
+        }
+        if (got == 0) break;  // the round found no candidate at all: B exceeds the tree
     }
-    if (made < B && lane == 0) report_status(status, TV_ERR_INVALID_ARG);
-    for (int i = lane; i < B; i += 32) {
+    __syncthreads();
+    if (made < B && tid == 0) report_status(status, TV_ERR_INVALID_ARG);
+    for (int i = tid; i < B; i += kTreeThreads) {
         const bool ok = i < made;
         parent[(size_t)b * B + i] = ok ? par[i] : -1;
         token[(size_t)b * B + i] = (ok && i > 0) ? tk[(size_t)(dep[i] - 1) * K + rank[i]] : -1;
@@ -280,8 +175,8 @@ __global__ void __launch_bounds__(32) build_tree_kernel(const float *__restrict_
 cudaError_t launch_build_tree(const float *logp, const int32_t *tok, int nb, int Dmax, int K, int B, int w,
                               int32_t *parent, int32_t *token, float *score, int32_t *status, cudaStream_t stream)
 {
-    return launch_dependent(build_tree_kernel, dim3((unsigned)nb), dim3(32), 0, stream, logp, tok, Dmax, K, B, w,
-                            parent, token, score, status);
+    return launch_dependent(build_tree_kernel, dim3((unsigned)nb), dim3(kTreeThreads), 0, stream, logp, tok, Dmax, K,
+                            B, w, parent, token, score, status);
 }
 
 }  // namespace tv
