@@ -151,7 +151,10 @@ typedef struct tv_attn_args {
 TV_API size_t tv_attn_workspace_size(const tv_attn_args *args);
 
 /* Enqueue the attention: two kernel launches on `stream`, the attention and a
- * merge of split-KV pieces.  workspace_d: device buffer of at least
+ * merge of split-KV pieces; a small launch (every (sequence, kv head) unit fits
+ * the CTA count at once and the block table covers at most 8 KV tiles of 128
+ * keys per sequence) gives each unit its own CTAs, cuts no tile and launches
+ * the attention alone.  workspace_d: device buffer of at least
  * tv_attn_workspace_size(args) bytes, 16-byte aligned, contents ignored on
  * entry; it holds the normalised partial outputs (fp16) and LSEs (fp32) of row
  * tiles whose key range was split between CTAs, written by the attention and

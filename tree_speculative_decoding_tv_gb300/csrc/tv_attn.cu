@@ -65,6 +65,7 @@ constexpr int kSlots = 5;      // K/V ring: K(j) -> slot (2j) % 5, V(j) -> slot 
 constexpr int kThreads = 384;
 constexpr int kSoftmaxWarps = kM / 32;  // warps of one softmax warpgroup: each arrives once per phase
 constexpr int kMinTilesPerCta = 2;
+constexpr int kAlignedMaxTiles = 8;  // unit-aligned schedule: at most this many KV tiles per unit
 constexpr uint32_t kRegsLow = 64;    // warpgroup 0 after setmaxnreg.dec (128 x 64 + 256 x 216 <= 384 x 168)
 constexpr uint32_t kRegsHigh = 216; // softmax warpgroups after setmaxnreg.inc
 
@@ -126,6 +127,7 @@ struct AttnParams {
     uint4 *ws_o;    // [2 * grid][2 tiles][16 chunks][128 rows] x 8 fp16: partial O (normalised)
     float *ws_lse;  // [2 * grid][2 tiles][128]
     int nb, B, Hq, Hkv, G, NT, MT, W, max_pages, num_blocks;
+    int unit_aligned;  // 1: group k is exactly unit k (sequence k / Hkv, kv head k % Hkv); nothing is cut
     float scale_log2;
 };
 
@@ -418,19 +420,33 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
         // CTA c runs lane (pair tile) c % NP of group c / NP; each group takes an equal
         // share of the group items.  A grid smaller than NP forms one group whose lanes
         // its CTAs take in turn.
-        const long long total = sched_total(sch, lane);
+        // Small launches (p.unit_aligned, chosen by the host) instead give group k exactly
+        // unit k, so no tile is cut and no merge is needed.
         const int grid = (int)gridDim.x;
-        const long long G = active_groups(total, grid_groups(grid, sch.NP));
         const int grp = grid >= sch.NP ? (int)blockIdx.x / sch.NP : 0;
         const int lane0 = grid >= sch.NP ? (int)blockIdx.x % sch.NP : (int)blockIdx.x;
         long long t0 = 0, t1 = 0;
-        if (grp < G) {
-            t0 = total * grp / G;
-            t1 = total * (grp + 1) / G;
-        }
         int b0 = sch.nb;
         long long off0 = 0;
-        if (t1 > t0) sched_locate(sch, t0, lane, b0, off0);
+        if (p.unit_aligned) {
+            const int bb = grp / sch.Hkv;
+            if (bb < sch.nb) {
+                const int ut = unit_tiles(sch, __ldcg(sch.prefix_lens + bb));
+                if (ut > 0) {
+                    b0 = bb;
+                    off0 = (long long)(grp % sch.Hkv) * ut;
+                    t1 = ut;
+                }
+            }
+        } else {
+            const long long total = sched_total(sch, lane);
+            const long long G = active_groups(total, grid_groups(grid, sch.NP));
+            if (grp < G) {
+                t0 = total * grp / G;
+                t1 = total * (grp + 1) / G;
+            }
+            if (t1 > t0) sched_locate(sch, t0, lane, b0, off0);
+        }
         if (lane == 0) {
             *sh_b0 = b0;
             *sh_off0 = off0;
@@ -1243,11 +1259,19 @@ int32_t launch_attn(const tv_attn_args *a, int ctas, void *workspace, cudaStream
     p.num_blocks = a->num_blocks;
     const float scale = a->scale > 0.f ? a->scale : 1.0f / sqrtf((float)kHeadDim);
     p.scale_log2 = scale * 1.4426950408889634f;
+    // A launch whose units all fit the grid at once and whose block table covers only a
+    // few KV tiles per unit (its length bounds every unit's) gives each unit its own CTA
+    // group: no tile is cut, so the merge kernel is not launched at all.
+    const int NP = (p.MT + 1) / 2;
+    const long long unit_ctas = (long long)a->nb * a->Hkv * NP;
+    const long long max_unit_tiles = ((long long)a->max_pages * kPage + kN - 1) / kN;
+    p.unit_aligned = (unit_ctas <= ctas && max_unit_tiles <= kAlignedMaxTiles) ? 1 : 0;
+    const int grid = p.unit_aligned ? (int)unit_ctas : ctas;
 
     cudaError_t e = attn_smem_opt_in();
     if (e == cudaSuccess)
-        e = launch_dependent(tree_attn_kernel, dim3(ctas), dim3(kThreads), kSmemBytes, stream, p);
-    if (e == cudaSuccess) {
+        e = launch_dependent(tree_attn_kernel, dim3(grid), dim3(kThreads), kSmemBytes, stream, p);
+    if (e == cudaSuccess && !p.unit_aligned) {
         // The merge kernel may be scheduled while the attention grid drains; it waits
         // (griddepcontrol.wait) before reading partials.
         MergeParams mp{a->prefix_lens_d, p.ws_o, p.ws_lse, p.o, p.lse, p.nb, p.B, p.Hq, p.Hkv, p.G, p.NT, p.MT,
