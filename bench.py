@@ -412,10 +412,10 @@ def stage_rooflines(w: wl.Workload, t_attn: float, t_acc: float, peaks: dict, pe
     else:
         attn = {"kernel": kname, "bound": "hbm", "achieved": ab / t_attn / 1e9, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "peak_nominal": NOMINAL_PEAKS["hbm_gbs"]}
-    acc = {"kernel": "argmax_rows_kernel + accept_kernel (tv_accept)", "bound": "hbm",
+    acc = {"kernel": "argmax_span_kernel + accept_kernel (tv_accept)", "bound": "hbm",
            "achieved": lb / t_acc / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
            "peak_nominal": NOMINAL_PEAKS["hbm_gbs"]}
-    for r, src, name in ((attn, "tv_attn.cu", "tree_attn_kernel"), (acc, "tv_accept.cu", "argmax_rows_kernel")):
+    for r, src, name in ((attn, "tv_attn.cu", "tree_attn_kernel"), (acc, "tv_accept.cu", "argmax_span_kernel")):
         r["frac"] = r["achieved"] / r["peak"]
         r["frac_nominal"] = r["achieved"] / r["peak_nominal"]
         r["peak_source"] = peak_src + " burst; frac_nominal is of the GB300 data-sheet figure"
