@@ -597,13 +597,6 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                     umma_bf16_ts_lohi(tmem + tmem_o(x), tmem + tmem_s(x) + kk * 8, va + kk * (2048 >> 4), kDescHi,
                                       kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
             };
-            // P_x of the slot's lx-th tile in the segment is in TMEM; before the slot's first PV
-            // of a segment, the previous segment's epilogue of slot x has read O_x
-            auto wait_p = [&](int x, int lx) -> bool {
-                const uint32_t gsx = x ? gs1 : gs0, scx = x ? sc1 : sc0;
-                if (!wait_bar(BAR_P_FULL + x, (gsx + lx) & 1)) return false;
-                return !(lx == 0 && scx > 0 && !wait_bar(BAR_O_EMPTY + x, (scx - 1) & 1));
-            };
             while (ok && next_seg(sch, cur, sg)) {
                 const int n = sg.j1 - sg.j0;
                 const bool pair = sg.has_b;
@@ -622,26 +615,54 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                         if (n == 1) umma_commit(BAR(BAR_Q_EMPTY));
                     }
                     __syncwarp();
+                    // Per step t the waits before a group go out as one try_wait over the
+                    // warp's lanes (each lane names its own barrier).
                     RingPos rv = ahead(r0, 1), rk = ahead(r0, 2);  // V(t), K(t + 1)
                     for (int t = 0; t < n; ++t) {
                         const bool more = t + 1 < n;
-                        if (!full(rv) || (more && !full(rk))) { ok = false; break; }
-                        for (int x = 0; x < 2; ++x) {
-                            if (!wait_p(x, t)) { ok = false; break; }
-                            tc_fence_after();
-                            if (lane == 0) {
-                                pv(x, rv, t > 0);
-                                if (more) {
-                                    qk(x, x, rk);
-                                    umma_commit(BAR(BAR_S_FULL + x));
-                                } else {
-                                    umma_commit(BAR(BAR_PV_DONE + x));
-                                }
-                            }
-                            __syncwarp();
+                        // lane 0: V(t); lane 1: K(t + 1); lane 2: slot 0's P(t); lane 3: slot 0's O
+                        // read by the previous segment's epilogue (first tile only)
+                        uint32_t wb = BAR(BAR_KV_FULL + rv.slot), wp = rv.phase;
+                        if (lane == 1 && more) {
+                            wb = BAR(BAR_KV_FULL + rk.slot);
+                            wp = rk.phase;
+                        } else if (lane == 2) {
+                            wb = BAR(BAR_P_FULL + 0);
+                            wp = (gs0 + t) & 1;
+                        } else if (lane == 3 && t == 0 && sc0 > 0) {
+                            wb = BAR(BAR_O_EMPTY + 0);
+                            wp = (sc0 - 1) & 1;
                         }
-                        if (!ok) break;
+                        if (!mbar_wait_lanes(wb, wp, abort_flag, p.status)) { ok = false; break; }
+                        tc_fence_after();
                         if (lane == 0) {
+                            pv(0, rv, t > 0);
+                            if (more) {
+                                qk(0, 0, rk);
+                                umma_commit(BAR(BAR_S_FULL + 0));
+                            } else {
+                                umma_commit(BAR(BAR_PV_DONE + 0));
+                            }
+
+                        }
+                        __syncwarp();
+                        // lane 0: slot 1's P(t); lane 1: slot 1's O (first tile only)
+                        wb = BAR(BAR_P_FULL + 1);
+                        wp = (gs1 + t) & 1;
+                        if (lane == 1 && t == 0 && sc1 > 0) {
+                            wb = BAR(BAR_O_EMPTY + 1);
+                            wp = (sc1 - 1) & 1;
+                        }
+                        if (!mbar_wait_lanes(wb, wp, abort_flag, p.status)) { ok = false; break; }
+                        tc_fence_after();
+                        if (lane == 0) {
+                            pv(1, rv, t > 0);
+                            if (more) {
+                                qk(1, 1, rk);
+                                umma_commit(BAR(BAR_S_FULL + 1));
+                            } else {
+                                umma_commit(BAR(BAR_PV_DONE + 1));
+                            }
                             umma_commit(BAR(BAR_KV_EMPTY + rv.slot));
                             if (more) umma_commit(BAR(BAR_KV_EMPTY + rk.slot));
                             if (t + 2 == n) umma_commit(BAR(BAR_Q_EMPTY));
@@ -673,7 +694,21 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                         const bool more = t + 2 < n;
                         // PV(t) waits only for V(t): these segments are bandwidth-bound, and K(t+2)
                         // is two tiles further out in the ring
-                        if (!full(rv) || !wait_p(x, t >> 1)) { ok = false; break; }
+                        // lane 0: V(t); lane 1: slot x's P; lane 2: slot x's O read by the previous
+                        // segment's epilogue (the slot's first tile only)
+                        {
+                            const int lx = t >> 1;
+                            const uint32_t gsx = x ? gs1 : gs0, scx = x ? sc1 : sc0;
+                            uint32_t wb = BAR(BAR_KV_FULL + rv.slot), wp = rv.phase;
+                            if (lane == 1) {
+                                wb = BAR(BAR_P_FULL + x);
+                                wp = (gsx + lx) & 1;
+                            } else if (lane == 2 && lx == 0 && scx > 0) {
+                                wb = BAR(BAR_O_EMPTY + x);
+                                wp = (scx - 1) & 1;
+                            }
+                            if (!mbar_wait_lanes(wb, wp, abort_flag, p.status)) { ok = false; break; }
+                        }
                         tc_fence_after();
                         if (lane == 0) {
                             pv(x, rv, t > 1);

@@ -117,6 +117,33 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     return mbar_wait_for(bar, parity, abort_flag, status, kWaitLimitNs);
 }
 
+// Whole warp: each lane waits for the phase of parity `parity` of its own barrier `bar`
+// (lanes may name different barriers, so one try_wait instruction checks several), and
+// the call returns once every lane's phase is complete.  Returns false (in every lane)
+// when the abort flag is raised or the wait runs past kWaitLimitNs (the flag is then
+// raised and TV_ERR_TIMEOUT reported).
+__device__ __forceinline__ bool mbar_wait_lanes(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                                int32_t *status)
+{
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (__all_sync(0xffffffffu, mbar_try_wait_suspend(bar, parity, kSuspendHintNs))) return true;
+        if ((it & 3) == 0) {
+            int stop = 0;
+            if ((threadIdx.x & 31) == 0) stop = *abort_flag ? 1 : (global_timer_ns() - t0 > kWaitLimitNs ? 2 : 0);
+            stop = __shfl_sync(0xffffffffu, stop, 0);
+            if (stop) {
+                if (stop == 2 && (threadIdx.x & 31) == 0) {
+                    *abort_flag = 1;
+                    report_status(status, TV_ERR_TIMEOUT);
+                }
+                return false;
+            }
+        }
+    }
+}
+
 // ----------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap)
