@@ -643,7 +643,6 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                             } else {
                                 umma_commit(BAR(BAR_PV_DONE + 0));
                             }
-
                         }
                         __syncwarp();
                         // lane 0: slot 1's P(t); lane 1: slot 1's O (first tile only)
