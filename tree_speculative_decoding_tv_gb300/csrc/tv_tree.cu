@@ -15,14 +15,15 @@
 // pool's best candidates in one step, as many as the serial process would take before
 // anything it creates could compete with them:
 //   * within a w > 1 round nothing new enters the pool (the round's nodes offer their
-//     children when it ends), so a batch is the round's best min(w, 32) candidates;
+//     children when it ends), so a batch is the round's best min(w, kTreeCap) candidates;
 //   * for w = 1, a new node's candidates are all at most its first child, whose key
 //     (score + the next depth's best log-prob, parent index at least `made`) bounds
-//     everything a batch can create.  With T0 the bound of the pool's best candidate and
-//     T1 the largest bound among the candidates above T0, the candidates above T1 come out
-//     of the serial process before any created one (each is above every bound of the
-//     candidates above it), so they form a batch.
-// A batch larger than 32 keeps its 32 best (an exact radix selection on the keys); each
+//     everything a batch can create, and lies below x.  With T0 the largest bound of the
+//     lists' heads and T1 the largest bound among the candidates above T0, the candidates
+//     above T1 come out of the serial process before any created one (each is above every
+//     bound of the candidates above it), so they form a batch.
+// A batch larger than kTreeCap keeps its kTreeCap best (exact: rank counting, or a radix
+// selection on the keys when there are more than kTreeCand candidates); each
 // batch member's rank among the others gives its node index.  Keys order candidates
 // exactly as the serial process does: (order-preserving score << 32) | ~((parent << 16) |
 // rank).
@@ -38,8 +39,8 @@ namespace tv {
 constexpr int kTreeMaxB = 256;
 constexpr int kTreeThreads = kTreeMaxB;  // thread j: node j's list
 constexpr int kTreeWarps = kTreeThreads / 32;
-constexpr int kTreeCap = 32;             // nodes made per batch at most
-constexpr int kTreeCand = 64;            // candidates ranked directly (more go through a radix selection)
+constexpr int kTreeCap = 64;             // nodes made per batch at most
+constexpr int kTreeCand = 128;           // candidates ranked directly (more go through a radix selection)
 constexpr int kTreeKeys = 4;             // a list's next keys kept in registers
 constexpr int kTreeSmemLp = 8192;        // log-prob tables up to this size are staged in shared memory
 
@@ -286,7 +287,7 @@ __global__ void __launch_bounds__(kTreeThreads) build_tree_kernel(const float *_
             m = block_max(m);
             T = m > 1u ? bound_key(m) : 0ull;
         } else {
-            // the round's best min(want, 32) candidates lie at or above its qh-th best head
+            // the round's best min(want, kTreeCap) candidates lie at or above its qh-th best head
             if (kn[0] != 0ull) sh.heads[atomicAdd(&sh.nheads[cb], 1)] = kn[0];
             __syncthreads();
             const int nh = sh.nheads[cb];
