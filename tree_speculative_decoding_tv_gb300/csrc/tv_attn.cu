@@ -546,8 +546,11 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
         // tcgen05.mma issue stalls while the tensor pipe is busy, so everything this warp
         // does between two MMA groups is pipe idle time: a slot's PV(t) and its next QK
         // go out back to back under one commit (S_FULL, which the softmax needs anyway),
-        // a step's K/V waits are done once up front, PV_DONE is committed only after a
-        // slot's last PV of the segment, and ring releases follow both slots' groups.
+        // a step's K/V waits are done once up front, and PV_DONE is committed only after a
+        // slot's last PV of the segment.  A commit costs the pipe about as much as an MMA, so
+        // in pair segments the ring slots are released by slot 1's softmax instead (S_FULL_1(t)
+        // completes only after every MMA before QK_1(t), which includes all readers of V(t-1)
+        // and K(t)); single-tile segments release them here, after their readers.
         // The warp shares its SM sub-partition with two softmax warps, so its own
         // instruction count matters too: ring positions advance incrementally and the
         // descriptors come from one register.  The control flow stays warp-uniform (lane 0
@@ -611,7 +614,6 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                         umma_commit(BAR(BAR_S_FULL + 0));
                         qk(1, 1, r0);
                         umma_commit(BAR(BAR_S_FULL + 1));
-                        umma_commit(BAR(BAR_KV_EMPTY + r0.slot));
                         if (n == 1) umma_commit(BAR(BAR_Q_EMPTY));
                     }
                     __syncwarp();
@@ -662,8 +664,6 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                             } else {
                                 umma_commit(BAR(BAR_PV_DONE + 1));
                             }
-                            umma_commit(BAR(BAR_KV_EMPTY + rv.slot));
-                            if (more) umma_commit(BAR(BAR_KV_EMPTY + rk.slot));
                             if (t + 2 == n) umma_commit(BAR(BAR_Q_EMPTY));
                         }
                         __syncwarp();
@@ -763,12 +763,18 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
         // gx: this slot's tiles so far; sx: segments with tiles for this slot; n_merge:
         // single-tile hand-overs so far (ML_* phases)
         uint32_t gx = 0, sx = 0, seg_i = 0, n_merge = 0;
+        uint32_t kvs = 0;  // KV tiles of the CTA's earlier segments (ring positions 2 kvs on)
+        // Pair segments: this thread (slot 1, row 0) releases the ring slots of K(t) and V(t-1)
+        // once S_1(t) is complete, and the last V once the slot's last PV is.
+        const bool releaser = x == 1 && row == 0;
+        auto release = [&](uint32_t q) { mbar_arrive(BAR(BAR_KV_EMPTY + ring_slot(q))); };
         bool ok = true, mask_ready = false;
         while (ok && next_seg(sch, cur, sg)) {
             const int n = sg.j1 - sg.j0;
             const bool pair = sg.has_b;
             const int nx = pair ? n : (x == 0 ? (n + 1) / 2 : n / 2);
             if (nx == 0) {  // slot unused in this segment
+                kvs += n;
                 ++seg_i;
                 continue;
             }
@@ -796,6 +802,10 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                 if (!__all_sync(0xffffffffu, mbar_wait(BAR(BAR_S_FULL + x), g_t & 1, abort_flag, p.status))) {
                     ok = false;
                     break;
+                }
+                if (pair && releaser) {
+                    if (t > 0) release(2 * (kvs + t) - 1);  // V(t - 1)
+                    release(2 * (kvs + t));                 // K(t)
                 }
                 tc_fence_after();
                 uint32_t s[4][32];
@@ -898,6 +908,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
             // phase per segment in which the slot has tiles)
             if (!__all_sync(0xffffffffu, mbar_wait(BAR(BAR_PV_DONE + x), sx & 1, abort_flag, p.status))) break;
             ++sx;
+            if (pair && releaser) release(2 * (kvs + n) - 1);  // V(n - 1)
             const bool merge_slots = !pair && n > 1;  // slot 1 holds the odd KV tiles of the same rows
             if (merge_slots && x == 1) {
                 // hand the row's (max, sum) to slot 0, which reads O_1 from TMEM itself
@@ -910,6 +921,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                 tc_fence_after();
                 if (lane == 0) mbar_arrive(BAR(BAR_O_EMPTY + 1));
                 gx += nx;
+                kvs += n;
                 ++seg_i;
                 ++n_merge;
                 continue;
@@ -997,6 +1009,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                     p.ws_lse[slot * kM + row] = lse_nat;
             }
             gx += nx;
+            kvs += n;
             ++seg_i;
         }
     }
