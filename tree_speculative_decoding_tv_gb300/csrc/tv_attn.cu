@@ -473,8 +473,9 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
         // Warp 0 loads Q and the K tiles, warp 2 the V tiles.  A 16-row page half is a
         // 2 KB copy, and one warp issues them at ~26 B/clk/SM on GB300, below the MMA
         // loop's need; two issuing warps overlap their copies.  Each warp waits its own
-        // ring positions in order, and the MMA warp releases positions in order, so no
-        // wait can alias a later phase of its slot.
+        // ring positions in order, and positions are released in order (by the MMA warp, or
+        // in pair segments by slot 1's softmax), so no wait can alias a later phase of its
+        // slot.
         regs_decrease<kRegsLow>();
         const int kvh = warp == 0 ? 0 : 1;
         Cursor cur = cur0;
