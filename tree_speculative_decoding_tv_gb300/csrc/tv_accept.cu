@@ -43,6 +43,7 @@
 #include <atomic>
 #include <mutex>
 
+#include "tv_argmax.cuh"
 #include "tv_device.cuh"
 #include "tv_internal.h"
 
@@ -54,65 +55,6 @@ constexpr int kArgChunk = 32 * kArgVec * 8;   // logits per unit (8 KB): one war
 constexpr int kArgCtasPerSm = 2;  // resident CTAs per SM at the kernel's register use
 constexpr int kMaxB = 256;
 constexpr int kMaxW = kMaxB / 32;
-
-// (av, ai) beats (bv, bi): NaN above everything, then larger value, then smaller index.
-__device__ __forceinline__ bool beats(float av, int ai, float bv, int bi)
-{
-    const bool an = av != av, bn = bv != bv;
-    if (an != bn) return an;
-    if (!an && av != bv) return av > bv;
-    return ai < bi;
-}
-
-__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
-
-// Streaming 16-byte load (evict-first); volatile so a batch of them is issued back to back.
-__device__ __forceinline__ uint4 ld_stream_v4(const uint4 *p)
-{
-    uint4 v;
-    asm volatile("ld.global.cs.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-    return v;
-}
-
-// 64-bit key whose unsigned order is the argmax order: the value's rank in the
-// high half (every NaN ranks highest, -0 ranks with +0), then 0xFFFFFFFF - index
-// so that equal values favour the smaller index.
-__device__ __forceinline__ unsigned long long argmax_key(float v, int i)
-{
-    const uint32_t u = __float_as_uint(v);
-    uint32_t rank;
-    if (v != v)
-        rank = 0xFFFFFFFFu;
-    else if (v == 0.f)
-        rank = 0x80000000u;
-    else
-        rank = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-    return ((unsigned long long)rank << 32) | (0xFFFFFFFFu - (uint32_t)i);
-}
-
-// max with a NaN counting as the largest value
-__device__ __forceinline__ float max_nan(float a, float b) { return (a != a) ? a : ((b != b) ? b : fmaxf(a, b)); }
-
-__device__ __forceinline__ float vec_max(const uint4 &v)
-{
-    __nv_bfloat162 a = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162 *>(&v.x),
-                                   *reinterpret_cast<const __nv_bfloat162 *>(&v.y));
-    const __nv_bfloat162 c = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162 *>(&v.z),
-                                         *reinterpret_cast<const __nv_bfloat162 *>(&v.w));
-    a = __hmax2_nan(a, c);
-    return __bfloat162float(__hmax_nan(a.x, a.y));
-}
-
-// Order-preserving 32-bit rank of a value (the high half of its key): every NaN
-// on top, -0 with +0, never 0.
-__device__ __forceinline__ uint32_t value_rank(float v) { return (uint32_t)(argmax_key(v, 0) >> 32); }
-
-__device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t w) { return *reinterpret_cast<__nv_bfloat162 *>(&w); }
-
-__device__ __forceinline__ __nv_bfloat162 vec_max2(const uint4 &v)
-{
-    return __hmax2_nan(__hmax2_nan(as_bf2(v.x), as_bf2(v.y)), __hmax2_nan(as_bf2(v.z), as_bf2(v.w)));
-}
 
 // Shared memory of one acceptance walk (one sequence, one thread per node).
 struct AcceptSmem {
