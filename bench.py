@@ -179,13 +179,15 @@ class Step:
         self.lse = torch.empty((w.nb * w.B, w.Hq), dtype=torch.float32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         args = tv.attn_args(self.q, self.k, self.v, self.bt, self.pl, self.mask, self.o, self.lse, self.status)
-        self.ws = torch.empty(tv.attn_workspace_size(args), dtype=torch.uint8, device=dev)
+        self.ws = torch.zeros(tv.attn_workspace_size(args), dtype=torch.uint8, device=dev)
         self.acc_out = (torch.empty(w.nb * w.B, dtype=torch.int32, device=dev),
                         torch.empty(w.nb, dtype=torch.int32, device=dev),
                         torch.empty((w.nb, w.B), dtype=torch.int32, device=dev),
                         torch.empty(w.nb, dtype=torch.int32, device=dev))
         self.acc_ws = torch.zeros(tv.accept_workspace_size(w.V, w.B, w.nb), dtype=torch.uint8, device=dev)
-        self.launches_per_step = 4  # attention, merge, argmax, acceptance (the masks are folded in)
+        # the attention (1, or 2 with the split-KV merge kernel), argmax, acceptance (the masks are folded in)
+        self.launches_per_step = tv.attn_launches(tv.attn_args(self.q, self.k, self.v, self.bt, self.pl, None, self.o,
+                                                               self.lse, self.status, parent=self.parent)) + 2
         self.g_step = self.g_attn = self.g_acc = None
 
     # The step is the folded form: the attention and the acceptance walk derive the ancestor
@@ -201,9 +203,9 @@ class Step:
 
     def time_step_form(self, flush, steps, form):
         """Mean ms of one form of the whole step (its own graph, same flush, own outputs):
-        "mask": tv_build_mask + attention + merge + argmax + walk (5 launches);
-        "folded": attention and walk build the ancestor bits from the parent array (4 launches);
-        "fused": folded, with argmax and walk in one kernel, tv_accept_fused (3 launches)."""
+        "mask": tv_build_mask + attention (+ merge) + argmax + walk;
+        "folded": attention and walk build the ancestor bits from the parent array (no mask kernel);
+        "fused": folded, with argmax and walk in one kernel, tv_accept_fused."""
         torch, tv = self.torch, self.tv
         dev = self.q.device
         ws = torch.zeros(tv.accept_fused_workspace_size(self.w.V, self.w.B, self.w.nb), dtype=torch.uint8, device=dev)
@@ -405,7 +407,8 @@ def stage_rooflines(w: wl.Workload, t_attn: float, t_acc: float, peaks: dict, pe
     the acceptance stage (HBM), for stage times in seconds.  frac is against the measured peak
     (peaks), frac_nominal against the GB300 data-sheet figure (NOMINAL_PEAKS)."""
     ab, af, lb = attn_bytes(w), attn_flops(w), accept_bytes(w)
-    kname = "attention stage: tree_attn_kernel (ancestor bits from the parent array) + tree_attn_merge_kernel"
+    kname = ("attention stage: tree_attn_kernel (ancestor bits from the parent array; split-KV merge inside, or "
+             "tree_attn_merge_kernel after it when split tiles have many parts)")
     if af / (peaks["bf16_tflops"] * 1e12) >= ab / (peaks["hbm_gbs"] * 1e9):
         attn = {"kernel": kname, "bound": "tensor", "achieved": af / t_attn / 1e12, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "peak_nominal": NOMINAL_PEAKS["bf16_tflops"]}
@@ -611,16 +614,17 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         "config": {"workload": wl.CONFIG_NAMES[args.config], "nb": w.nb, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
                    "D": w.D, "prefix_lens": [int(x) for x in w.prefix_lens][:8], "V": w.V,
                    "l2": "flushed before every timed step (512 MB write)", "parallelism": f"replicas x{world}",
-                   "launch": "one CUDA graph per step (attention with the ancestor bits from the parent array, merge, "
-                             "argmax, acceptance walk), captured once"},
+                   "launch": "one CUDA graph per step (attention with the ancestor bits from the parent array and "
+                             "the split-KV merge, argmax, acceptance walk; %d launches), captured once"
+                             % st.launches_per_step},
         "roofline": roof,
         "breakdown": {
             "attention_stage_ms": attn_stage_ms, "accept_ms": acc_stage_ms, "accept_fused_ms": acc_fused_ms,
             "accept_fused_nomask_ms": acc_fused_nomask_ms, "step_forms_ms": forms_ms,
             "step_forms_note": "each form of the whole step from its own graph with the same flush: mask = "
-                               "tv_build_mask + attention + merge + argmax + walk (5 launches); folded = the "
-                               "attention and the walk derive the ancestor bits from the parent array (4); fused = "
-                               "folded with tv_accept_fused (3)",
+                               "tv_build_mask + attention + argmax + walk; folded = the attention and the walk "
+                               "derive the ancestor bits from the parent array (no mask kernel); fused = folded "
+                               "with tv_accept_fused (argmax and walk in one kernel)",
             "accept_note": "the step's acceptance is the two-kernel tv_accept (argmax, then the walk as a programmatic "
                            "dependent); accept_fused_ms is tv_accept_fused (one kernel) on the same inputs with the "
                            "step's mask, accept_fused_nomask_ms the same building the mask from the parent array",

@@ -150,15 +150,23 @@ typedef struct tv_attn_args {
  * arguments are invalid. */
 TV_API size_t tv_attn_workspace_size(const tv_attn_args *args);
 
-/* Enqueue the attention: two kernel launches on `stream`, the attention and a
- * merge of split-KV pieces; a small launch (every (sequence, kv head) unit fits
- * the CTA count at once and the block table covers at most 8 KV tiles of 128
- * keys per sequence) gives each unit its own CTAs, cuts no tile and launches
- * the attention alone.  workspace_d: device buffer of at least
- * tv_attn_workspace_size(args) bytes, 16-byte aligned, contents ignored on
- * entry; it holds the normalised partial outputs (fp16) and LSEs (fp32) of row
- * tiles whose key range was split between CTAs, written by the attention and
- * read by the merge, so concurrent calls need separate workspaces.
+/* Enqueue the attention: one or two kernel launches on `stream`
+ * (tv_attn_launches says which).  Row tiles whose key range is split between
+ * CTAs leave normalised partial outputs (fp16) and LSEs (fp32) in the
+ * workspace.  The CTAs form groups of NP = ceil(MT / 2) (MT = ceil(B / (128 /
+ * (Hq / Hkv))) row tiles per (sequence, kv head) unit); with fewer groups than
+ * twice the units (a split tile then has about two parts) the CTA whose part
+ * of a tile lands last merges it, otherwise a second kernel merges every split
+ * tile.  A small launch (every unit fits the CTA count at once and the block
+ * table covers at most 8 KV tiles of 128 keys per sequence) gives each unit
+ * its own CTAs and splits nothing.
+ * workspace_d: device buffer of at least tv_attn_workspace_size(args) bytes,
+ * 16-byte aligned.  It must be zero-filled (cudaMemset) before its first call;
+ * besides the partials it holds arrival counters, at offsets that do not
+ * depend on the arguments, which every call leaves zero, so a workspace can
+ * serve calls of any shape after that.  A call that reports TV_ERR_TIMEOUT
+ * may leave counters behind: zero the workspace again before reusing it.
+ * Concurrent calls need separate workspaces.
  *
  * Ordering: the attention kernel is launched as a programmatic dependent of the
  * previous kernel on the stream and reads q, the caches, block_table and
@@ -171,6 +179,12 @@ TV_API size_t tv_attn_workspace_size(const tv_attn_args *args);
  * Returns TV_OK, TV_ERR_INVALID_ARG, TV_ERR_UNSUPPORTED_SHAPE or TV_ERR_CUDA.
  * nb == 0 is a no-op. */
 TV_API int32_t tv_attn(const tv_attn_args *args, void *workspace_d, size_t workspace_bytes, void *stream);
+
+/* Kernel launches tv_attn enqueues for these arguments: 1 (the attention,
+ * merging split tiles itself) or 2 (the attention, then the merge kernel);
+ * 0 when nb == 0 or the arguments are invalid.  With num_ctas == 0 it asks the
+ * current device for its SM count. */
+TV_API int32_t tv_attn_launches(const tv_attn_args *args);
 
 /*
  * Vocab argmax and greedy acceptance  [JF-4] (rule: this library's reading)

@@ -84,6 +84,30 @@ def test_attn_argument_checks(L, kw, code):
 def test_attn_null_args(L):
     assert L.tv_attn(None, None, 0, None) == 1
     assert L.tv_attn_workspace_size(None) == 0
+    assert L.tv_attn_launches(None) == 0
+
+
+@pytest.mark.parametrize("kw,launches", [
+    # 4 sequences x 8 kv heads, 256-node trees (4 pair tiles per unit), 32K prefixes, 152 CTAs:
+    # 38 groups over 32 units, so a split tile has about two parts and is merged in place
+    (dict(nb=4, B=256, max_pages=2064, num_blocks=8256, num_ctas=152), 1),
+    # one sequence: 38 groups over 8 units, many parts per split tile: the merge kernel runs
+    (dict(nb=1, B=256, max_pages=272, num_blocks=272, num_ctas=152), 2),
+    # 8 sequences x 8 kv heads, 64-node trees (one pair tile per unit): 152 groups, 64 units
+    (dict(nb=8, B=64, max_pages=1030, num_blocks=8240, num_ctas=152), 2),
+    # 32 sequences x 4 kv heads, 16-node trees: 152 groups over 128 units
+    (dict(nb=32, B=16, Hkv=4, max_pages=514, num_blocks=16448, num_ctas=152), 1),
+    # every unit fits the grid and the block table covers few KV tiles: nothing is split
+    (dict(nb=1, B=16, max_pages=33, num_blocks=33, num_ctas=152), 1),
+    # fewer CTAs than pair tiles per unit: one group, nothing is split
+    (dict(nb=1, B=256, max_pages=272, num_blocks=272, num_ctas=3), 1),
+    (dict(nb=0, num_ctas=152), 0),                 # nothing to do
+    (dict(B=0, num_ctas=152), 0),                  # invalid
+])
+def test_attn_launch_count(L, kw, launches):
+    """tv_attn_launches (host-only with an explicit CTA count): one kernel when split tiles
+    have about two parts or none, the merge kernel too when they have more."""
+    assert L.tv_attn_launches(C.byref(_args(**kw))) == launches
 
 
 def test_accept_argument_checks(L):

@@ -76,7 +76,7 @@ def test_attention_needs_mask_or_parent():
 
 @pytest.mark.parametrize("config", [1, 3])
 def test_folded_step_matches_oracle(config):
-    """attention from parents + merge + tv_accept_fused without a mask: three launches."""
+    """attention from parents + tv_accept_fused without a mask: two launches."""
     w = wl.config(config, seed=5)
     d = DevWorkload(w)
     O, L = tv.attn(d.q, d.k, d.v, d.bt, d.pl, None, status=d.status, parent=d.parent)

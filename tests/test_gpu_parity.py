@@ -193,6 +193,44 @@ def test_attention_many_ctas_ragged_prefixes():
     assert d.status.item() == 0
 
 
+# tv_attn's workspace per CTA: 128 bytes of arrival counters, four 32 KB fp16 partial
+# outputs and their four 512-byte LSE rows
+ATTN_WS_BLOCK = 128 + 4 * 32768 + 4 * 512
+
+
+def test_attention_workspace_reused_across_shapes():
+    """One workspace, zeroed once, serves split-KV calls of different shapes and CTA counts
+    (pair tiles, a single-tile unit, ragged prefixes), merged in place or by the merge
+    kernel: every call matches the oracle, leaves every arrival counter zero, and a repeated
+    call gives bit-identical outputs (the merge does not depend on which CTA lands last)."""
+    cases = [
+        # (workload, CTA counts): 300 and 0 (one per SM) take the merge kernel here, 7 and
+        # fewer merge in place (fewer CTA groups than twice the units)
+        (_workload(21, 6, 40, 32, 8, [5000, 1, 2222, 4097, 0, 129], V=8), (300, 7, 0)),  # pairs, ragged
+        (_workload(22, 2, 16, 32, 8, [4000, 1500], V=8), (300, 7, 0)),                   # one M tile per unit
+        (_workload(23, 1, 256, 32, 8, [3000], V=8), (300, 7, 0)),                        # four pair tiles per unit
+        # two units, one 157 KV tiles long: on 3 CTAs it is cut into three pieces (one from
+        # a CTA whose whole share lies inside it), merged in place
+        (_workload(24, 2, 16, 8, 1, [20000, 10], V=8), (3, 2, 300)),
+    ]
+    ws = torch.zeros(300 * ATTN_WS_BLOCK, dtype=torch.uint8, device="cuda")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for w, ctas_list in cases:
+        d = DevWorkload(w)
+        mask, _ = d.mask()
+        O_ref, L_ref = oracle.attn_workload(w)
+        for ctas in ctas_list:
+            O, L = tv.attn(d.q, d.k, d.v, d.bt, d.pl, mask, status=d.status, num_ctas=ctas, workspace=ws)
+            O2, L2 = tv.attn(d.q, d.k, d.v, d.bt, d.pl, mask, status=d.status, num_ctas=ctas, workspace=ws)
+            torch.cuda.synchronize()
+            assert d.status.item() == 0
+            assert_attn_close(O, L, O_ref, L_ref, w)
+            assert torch.equal(O.view(torch.int16), O2.view(torch.int16)) and torch.equal(L, L2)
+            n = ctas if ctas > 0 else sms
+            counters = ws[: n * ATTN_WS_BLOCK].view(n, ATTN_WS_BLOCK)[:, :128]
+            assert int(counters.count_nonzero()) == 0
+
+
 def test_attention_explicit_scale():
     w = _workload(12, 1, 20, 8, 2, [77], V=8)
     d = DevWorkload(w)

@@ -23,7 +23,7 @@ TV_ERR_CUDA = 4
 TV_ERR_TIMEOUT = 5
 TV_ERR_UNIMPLEMENTED = 6
 
-EXPORTED = ("tv_status_str", "tv_version", "tv_build_mask", "tv_attn_workspace_size", "tv_attn",
+EXPORTED = ("tv_status_str", "tv_version", "tv_build_mask", "tv_attn_workspace_size", "tv_attn", "tv_attn_launches",
             "tv_accept_workspace_size", "tv_accept", "tv_accept_fused_workspace_size", "tv_accept_fused",
             "tv_accept_noalloc", "tv_kv_commit", "tv_build_tree", "tv_gdn_tree_workspace_size", "tv_gdn_tree", "tv_gdn_commit",
             "tv_selftest_wait")
@@ -67,6 +67,8 @@ def lib() -> C.CDLL:
         L.tv_build_mask.restype = I
         L.tv_attn_workspace_size.argtypes = [C.POINTER(AttnArgs)]
         L.tv_attn_workspace_size.restype = C.c_size_t
+        L.tv_attn_launches.argtypes = [C.POINTER(AttnArgs)]
+        L.tv_attn_launches.restype = C.c_int32
         L.tv_attn.argtypes = [C.POINTER(AttnArgs), P, C.c_size_t, P]
         L.tv_attn.restype = I
         L.tv_accept_workspace_size.argtypes = [I, I, I]
@@ -148,10 +150,17 @@ def attn_workspace_size(args: AttnArgs) -> int:
     return int(lib().tv_attn_workspace_size(C.byref(args)))
 
 
+def attn_launches(args: AttnArgs) -> int:
+    """Kernel launches tv_attn enqueues for these arguments (1, or 2 with the merge kernel)."""
+    return int(lib().tv_attn_launches(C.byref(args)))
+
+
 def attn(q, k_cache, v_cache, block_table, prefix_lens, mask, status=None, scale: float = 0.0, num_ctas: int = 0,
          o=None, lse=None, workspace=None, stream=None, parent=None):
     """tv_attn: returns (O bf16 [nb*B][Hq][D], LSE fp32 [nb*B][Hq]); mask=None with parent
-    given folds the mask build into the attention."""
+    given folds the mask build into the attention.  A workspace passed in must have been
+    zeroed once before its first use (every call leaves its counters zero); without one,
+    a zeroed workspace is allocated for this call."""
     if o is None:
         o = torch.empty_like(q)
     if lse is None:
@@ -162,7 +171,7 @@ def attn(q, k_cache, v_cache, block_table, prefix_lens, mask, status=None, scale
         _check(lib().tv_attn(C.byref(a), None, 0, _stream(stream)), "tv_attn")
         return o, lse
     if workspace is None or workspace.numel() * workspace.element_size() < need:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
     rc = lib().tv_attn(C.byref(a), _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "tv_attn")
     return o, lse

@@ -110,6 +110,14 @@ size_t tv_attn_workspace_size(const tv_attn_args *args)
     return tv::attn_workspace_bytes(ctas, tv::attn_row_tiles(args));
 }
 
+int32_t tv_attn_launches(const tv_attn_args *args)
+{
+    if (check_attn(args) != TV_OK || args->nb == 0) return 0;
+    const int ctas = attn_ctas(args);
+    if (ctas < 1) return 0;
+    return tv::attn_kernel_launches(args, ctas);
+}
+
 int32_t tv_attn(const tv_attn_args *args, void *workspace_d, size_t workspace_bytes, void *stream)
 {
     const int32_t rc = check_attn(args);

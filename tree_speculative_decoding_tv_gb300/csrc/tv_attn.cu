@@ -17,10 +17,12 @@
 //   * Stream-K: the (pair tile, 128-key KV tile) items of all sequences are
 //     cut into equal contiguous shares, one per CTA, computed in-kernel from
 //     prefix_lens, so ragged prefixes balance by construction.  A pair tile cut
-//     between CTAs leaves fp32 partials (normalised O, LSE) in the workspace,
-//     and a merge kernel launched as a programmatic dependent of this one
-//     combines them with every SM at once (its launch overlaps this kernel's
-//     tail; no CTA ever waits on another).
+//     between CTAs leaves partials (normalised O in fp16, LSE) in the
+//     workspace.  When the cut tiles have few pieces, each 32-row quarter of a
+//     tile counts its pieces in and the warp whose piece lands last merges that
+//     quarter right away; otherwise a merge kernel launched as a programmatic
+//     dependent of this one combines them with every SM at once.  No CTA ever
+//     waits on another.
 //   * Warp roles (384 threads): warp 0 issues TMA (Q by a 4-D map whose node
 //     axis stops at B; K/V one 16-key page x 64 columns per copy through a 2-D
 //     map over [pages*Hkv*16][D], page ids from the block table, rows past the
@@ -124,12 +126,37 @@ struct AttnParams {
     uint16_t *o;
     float *lse;
     int32_t *status;
-    uint4 *ws_o;    // [2 * grid][2 tiles][16 chunks][128 rows] x 8 fp16: partial O (normalised)
-    float *ws_lse;  // [2 * grid][2 tiles][128]
+    uint8_t *ws;  // one block of kWsBlock bytes per CTA (ws_cnt, ws_piece_o, ws_piece_lse)
     int nb, B, Hq, Hkv, G, NT, MT, W, max_pages, num_blocks;
     int unit_aligned;  // 1: group k is exactly unit k (sequence k / Hkv, kv head k % Hkv); nothing is cut
+    int merge_in_place;  // 1: the warp whose piece of a cut tile lands last merges it; 0: the merge kernel does
     float scale_log2;
 };
+
+// ------------------------------------------------------------------ workspace
+
+// CTA c's block of the workspace: arrival counters, then four piece slots (slot
+// 2 * (starts its tile) + x) of normalised O in fp16, chunk-major (8-column chunk k of
+// row r at [k][r], so a warp's 32 rows store 512 contiguous bytes per instruction), then
+// their LSEs.  A block's counters sit at the same offset whatever the shape or the CTA
+// count, so a workspace zeroed once keeps them zero from call to call: every counter
+// that is counted up is set back to zero by the warp that merges.
+constexpr size_t kWsCntBytes = 128;                           // 8 counters used: [x][quarter]
+constexpr size_t kWsSlotO = (size_t)kM * kHeadDim * 2;         // 32 KB
+constexpr size_t kWsBlock = kWsCntBytes + 4 * kWsSlotO + 4 * (size_t)kM * sizeof(float);
+
+__device__ __forceinline__ uint32_t *ws_cnt(uint8_t *ws, int cta)
+{
+    return reinterpret_cast<uint32_t *>(ws + (size_t)cta * kWsBlock);
+}
+__device__ __forceinline__ uint4 *ws_piece_o(uint8_t *ws, int cta, int slot)
+{
+    return reinterpret_cast<uint4 *>(ws + (size_t)cta * kWsBlock + kWsCntBytes + (size_t)slot * kWsSlotO);
+}
+__device__ __forceinline__ float *ws_piece_lse(uint8_t *ws, int cta, int slot)
+{
+    return reinterpret_cast<float *>(ws + (size_t)cta * kWsBlock + kWsCntBytes + 4 * kWsSlotO) + (size_t)slot * kM;
+}
 
 // ------------------------------------------------------------------ schedule
 
@@ -232,11 +259,13 @@ struct Cursor {
     int lane_step;   // next lane: lane + lane_step (only when the grid is smaller than NP)
     int b0;          // the range's start and length, to revisit it for the next lane
     long long off0, left0;
+    long long sbase, sbase0;  // global index of sequence b's (b0's) first group item
 };
 
 struct Seg {
     int b, g, mp, j0, j1, n_row, P;
     bool has_b;
+    long long su;  // global index of the unit's first group item
 };
 
 // Next segment (a run of KV tiles of one pair tile) of this CTA's share.  A group's CTAs
@@ -251,6 +280,7 @@ __device__ __forceinline__ bool next_seg(const Sched &s, Cursor &c, Seg &sg)
             const int P = __ldcg(s.prefix_lens + c.b);
             const int ut = unit_tiles(s, P);
             if (c.off >= (long long)ut * s.Hkv) {
+                c.sbase += (long long)ut * s.Hkv;
                 ++c.b;
                 c.off = 0;
                 continue;
@@ -270,6 +300,7 @@ __device__ __forceinline__ bool next_seg(const Sched &s, Cursor &c, Seg &sg)
             sg.n_row = n;
             sg.P = P;
             sg.has_b = 2 * c.lane + 1 < s.MT;
+            sg.su = c.sbase + (long long)g * ut;
             return true;
         }
         if (c.left0 <= 0 || c.lane + c.lane_step >= s.NP) return false;
@@ -277,6 +308,7 @@ __device__ __forceinline__ bool next_seg(const Sched &s, Cursor &c, Seg &sg)
         c.b = c.b0;
         c.off = c.off0;
         c.left = c.left0;
+        c.sbase = c.sbase0;
     }
 }
 
@@ -358,6 +390,80 @@ __device__ __forceinline__ uint32_t visible_bits(int kstart, int P, int B, const
     return v;
 }
 
+// ------------------------------------------------------------------ merge
+
+// The split-KV combine of one row of a cut M tile, over the pieces of groups k0 .. k1
+// (group k's piece is in CTA k * NP + pm, slot 2 * (k == k0) + x): with lse_k the
+// pieces' log-sum-exps and O_k their normalised outputs, lse = ln sum_k e^{lse_k} and
+// O = sum_k e^{lse_k - lse} O_k.  One pass per 64 columns over pairs of pieces, each
+// pair's LSEs and outputs loaded together, with a running maximum that rescales the
+// sums between pairs.  A piece whose keys were all masked has lse_k = -inf and weight
+// 0; a row with no visible key at all gets O = 0 and lse = -inf.
+__device__ __noinline__ void merge_pieces(uint8_t *ws, int k0, int k1, int NP, int pm, int x, int row,
+                                          uint4 *__restrict__ o_row, float *__restrict__ lse_out)
+{
+    float m = -INFINITY, wsum = 0.f;
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+        float acc[64];
+#pragma unroll
+        for (int e = 0; e < 64; ++e) acc[e] = 0.f;
+        m = -INFINITY;
+        wsum = 0.f;
+#pragma unroll 1
+        for (int k = k0; k <= k1; k += 2) {
+            float l[2];
+            uint4 v[2][8];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const bool in = k + u <= k1;
+                const int kk = in ? k + u : k;
+                const int cta = kk * NP + pm, slot = (kk == k0 ? 2 : 0) + x;
+                l[u] = in ? __ldcg(ws_piece_lse(ws, cta, slot) + row) : -INFINITY;
+                const uint4 *src = ws_piece_o(ws, cta, slot) + (size_t)(h * 8) * kM + row;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) v[u][c] = in ? __ldcg(src + (size_t)c * kM) : make_uint4(0u, 0u, 0u, 0u);
+            }
+            const float mb = fmaxf(m, fmaxf(l[0], l[1]));
+            if (mb == -INFINITY) continue;  // no piece with a visible key yet
+            const float sc = expf(m - mb);   // 0 while m is still -inf
+            wsum *= sc;
+#pragma unroll
+            for (int e = 0; e < 64; ++e) acc[e] *= sc;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const float w = expf(l[u] - mb);  // 0 for an empty piece
+                wsum += w;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const float2 a = unpack_f16x2(v[u][c].x), b = unpack_f16x2(v[u][c].y);
+                    const float2 d = unpack_f16x2(v[u][c].z), e = unpack_f16x2(v[u][c].w);
+                    acc[8 * c + 0] = fmaf(w, a.x, acc[8 * c + 0]);
+                    acc[8 * c + 1] = fmaf(w, a.y, acc[8 * c + 1]);
+                    acc[8 * c + 2] = fmaf(w, b.x, acc[8 * c + 2]);
+                    acc[8 * c + 3] = fmaf(w, b.y, acc[8 * c + 3]);
+                    acc[8 * c + 4] = fmaf(w, d.x, acc[8 * c + 4]);
+                    acc[8 * c + 5] = fmaf(w, d.y, acc[8 * c + 5]);
+                    acc[8 * c + 6] = fmaf(w, e.x, acc[8 * c + 6]);
+                    acc[8 * c + 7] = fmaf(w, e.y, acc[8 * c + 7]);
+                }
+            }
+            m = mb;
+        }
+        const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            uint4 q;
+            q.x = pack_bf16x2(acc[8 * c + 0] * inv, acc[8 * c + 1] * inv);
+            q.y = pack_bf16x2(acc[8 * c + 2] * inv, acc[8 * c + 3] * inv);
+            q.z = pack_bf16x2(acc[8 * c + 4] * inv, acc[8 * c + 5] * inv);
+            q.w = pack_bf16x2(acc[8 * c + 6] * inv, acc[8 * c + 7] * inv);
+            o_row[h * 8 + c] = q;
+        }
+    }
+    *lse_out = wsum > 0.f ? m + logf(wsum) : -INFINITY;
+}
+
 // ------------------------------------------------------------------ kernel
 
 __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_constant__ AttnParams p)
@@ -376,6 +482,9 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
     long long *sh_left = reinterpret_cast<long long *>(gbase + kOffMisc + 24);
     int *sh_lane = reinterpret_cast<int *>(gbase + kOffMisc + 32);
     int *sh_step = reinterpret_cast<int *>(gbase + kOffMisc + 36);
+    long long *sh_sbase = reinterpret_cast<long long *>(gbase + kOffMisc + 40);
+    long long *sh_total = reinterpret_cast<long long *>(gbase + kOffMisc + 48);   // group items
+    long long *sh_groups = reinterpret_cast<long long *>(gbase + kOffMisc + 56);  // groups with work
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -425,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
         const int grid = (int)gridDim.x;
         const int grp = grid >= sch.NP ? (int)blockIdx.x / sch.NP : 0;
         const int lane0 = grid >= sch.NP ? (int)blockIdx.x % sch.NP : (int)blockIdx.x;
-        long long t0 = 0, t1 = 0;
+        long long t0 = 0, t1 = 0, total = 0, G = 1;
         int b0 = sch.nb;
         long long off0 = 0;
         if (p.unit_aligned) {
@@ -439,8 +548,8 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                 }
             }
         } else {
-            const long long total = sched_total(sch, lane);
-            const long long G = active_groups(total, grid_groups(grid, sch.NP));
+            total = sched_total(sch, lane);
+            G = active_groups(total, grid_groups(grid, sch.NP));
             if (grp < G) {
                 t0 = total * grp / G;
                 t1 = total * (grp + 1) / G;
@@ -453,6 +562,9 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
             *sh_left = t1 - t0;
             *sh_lane = lane0;
             *sh_step = grid >= sch.NP ? sch.NP : grid;
+            *sh_sbase = t0 - off0;  // (stream-K) t0 is item off0 of sequence b0
+            *sh_total = total;
+            *sh_groups = G;
         }
         if (blockIdx.x == 0) {
             for (int b = lane; b < sch.nb; b += 32) {
@@ -465,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const Cursor cur0{*sh_b0, *sh_off0, *sh_left, *sh_lane, *sh_step, *sh_b0, *sh_off0, *sh_left};
+    const Cursor cur0{*sh_b0, *sh_off0, *sh_left, *sh_lane, *sh_step, *sh_b0, *sh_off0, *sh_left, *sh_sbase, *sh_sbase};
     pdl_launch_dependents();
 
     if (warp == 0 || warp == 2) {
@@ -757,26 +869,28 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
         const int node_local = row / p.G;
         const int hg = row - node_local * p.G;
         const float sl2 = p.scale_log2;
+        const long long s_total = *sh_total, s_groups = *sh_groups;
         float *sh_m = reinterpret_cast<float *>(gbase + kOffML);  // slot 1's running max / sum per row
         float *sh_l = sh_m + kM;
         Cursor cur = cur0;
         Seg sg;
         // gx: this slot's tiles so far; sx: segments with tiles for this slot; n_merge:
         // single-tile hand-overs so far (ML_* phases)
-        uint32_t gx = 0, sx = 0, seg_i = 0, n_merge = 0;
+        uint32_t gx = 0, sx = 0, n_merge = 0;
         uint32_t kvs = 0;  // KV tiles of the CTA's earlier segments (ring positions 2 kvs on)
         // Pair segments: this thread (slot 1, row 0) releases the ring slots of K(t) and V(t-1)
         // once S_1(t) is complete, and the last V once the slot's last PV is.
         const bool releaser = x == 1 && row == 0;
         auto release = [&](uint32_t q) { mbar_arrive(BAR(BAR_KV_EMPTY + ring_slot(q))); };
-        bool ok = true, mask_ready = false;
+        // primary_done: this thread has waited for the previous kernel (griddepcontrol.wait),
+        // before its first read of the masks or parents and before its first global write
+        bool ok = true, primary_done = false;
         while (ok && next_seg(sch, cur, sg)) {
             const int n = sg.j1 - sg.j0;
             const bool pair = sg.has_b;
             const int nx = pair ? n : (x == 0 ? (n + 1) / 2 : n / 2);
             if (nx == 0) {  // slot unused in this segment
                 kvs += n;
-                ++seg_i;
                 continue;
             }
             const int i = (2 * sg.mp + (pair ? x : 0)) * p.NT + node_local;
@@ -788,9 +902,9 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
             // path (dependent loads over the parent array) now, while the first S of the
             // segment is still on its way, rather than at its first masked tile.
             if (!mrow && valid && (long long)sg.j1 * kN > sg.P) {
-                if (!mask_ready) {  // the parents may come from the previous kernel
+                if (!primary_done) {  // the parents may come from the previous kernel
                     pdl_wait_primary();
-                    mask_ready = true;
+                    primary_done = true;
                 }
                 row_mask_from_parents(p.parent + (size_t)sg.b * p.B, i, mreg, p.status);
                 mreg_built = true;
@@ -819,9 +933,9 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
 
                 // tree / tail mask (prefix-only tiles skip it), then the row max of the raw scores
                 if (!(valid && k0 + kN <= sg.P)) {
-                    if (!mask_ready) {  // the masks (or parents) may come from the previous kernel
+                    if (!primary_done) {  // the masks (or parents) may come from the previous kernel
                         pdl_wait_primary();
-                        mask_ready = true;
+                        primary_done = true;
                     }
                     if (!mrow && valid && !mreg_built) {
                         row_mask_from_parents(p.parent + (size_t)sg.b * p.B, i, mreg, p.status);
@@ -923,7 +1037,6 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                 if (lane == 0) mbar_arrive(BAR(BAR_O_EMPTY + 1));
                 gx += nx;
                 kvs += n;
-                ++seg_i;
                 ++n_merge;
                 continue;
             }
@@ -948,12 +1061,17 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
             const int h = sg.g * p.G + hg;
             const size_t orow = ((size_t)sg.b * p.B + i) * p.Hq + h;
             const bool whole = sg.j0 == 0 && sg.j1 == sg.n_row;  // else a piece cut between CTAs
-            // A piece is parked for the merge kernel in fp16 (it is normalised, |O| <= max|V|),
-            // chunk-major: 8-column chunk k of row r at [slot][k][r], so a warp's 32 rows
-            // store 512 contiguous bytes per instruction.
-            const size_t slot = (2 * (size_t)blockIdx.x + (seg_i == 0 ? 0 : 1)) * 2 + x;
+            // A piece is parked in fp16 (it is normalised, |O| <= max|V|).  A CTA's only piece
+            // that continues a tile is its first segment and its only piece that starts one
+            // is its last, so the slot (2 * starts + x) is unique in the CTA and its owner is
+            // known to every other piece of the tile.
+            const int wslot = (sg.j0 == 0 ? 2 : 0) + x;
             uint4 *dst_o = reinterpret_cast<uint4 *>(p.o + orow * kHeadDim);
-            uint4 *dst_w = p.ws_o + slot * (kHeadDim / 8) * kM + row;
+            uint4 *dst_w = ws_piece_o(p.ws, (int)blockIdx.x, wslot) + row;
+            if (!primary_done) {  // a kernel before this one may still read what is written here
+                pdl_wait_primary();
+                primary_done = true;
+            }
             // 32 columns at a time: TMEM -> registers -> global
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
@@ -1007,11 +1125,29 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                 if (whole)
                     p.lse[orow] = lse_nat;
                 else
-                    p.ws_lse[slot * kM + row] = lse_nat;
+                    ws_piece_lse(p.ws, (int)blockIdx.x, wslot)[row] = lse_nat;
+            }
+            if (!whole && p.merge_in_place) {
+                // The tile's pieces come from groups k0 .. k1 (lane sg.mp of each); this warp's
+                // 32 rows count in at group k0's CTA, and the warp that lands last merges them.
+                const long long k0 = group_of(sg.su, s_total, s_groups);
+                const long long k1 = group_of(sg.su + sg.n_row - 1, s_total, s_groups);
+                uint32_t *cnt = ws_cnt(p.ws, (int)k0 * sch.NP + sg.mp) + x * 4 + (warp & 3);
+                fence_acq_rel_gpu();  // this warp's piece is visible before it is counted
+                __syncwarp();
+                uint32_t seen = 0;
+                if (lane == 0) seen = atomicAdd(cnt, 1u);
+                seen = __shfl_sync(0xffffffffu, seen, 0);
+                if (seen == (uint32_t)(k1 - k0)) {
+                    fence_acq_rel_gpu();  // every other piece counted in before: read them now
+                    if (valid)
+                        merge_pieces(p.ws, (int)k0, (int)k1, sch.NP, sg.mp, x, row,
+                                     reinterpret_cast<uint4 *>(p.o + orow * kHeadDim), p.lse + orow);
+                    if (lane == 0) *cnt = 0u;  // zero again for the next call
+                }
             }
             gx += nx;
             kvs += n;
-            ++seg_i;
         }
     }
 
@@ -1027,7 +1163,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
 #undef BAR
 }
 
-// ------------------------------------------------------------------ merge
+// ------------------------------------------------------------------ merge kernel
 
 constexpr int kMergeThreads = 128;  // 32 rows x 4 column quarters
 constexpr int kMergeSplit = kM / 32; // CTAs per M tile
@@ -1046,25 +1182,23 @@ __device__ long long sched_prefix(const Sched &s, int b_end, int lane)
 
 struct MergeParams {
     const int32_t *prefix_lens;
-    const uint4 *ws_o;
-    const float *ws_lse;
+    uint8_t *ws;
     uint16_t *o;
     float *lse;
     int nb, B, Hq, Hkv, G, NT, MT, max_pages, attn_grid;
 };
 
-// kMergeSplit CTAs per M tile (sequence, kv head, mt), each for 32 of its rows;
-// thread (warp q, lane l) owns row 32s + l and the columns 32q .. 32q+31.  The
-// attention grid's groups k0..k1 hold the pieces of an M tile whose pair tile (lane
-// mp of its unit) was cut between groups: lane mp of group k0 keeps its piece in its
-// last slot (or its first, when nothing of that lane comes before it in k0), lanes
-// mp of groups k0+1 .. k1 in their first.  lse = ln sum_u e^{lse_u},
-// O = sum_u e^{lse_u - lse} O_u, in one pass over batches of four pieces whose
-// lse and O loads are all in flight together (chunk-major partials: a warp's
-// loads are 512 contiguous bytes), with a running maximum between batches.
+// The merge of launches whose cut M tiles have many pieces (the attention kernel merges
+// in place when they have few: there one warp per 32 rows is fast enough).  kMergeSplit
+// CTAs per M tile (sequence, kv head, mt), each for 32 of its rows; thread (warp q, lane
+// l) owns row 32s + l and the columns 32q .. 32q+31.  The pieces of a tile whose pair
+// tile (lane pm of its unit) was cut come from groups k0 .. k1, group k's in CTA
+// k * NP + pm, slot 2 * (k == k0) + x.  The same combine as merge_pieces, in one pass
+// over batches of four pieces whose lse and O loads are all in flight together
+// (chunk-major partials: a warp's loads are 512 contiguous bytes).
 __global__ void __launch_bounds__(kMergeThreads) tree_attn_merge_kernel(const MergeParams mp)
 {
-    __shared__ int s_k0, s_k1, s_first0;
+    __shared__ int s_k0, s_k1;
     const int id = blockIdx.x / kMergeSplit;
     const int split = blockIdx.x % kMergeSplit;
     const int b = id / (mp.Hkv * mp.MT);
@@ -1082,39 +1216,19 @@ __global__ void __launch_bounds__(kMergeThreads) tree_attn_merge_kernel(const Me
         const long long start_b = sched_prefix(sch, b, lane);
         const int P = __ldcg(mp.prefix_lens + b);
         const int ut = unit_tiles(sch, P);
-        int k0 = 0, k1 = 0, first0 = 0;
+        int k0 = 0, k1 = 0;
         if (ut > 0 && total > 0) {
             const long long su = start_b + (long long)g * ut;  // the unit's first group item
-            const long long r1 = su + pair_tiles(sch, P, pm);   // past this pair tile's last one
             k0 = (int)group_of(su, total, G);
-            k1 = (int)group_of(r1 - 1, total, G);
-            if (k1 > k0) {
-                // Lane pm has something in group k0 before this unit unless k0 starts with
-                // this unit, or k0 starts inside the unit right before it, past the tiles
-                // this lane needs there.
-                const long long s0 = total * k0 / G;
-                first0 = 1;
-                if (s0 == su) {
-                    first0 = 0;
-                } else {
-                    int bb;
-                    long long off;
-                    sched_locate(sch, s0, lane, bb, off);
-                    const int Pb = __ldcg(mp.prefix_lens + bb);
-                    const int utb = unit_tiles(sch, Pb);
-                    const long long rem = off % utb;
-                    if (s0 - rem + utb == su && rem >= pair_tiles(sch, Pb, pm)) first0 = 0;
-                }
-            }
+            k1 = (int)group_of(su + pair_tiles(sch, P, pm) - 1, total, G);
         }
         if (lane == 0) {
             s_k0 = k0;
             s_k1 = k1;
-            s_first0 = first0;
         }
     }
     __syncthreads();
-    const int k0 = s_k0, k1 = s_k1, first0 = s_first0;
+    const int k0 = s_k0, k1 = s_k1;
     // Every CTA waits for the attention grid (so this grid never completes before it);
     // past this point the partials are complete and visible.
     pdl_wait_primary();
@@ -1123,12 +1237,6 @@ __global__ void __launch_bounds__(kMergeThreads) tree_attn_merge_kernel(const Me
     const int i = mt * mp.NT + r / mp.G;
     if (i >= mp.B) return;  // a row past the tree
 
-    // group k's lane pm is CTA k * NP + pm (several groups exist only when the grid holds NP CTAs)
-    auto slot_of = [&](int k) -> size_t {
-        return (2 * ((size_t)k * sch.NP + pm) + (k == k0 ? first0 : 0)) * 2 + x;
-    };
-    // One pass: each batch's lse and O loads are in flight together; a running
-    // maximum rescales the sums between batches.
     float m = -INFINITY, wsum = 0.f;
     float4 acc[8];
 #pragma unroll
@@ -1140,11 +1248,12 @@ __global__ void __launch_bounds__(kMergeThreads) tree_attn_merge_kernel(const Me
         for (int u = 0; u < 4; ++u) {
             const int k = kb + u;
             const bool in = k <= k1;
-            const size_t slot = slot_of(in ? k : k0);
-            l[u] = in ? __ldcg(mp.ws_lse + slot * kM + r) : -INFINITY;
-            const uint4 *src = mp.ws_o + (slot * (kHeadDim / 8) + q * 4) * kM + r;
+            const int kk = in ? k : k0;
+            const int cta = kk * sch.NP + pm, slot = (kk == k0 ? 2 : 0) + x;
+            l[u] = in ? __ldcg(ws_piece_lse(mp.ws, cta, slot) + r) : -INFINITY;
+            const uint4 *src = ws_piece_o(mp.ws, cta, slot) + (size_t)(q * 4) * kM + r;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) v[u][k] = in ? __ldcg(src + (size_t)k * kM) : make_uint4(0u, 0u, 0u, 0u);
+            for (int c = 0; c < 4; ++c) v[u][c] = in ? __ldcg(src + (size_t)c * kM) : make_uint4(0u, 0u, 0u, 0u);
         }
         const float mb = fmaxf(fmaxf(m, fmaxf(l[0], l[1])), fmaxf(l[2], l[3]));
         if (mb == -INFINITY) continue;  // no piece with a visible key yet
@@ -1162,39 +1271,32 @@ __global__ void __launch_bounds__(kMergeThreads) tree_attn_merge_kernel(const Me
             const float w = expf(l[u] - mb);  // 0 for an empty piece
             wsum += w;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float2 a = unpack_f16x2(v[u][k].x), b = unpack_f16x2(v[u][k].y);
-                const float2 c = unpack_f16x2(v[u][k].z), d = unpack_f16x2(v[u][k].w);
-                acc[2 * k].x = fmaf(w, a.x, acc[2 * k].x);
-                acc[2 * k].y = fmaf(w, a.y, acc[2 * k].y);
-                acc[2 * k].z = fmaf(w, b.x, acc[2 * k].z);
-                acc[2 * k].w = fmaf(w, b.y, acc[2 * k].w);
-                acc[2 * k + 1].x = fmaf(w, c.x, acc[2 * k + 1].x);
-                acc[2 * k + 1].y = fmaf(w, c.y, acc[2 * k + 1].y);
-                acc[2 * k + 1].z = fmaf(w, d.x, acc[2 * k + 1].z);
-                acc[2 * k + 1].w = fmaf(w, d.y, acc[2 * k + 1].w);
+            for (int c = 0; c < 4; ++c) {
+                const float2 a = unpack_f16x2(v[u][c].x), bb = unpack_f16x2(v[u][c].y);
+                const float2 d = unpack_f16x2(v[u][c].z), e = unpack_f16x2(v[u][c].w);
+                acc[2 * c].x = fmaf(w, a.x, acc[2 * c].x);
+                acc[2 * c].y = fmaf(w, a.y, acc[2 * c].y);
+                acc[2 * c].z = fmaf(w, bb.x, acc[2 * c].z);
+                acc[2 * c].w = fmaf(w, bb.y, acc[2 * c].w);
+                acc[2 * c + 1].x = fmaf(w, d.x, acc[2 * c + 1].x);
+                acc[2 * c + 1].y = fmaf(w, d.y, acc[2 * c + 1].y);
+                acc[2 * c + 1].z = fmaf(w, e.x, acc[2 * c + 1].z);
+                acc[2 * c + 1].w = fmaf(w, e.y, acc[2 * c + 1].w);
             }
         }
         m = mb;
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        acc[k].x *= inv;
-        acc[k].y *= inv;
-        acc[k].z *= inv;
-        acc[k].w *= inv;
-    }
     const size_t orow = ((size_t)b * mp.B + i) * mp.Hq + g * mp.G + r % mp.G;
     uint4 *dst = reinterpret_cast<uint4 *>(mp.o + orow * kHeadDim) + q * 4;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int c = 0; c < 4; ++c) {
         uint4 w4;
-        w4.x = pack_bf16x2(acc[2 * k].x, acc[2 * k].y);
-        w4.y = pack_bf16x2(acc[2 * k].z, acc[2 * k].w);
-        w4.z = pack_bf16x2(acc[2 * k + 1].x, acc[2 * k + 1].y);
-        w4.w = pack_bf16x2(acc[2 * k + 1].z, acc[2 * k + 1].w);
-        dst[k] = w4;
+        w4.x = pack_bf16x2(acc[2 * c].x * inv, acc[2 * c].y * inv);
+        w4.y = pack_bf16x2(acc[2 * c].z * inv, acc[2 * c].w * inv);
+        w4.z = pack_bf16x2(acc[2 * c + 1].x * inv, acc[2 * c + 1].y * inv);
+        w4.w = pack_bf16x2(acc[2 * c + 1].z * inv, acc[2 * c + 1].w * inv);
+        dst[c] = w4;
     }
     if (q == 0) mp.lse[orow] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
 }
@@ -1222,7 +1324,7 @@ static EncodeTiledFn encode_fn()
 size_t attn_workspace_bytes(int ctas, int row_tiles)
 {
     (void)row_tiles;
-    return (size_t)4 * ctas * kM * (kHeadDim * 2 + sizeof(float));  // fp16 O + fp32 LSE per row
+    return (size_t)ctas * kWsBlock;  // per CTA: counters, four fp16 O pieces and their LSEs
 }
 
 int attn_row_tiles(const tv_attn_args *a)
@@ -1230,6 +1332,35 @@ int attn_row_tiles(const tv_attn_args *a)
     const int NT = kM / (a->Hq / a->Hkv);
     return a->nb * a->Hkv * ((a->B + NT - 1) / NT);
 }
+
+struct AttnPlan {
+    int grid, unit_aligned, merge_in_place;
+};
+
+// How a call with `ctas` CTAs runs.  A launch whose units all fit the grid at once and
+// whose block table covers only a few KV tiles per unit (its length bounds every unit's)
+// gives each unit its own CTA group: no tile is cut, so nothing is merged.  Otherwise,
+// with G groups over U units a cut tile has about G / U + 1 pieces.  Under three, the
+// last piece's warp merges its 32 rows at once (measured faster: no second kernel); from
+// three on, that one warp's dependent loads at the grid's tail take longer than the merge
+// kernel, which spreads each tile over four CTAs of four warps.
+static AttnPlan attn_plan(const tv_attn_args *a, int ctas)
+{
+    const int NT = kM / (a->Hq / a->Hkv);
+    const int MT = (a->B + NT - 1) / NT;
+    const int NP = (MT + 1) / 2;
+    const long long units = (long long)a->nb * a->Hkv;
+    const long long unit_ctas = units * NP;
+    const long long max_unit_tiles = ((long long)a->max_pages * kPage + kN - 1) / kN;
+    AttnPlan pl;
+    pl.unit_aligned = (unit_ctas <= ctas && max_unit_tiles <= kAlignedMaxTiles) ? 1 : 0;
+    pl.grid = pl.unit_aligned ? (int)unit_ctas : ctas;
+    const long long groups = ctas >= NP ? ctas / NP : 1;
+    pl.merge_in_place = (pl.unit_aligned || groups < 2 * units) ? 1 : 0;
+    return pl;
+}
+
+int attn_kernel_launches(const tv_attn_args *a, int ctas) { return attn_plan(a, ctas).merge_in_place ? 1 : 2; }
 
 // The attention kernel's shared-memory opt-in, once per device.
 static cudaError_t attn_smem_opt_in()
@@ -1293,8 +1424,7 @@ int32_t launch_attn(const tv_attn_args *a, int ctas, void *workspace, cudaStream
     p.o = static_cast<uint16_t *>(a->o_d);
     p.lse = a->lse_d;
     p.status = a->dev_status_d;
-    p.ws_o = static_cast<uint4 *>(workspace);
-    p.ws_lse = reinterpret_cast<float *>(p.ws_o + (size_t)4 * ctas * kM * (kHeadDim / 8));
+    p.ws = static_cast<uint8_t *>(workspace);
     p.nb = a->nb;
     p.B = a->B;
     p.Hq = a->Hq;
@@ -1307,23 +1437,17 @@ int32_t launch_attn(const tv_attn_args *a, int ctas, void *workspace, cudaStream
     p.num_blocks = a->num_blocks;
     const float scale = a->scale > 0.f ? a->scale : 1.0f / sqrtf((float)kHeadDim);
     p.scale_log2 = scale * 1.4426950408889634f;
-    // A launch whose units all fit the grid at once and whose block table covers only a
-    // few KV tiles per unit (its length bounds every unit's) gives each unit its own CTA
-    // group: no tile is cut, so the merge kernel is not launched at all.
-    const int NP = (p.MT + 1) / 2;
-    const long long unit_ctas = (long long)a->nb * a->Hkv * NP;
-    const long long max_unit_tiles = ((long long)a->max_pages * kPage + kN - 1) / kN;
-    p.unit_aligned = (unit_ctas <= ctas && max_unit_tiles <= kAlignedMaxTiles) ? 1 : 0;
-    const int grid = p.unit_aligned ? (int)unit_ctas : ctas;
+    const AttnPlan plan = attn_plan(a, ctas);
+    p.unit_aligned = plan.unit_aligned;
+    p.merge_in_place = plan.merge_in_place;
 
     cudaError_t e = attn_smem_opt_in();
     if (e == cudaSuccess)
-        e = launch_dependent(tree_attn_kernel, dim3(grid), dim3(kThreads), kSmemBytes, stream, p);
-    if (e == cudaSuccess && !p.unit_aligned) {
+        e = launch_dependent(tree_attn_kernel, dim3(plan.grid), dim3(kThreads), kSmemBytes, stream, p);
+    if (e == cudaSuccess && !p.merge_in_place) {
         // The merge kernel may be scheduled while the attention grid drains; it waits
         // (griddepcontrol.wait) before reading partials.
-        MergeParams mp{a->prefix_lens_d, p.ws_o, p.ws_lse, p.o, p.lse, p.nb, p.B, p.Hq, p.Hkv, p.G, p.NT, p.MT,
-                       p.max_pages, ctas};
+        MergeParams mp{a->prefix_lens_d, p.ws, p.o, p.lse, p.nb, p.B, p.Hq, p.Hkv, p.G, p.NT, p.MT, p.max_pages, ctas};
         e = launch_dependent(tree_attn_merge_kernel, dim3((unsigned)(a->nb * a->Hkv * p.MT * kMergeSplit)),
                              dim3(kMergeThreads), 0, stream, mp);
     }

@@ -83,6 +83,8 @@ cudaError_t launch_selftest_wait(uint64_t limit_ns, int32_t *status, cudaStream_
 // (sequence, kv head, 128-row tile) units, and that unit count for `a`.
 size_t attn_workspace_bytes(int ctas, int row_tiles);
 int attn_row_tiles(const tv_attn_args *a);
+// Kernels launch_attn enqueues for `a` with `ctas` CTAs: 1, or 2 with the merge kernel.
+int attn_kernel_launches(const tv_attn_args *a, int ctas);
 
 // Encodes the TMA descriptors and launches the attention kernel and its merge kernel.
 // Returns TV_OK or TV_ERR_CUDA (with *cuda_err set).
