@@ -87,6 +87,16 @@ def test_attn_null_args(L):
     assert L.tv_attn_launches(None) == 0
 
 
+@pytest.mark.parametrize("kw", [dict(num_ctas=1), dict(num_ctas=152), dict(nb=4, B=256, max_pages=2064,
+                                num_blocks=8256, num_ctas=300), dict(nb=32, B=16, Hkv=4, num_ctas=7)])
+def test_attn_workspace_is_one_fixed_block_per_cta(L, kw):
+    """tv_attn's workspace is one block per CTA whatever the shape: 128 bytes of arrival
+    counters, four 32 KB fp16 partial outputs and their four 512-byte LSE rows, so a
+    block's counters sit at the same offset for every call that shares the workspace."""
+    a = _args(**kw)
+    assert L.tv_attn_workspace_size(C.byref(a)) == kw["num_ctas"] * (128 + 4 * 32768 + 4 * 512)
+
+
 @pytest.mark.parametrize("kw,launches", [
     # 4 sequences x 8 kv heads, 256-node trees (4 pair tiles per unit), 32K prefixes, 152 CTAs:
     # 38 groups over 32 units, so a split tile has about two parts and is merged in place
