@@ -295,9 +295,23 @@ __global__ void __launch_bounds__(kTreeThreads) build_tree_kernel(const float *_
             const int qh = min(min(want, kTreeCap), nh);
             if (nh > qh) {
                 if (kn[0] != 0ull) {
-                    int r = 0;
-                    for (int e = 0; e < nh; ++e) r += sh.heads[e] > kn[0];
-                    if (r == qh - 1) sh.thr = kn[0] - 1ull;
+                    // eight independent counts, so the shared-memory loads overlap
+                    const unsigned long long v = kn[0];
+                    int r0 = 0, r1 = 0, r2 = 0, r3 = 0, r4 = 0, r5 = 0, r6 = 0, r7 = 0;
+                    int e = 0;
+                    for (; e + 8 <= nh; e += 8) {
+                        r0 += sh.heads[e] > v;
+                        r1 += sh.heads[e + 1] > v;
+                        r2 += sh.heads[e + 2] > v;
+                        r3 += sh.heads[e + 3] > v;
+                        r4 += sh.heads[e + 4] > v;
+                        r5 += sh.heads[e + 5] > v;
+                        r6 += sh.heads[e + 6] > v;
+                        r7 += sh.heads[e + 7] > v;
+                    }
+                    for (; e < nh; ++e) r0 += sh.heads[e] > v;
+                    const int r = ((r0 + r1) + (r2 + r3)) + ((r4 + r5) + (r6 + r7));
+                    if (r == qh - 1) sh.thr = v - 1ull;
                 }
                 __syncthreads();
                 T = sh.thr;
