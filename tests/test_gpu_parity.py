@@ -231,6 +231,22 @@ def test_attention_workspace_reused_across_shapes():
             assert int(counters.count_nonzero()) == 0
 
 
+def test_attention_long_prefix_many_pieces():
+    """A 65536-token prefix over 8 single-tile units: one CTA per SM cuts every row tile into
+    about twenty pieces (the merge kernel's batches of four, several times over); 15 CTAs
+    (fewer groups than twice the units) merge each tile's two or three pieces in place."""
+    w = _workload(25, 1, 16, 32, 8, [65536], V=8)
+    d = DevWorkload(w)
+    mask, _ = d.mask()
+    O_ref, L_ref = oracle.attn_workload(w)
+    ws = torch.zeros(300 * ATTN_WS_BLOCK, dtype=torch.uint8, device="cuda")
+    for ctas in (0, 15):
+        O, L = tv.attn(d.q, d.k, d.v, d.bt, d.pl, mask, status=d.status, num_ctas=ctas, workspace=ws)
+        torch.cuda.synchronize()
+        assert d.status.item() == 0
+        assert_attn_close(O, L, O_ref, L_ref, w)
+
+
 def test_attention_explicit_scale():
     w = _workload(12, 1, 20, 8, 2, [77], V=8)
     d = DevWorkload(w)
