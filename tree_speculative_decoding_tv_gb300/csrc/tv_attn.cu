@@ -1101,6 +1101,9 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                         dst_o[c * 4 + q] = v;
                     }
                 } else {
+                    // evict-last: a tile's first pieces wait here while the K/V stream passes
+                    // through L2, until the merge reads them
+                    const uint64_t pol = l2_policy_evict_last();
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         uint4 v;
@@ -1108,7 +1111,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_attn_kernel(const __grid_con
                         v.y = pack_f16x2(__uint_as_float(o[q * 8 + 2]), __uint_as_float(o[q * 8 + 3]));
                         v.z = pack_f16x2(__uint_as_float(o[q * 8 + 4]), __uint_as_float(o[q * 8 + 5]));
                         v.w = pack_f16x2(__uint_as_float(o[q * 8 + 6]), __uint_as_float(o[q * 8 + 7]));
-                        dst_w[(size_t)(c * 4 + q) * kM] = v;
+                        st_global_v4_hint(dst_w + (size_t)(c * 4 + q) * kM, v, pol);
                     }
                 }
             }
