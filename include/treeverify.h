@@ -164,8 +164,9 @@ TV_API size_t tv_attn_workspace_size(const tv_attn_args *args);
  * 16-byte aligned.  It must be zero-filled (cudaMemset) before its first call;
  * besides the partials it holds arrival counters, at offsets that do not
  * depend on the arguments, which every call leaves zero, so a workspace can
- * serve calls of any shape after that.  A call that reports TV_ERR_TIMEOUT
- * may leave counters behind: zero the workspace again before reusing it.
+ * serve calls of any shape after that.  A call whose dev_status_d reports
+ * TV_ERR_TIMEOUT may leave counters behind: zero the workspace again before
+ * reusing it.
  * Concurrent calls need separate workspaces.
  *
  * Ordering: the attention kernel is launched as a programmatic dependent of the
