@@ -159,6 +159,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int3
         : "memory");
 }
 
+// The same copy under an L2 cache policy (createpolicy).
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void *tmap, int32_t c0, int32_t c1, uint32_t bar,
+                                                 uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], "
+        "[%4], %5;" ::"r"(dst),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(bar), "l"(pol)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, int32_t c0, int32_t c1, int32_t c2,
                                             int32_t c3, uint32_t bar)
 {
@@ -194,6 +205,13 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last()
 {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+// An L2 cache policy that gives up the lines it is applied to first.
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     return pol;
 }
 __device__ __forceinline__ void st_global_v4_hint(uint4 *p, uint4 v, uint64_t pol)
